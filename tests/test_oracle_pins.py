@@ -1,0 +1,309 @@
+"""Pins for the fp64 oracle against facts that do not come from the oracle itself.
+
+Each test fixes one property by a closed form, a hand-worked case, an
+invariant, explicit bit patterns, or a textbook routine, chosen so that a
+plausible mistake (a dropped term, wrong sign, wrong nibble order, transposed
+operand, wrong tie-break) fails at least one of them.
+"""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+from skinny_gemm_bit_gb300 import synth
+
+ONE = 0x3F80  # bf16 1.0
+
+
+def bf16(v):
+    return synth.f32_to_bf16_bits(np.asarray(v, dtype=np.float32))
+
+
+def weights(wq, scales, biases, N, K, bits):
+    return {"wq": np.asarray(wq, np.uint32), "scales": np.asarray(scales, np.uint16),
+            "biases": np.asarray(biases, np.uint16), "N": N, "K": K, "bits": bits}
+
+
+# ---------------------------------------------------------------- unpack order
+
+def test_unpack_4bit_explicit_words():
+    # element j of a word sits in bits [4j, 4j+4): 0x76543210 holds 0..7 in order
+    wq = np.array([[0x76543210, 0xFEDCBA98]], dtype=np.uint32)
+    q = oracle.unpack(wq, 1, 16, 4)
+    assert q.tolist() == [list(range(16))]
+
+
+def test_unpack_8bit_explicit_words():
+    wq = np.array([[0x03020100, 0xFFFEFDFC]], dtype=np.uint32)
+    q = oracle.unpack(wq, 1, 8, 8)
+    assert q.tolist() == [[0, 1, 2, 3, 252, 253, 254, 255]]
+
+
+def test_unpack_rows_are_independent():
+    wq = np.array([[0x11111111], [0x22222222], [0xF0F0F0F0]], dtype=np.uint32)
+    q = oracle.unpack(wq, 3, 8, 4)
+    assert q.tolist() == [[1] * 8, [2] * 8, [0, 15] * 4]
+
+
+# ---------------------------------------------------------------- closed forms
+
+@pytest.mark.parametrize("c", [0, 1, 7, 15])
+def test_constant_code_unit_scale_ones(c):
+    # q = c everywhere, s = 1, b = 0, x = 1  ->  y = K * c exactly
+    N, K = 5, 256
+    wq = np.full((N, K // 8), c * 0x11111111, dtype=np.uint32)
+    w = weights(wq, np.full((N, K // 64), ONE), np.zeros((N, K // 64)), N, K, 4)
+    y, ad = oracle.qlinear(np.ones((1, K)), w)
+    assert np.all(y == K * c)
+    assert np.all(ad == K * c)
+
+
+def test_bias_only():
+    # s = 0, b = beta  ->  y = beta * sum(x)
+    N, K = 3, 128
+    wq = np.full((N, K // 8), 0x9ABCDEF0, dtype=np.uint32)
+    beta = bf16([-0.375, 0.5, 2.0])
+    w = weights(wq, np.zeros((N, K // 64)), np.repeat(beta[:, None], K // 64, 1), N, K, 4)
+    y, _ = oracle.qlinear(np.ones((2, K)), w)
+    assert np.all(y == np.array([-0.375, 0.5, 2.0]) * K)
+
+
+def test_constant_code_power_of_two_scale_random_x():
+    # q = 11, s = 2^-j, b = 0, random x  ->  y = s * 11 * sum(x)
+    rng = np.random.default_rng(7)
+    N, K = 6, 512
+    wq = np.full((N, K // 8), 11 * 0x11111111, dtype=np.uint32)
+    s = np.array([2.0 ** -j for j in range(N)], dtype=np.float32)
+    w = weights(wq, np.repeat(bf16(s)[:, None], K // 64, 1), np.zeros((N, K // 64)), N, K, 4)
+    x = rng.standard_normal((3, K))
+    y, _ = oracle.qlinear(x, w)
+    expect = x.sum(axis=1)[:, None] * (11 * s.astype(np.float64))[None, :]
+    np.testing.assert_allclose(y, expect, rtol=1e-12, atol=1e-12)
+
+
+def test_8bit_constant_code():
+    N, K = 2, 128
+    wq = np.full((N, K // 4), 0xFFFFFFFF, dtype=np.uint32)
+    w = weights(wq, np.full((N, K // 64), ONE), np.zeros((N, K // 64)), N, K, 8)
+    y, _ = oracle.qlinear(np.ones((1, K)), w)
+    assert np.all(y == 255 * K)
+
+
+def test_hand_case_4x64x8():
+    # q[n][k] = (n + k) mod 16 -> every row holds each code 4 times, sum 480;
+    # x[m][k] = m + 1, s_n = 2^-n, b_n = -n/8 (all exact in bf16):
+    # y[m][n] = (m + 1) * (480 * 2^-n - 64 * n / 8) = (m + 1) * (480 * 2^-n - 8 n)
+    M, K, N = 4, 64, 8
+    q = np.array([[(n + k) % 16 for k in range(K)] for n in range(N)])
+    s = bf16([2.0 ** -n for n in range(N)])[:, None]
+    b = bf16([-n / 8 for n in range(N)])[:, None]
+    w = weights(synth.pack_codes(q, 4), s, b, N, K, 4)
+    x = np.array([[m + 1] * K for m in range(M)], dtype=np.float64)
+    y, _ = oracle.qlinear(x, w)
+    expect = np.array([[(m + 1) * (480 * 2.0 ** -n - 8 * n) for n in range(N)] for m in range(M)])
+    assert np.array_equal(y, expect)
+
+
+def test_one_hot_rows_reveal_codes_scales_and_biases():
+    # x = e_k picks column k of W: y[k][n] = s_n * ((n + k) mod 16) + b_n
+    K, N = 128, 16
+    q = np.array([[(n + k) % 16 for k in range(K)] for n in range(N)])
+    s = np.array([[0.25, 2.0]] * N, dtype=np.float32)           # group 0, group 1
+    b = np.array([[-1.0 - n / 4, 3.0] for n in range(N)], dtype=np.float32)
+    w = weights(synth.pack_codes(q, 4), bf16(s), bf16(b), N, K, 4)
+    y, _ = oracle.qlinear(np.eye(K), w)
+    expect = np.array([[s[n, k // 64] * ((n + k) % 16) + b[n, k // 64] for n in range(N)]
+                       for k in range(K)])
+    assert np.array_equal(y, expect)
+
+
+# ---------------------------------------------------------------- invariants
+
+def _random_case(seed, M=3, K=256, N=24, bits=4):
+    rng = np.random.default_rng(seed)
+    w = synth.quant_weights(rng, N, K, bits)
+    x = oracle.bf16_to_f64(synth.activations(rng, M, K))
+    return x, w
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+def test_joint_group_permutation_leaves_y(bits):
+    x, w = _random_case(3, bits=bits)
+    K = w["K"]
+    G = K // 64
+    per = 32 // bits
+    perm = np.random.default_rng(4).permutation(G)
+    words_per_group = 64 // per
+    wq = w["wq"].reshape(w["N"], G, words_per_group)[:, perm].reshape(w["N"], -1)
+    w2 = dict(w, wq=wq, scales=w["scales"][:, perm], biases=w["biases"][:, perm])
+    x2 = x.reshape(x.shape[0], G, 64)[:, perm].reshape(x.shape[0], K)
+    y1, a1 = oracle.qlinear(x, w)
+    y2, a2 = oracle.qlinear(x2, w2)
+    np.testing.assert_allclose(y2, y1, rtol=1e-12, atol=1e-12 * np.abs(a1).max())
+
+
+def test_row_permutation_permutes_y():
+    x, w = _random_case(5)
+    perm = np.random.default_rng(6).permutation(w["N"])
+    w2 = dict(w, wq=w["wq"][perm], scales=w["scales"][perm], biases=w["biases"][perm])
+    y1, _ = oracle.qlinear(x, w)
+    y2, _ = oracle.qlinear(x, w2)
+    assert np.array_equal(y2, y1[:, perm])
+
+
+def test_rows_of_x_are_independent_and_linear():
+    x, w = _random_case(8, M=4)
+    y, _ = oracle.qlinear(x, w)
+    for m in range(4):
+        ym, _ = oracle.qlinear(x[m:m + 1], w)
+        assert np.array_equal(ym[0], y[m])
+    y2, _ = oracle.qlinear(2.0 * x, w)
+    assert np.array_equal(y2, 2.0 * y)
+
+
+def test_dequant_against_explicit_affine_values():
+    # scale 0.5, bias -4 on codes 0..15 gives -4, -3.5, ..., 3.5
+    wq = np.array([[0x76543210, 0xFEDCBA98] * 4], dtype=np.uint32)
+    w = weights(wq, [[bf16(0.5)]], [[bf16(-4.0)]], 1, 64, 4)
+    d = oracle.dequant(w)
+    assert d[0, :16].tolist() == [-4 + 0.5 * i for i in range(16)]
+
+
+# ---------------------------------------------------------------- rmsnorm
+
+def test_rmsnorm_constant_row():
+    K = 64
+    g = np.linspace(0.5, 1.5, K)
+    for c in (-3.0, 0.25, 7.0):
+        xn = oracle.rmsnorm(np.full((1, K), c), g, 0.0)
+        np.testing.assert_allclose(xn[0], math.copysign(1.0, c) * g, rtol=1e-15)
+        eps = 1e-2
+        xn = oracle.rmsnorm(np.full((1, K), c), g, eps)
+        np.testing.assert_allclose(xn[0], c / math.sqrt(c * c + eps) * g, rtol=1e-15)
+
+
+def test_rmsnorm_three_four():
+    # mean of squares of (3, 4) is 12.5
+    xn = oracle.rmsnorm(np.array([[3.0, 4.0]]), np.array([1.0, 2.0]), 0.0)
+    np.testing.assert_allclose(xn[0], [3 / math.sqrt(12.5), 8 / math.sqrt(12.5)], rtol=1e-15)
+
+
+def test_rmsnorm_scale_invariant_without_eps():
+    x = np.random.default_rng(1).standard_normal((2, 96))
+    g = np.ones(96)
+    np.testing.assert_allclose(oracle.rmsnorm(5.0 * x, g, 0.0), oracle.rmsnorm(x, g, 0.0), rtol=1e-14)
+
+
+# ---------------------------------------------------------------- swiglu
+
+def test_swiglu_closed_forms():
+    ln3 = math.log(3.0)
+    g = np.array([0.0, ln3, -ln3, 1000.0, -1000.0, 2.0])
+    u = np.array([5.0, 2.0, 2.0, 3.0, 3.0, -1.0])
+    h = oracle.swiglu(g, u)
+    # sigmoid(ln 3) = 3/4, sigmoid(-ln 3) = 1/4
+    np.testing.assert_allclose(h[:3], [0.0, 2 * 0.75 * ln3, -2 * 0.25 * ln3], rtol=1e-15, atol=0)
+    assert h[3] == 3000.0
+    assert h[4] == 0.0 or abs(h[4]) < 1e-300
+    np.testing.assert_allclose(h[5], -2.0 / (1.0 + math.exp(-2.0)), rtol=1e-15)
+
+
+# ---------------------------------------------------------------- routing
+
+def test_topk_matches_sorted_with_ties():
+    rng = np.random.default_rng(11)
+    # small integers force many exact ties
+    logits = rng.integers(-3, 4, size=(6, 128)).astype(np.float32)
+    idx, w = oracle.topk_softmax(logits, 8)
+    for m in range(6):
+        order = sorted(range(128), key=lambda e: (-float(logits[m, e]), e))[:8]
+        assert idx[m].tolist() == order
+        np.testing.assert_allclose(w[m].sum(), 1.0, rtol=1e-15)
+        assert np.all(np.diff(w[m]) <= 0)
+
+
+def test_topk_softmax_closed_forms():
+    logits = np.full((1, 16), -5.0, dtype=np.float32)
+    logits[0, 3] = 1.0
+    logits[0, 9] = 1.0 - math.log(2.0)
+    idx, w = oracle.topk_softmax(logits, 2)
+    assert idx.tolist() == [[3, 9]]
+    np.testing.assert_allclose(w[0], [2 / 3, 1 / 3], rtol=1e-7)
+    idx, w = oracle.topk_softmax(np.zeros((1, 128), np.float32), 8)
+    assert idx.tolist() == [list(range(8))]
+    np.testing.assert_allclose(w, np.full((1, 8), 1 / 8), rtol=1e-15)
+
+
+# ---------------------------------------------------------------- moe / chain
+
+def _tiny_moe(seed, identical=False, E=6, H=128, I=64, M=3, top_k=2):
+    rng = np.random.default_rng(seed)
+    x = oracle.bf16_to_f64(synth.activations(rng, M, H))
+    logits = synth.router_logits(rng, M, E)
+    mats = {}
+    for name, (n, k) in {"gate": (I, H), "up": (I, H), "down": (H, I)}.items():
+        w = synth.quant_weights(rng, n, k, 4, batch=E)
+        if identical:
+            for key in ("wq", "scales", "biases"):
+                w[key] = np.repeat(w[key][:1], E, axis=0)
+        mats[name] = w
+    return x, logits, mats, top_k
+
+
+def test_moe_with_identical_experts_is_the_dense_mlp():
+    x, logits, mats, top_k = _tiny_moe(21, identical=True)
+    out = oracle.moe(x, logits, mats["gate"], mats["up"], mats["down"], top_k)
+    gu = oracle.gateup(x, oracle.expert(mats["gate"], 0), oracle.expert(mats["up"], 0))
+    dense, _ = oracle.qlinear(gu["h"], oracle.expert(mats["down"], 0))
+    np.testing.assert_allclose(out["y"], dense, rtol=1e-12, atol=1e-12 * np.abs(dense).max())
+
+
+def test_moe_top1_is_the_selected_expert():
+    x, logits, mats, _ = _tiny_moe(22)
+    out = oracle.moe(x, logits, mats["gate"], mats["up"], mats["down"], 1)
+    for m in range(x.shape[0]):
+        e = int(np.argmax(logits[m]))
+        assert out["idx"][m, 0] == e and out["w"][m, 0] == 1.0
+        gu = oracle.gateup(x[m:m + 1], oracle.expert(mats["gate"], e), oracle.expert(mats["up"], e))
+        d, _ = oracle.qlinear(gu["h"], oracle.expert(mats["down"], e))
+        assert np.array_equal(out["y"][m], d[0])
+
+
+def _tiny_decoder(seed):
+    return synth.decoder(seed=seed, n_layers=2, d_model=128, d_ff=192, n_q_heads=2,
+                         n_kv_heads=1, head_dim=64, vocab=320, M=2)
+
+
+def _oracle_layers(cfg):
+    layers = []
+    for L in cfg["layers"]:
+        layers.append({k: (oracle.bf16_to_f64(v) if k.endswith("norm") else v) for k, v in L.items()})
+    return layers
+
+
+def test_decode_step_with_silent_o_and_down_is_the_readout_of_the_input():
+    cfg = _tiny_decoder(31)
+    for L in cfg["layers"]:
+        for name in ("o", "down"):
+            L[name]["scales"][:] = 0
+            L[name]["biases"][:] = 0
+    x = oracle.bf16_to_f64(cfg["x"])
+    fn = oracle.bf16_to_f64(cfg["final_norm"])
+    out = oracle.decode_step(x, _oracle_layers(cfg), fn, cfg["readout"], cfg["dims"]["q_dim"])
+    direct, _ = oracle.qlinear(oracle.rmsnorm(x, fn, 1e-6), cfg["readout"])
+    assert np.array_equal(out["logits"], direct)
+
+
+def test_decode_step_ignores_k_and_v_rows():
+    cfg = _tiny_decoder(32)
+    x = oracle.bf16_to_f64(cfg["x"])
+    fn = oracle.bf16_to_f64(cfg["final_norm"])
+    q_dim = cfg["dims"]["q_dim"]
+    a = oracle.decode_step(x, _oracle_layers(cfg), fn, cfg["readout"], q_dim)
+    for L in cfg["layers"]:
+        L["qkv"]["wq"][q_dim:] ^= np.uint32(0x5A5A5A5A)
+        L["qkv"]["scales"][q_dim:] = bf16(0.75)
+    b = oracle.decode_step(x, _oracle_layers(cfg), fn, cfg["readout"], q_dim)
+    assert np.array_equal(a["logits"], b["logits"])
+    assert not np.array_equal(a["stages"][0]["qkv"][:, q_dim:], b["stages"][0]["qkv"][:, q_dim:])
