@@ -1,0 +1,274 @@
+/*
+ * tfq.h -- C ABI of libtfq.so: 4/8-bit group-quantised decode projections on
+ * NVIDIA GB300 (sm_103a).
+ *
+ * What is computed (all entry points):
+ *
+ *   y[m][n] = sum_k x[m][k] * w[n][k],   w[n][k] = scale[n][k/64] * q[n][k] + bias[n][k/64]
+ *
+ * over MLX affine group-quantised weights: q in [0, 2^bits), one bf16 scale and
+ * one bf16 bias per 64 consecutive K elements, q packed 32/bits values per
+ * uint32 along K (uzu page, "Internals 1: models are assembled from
+ * configuration", weight_matrix row: MLX 4/8-bit originals consumed as-is;
+ * TensorFold page, box smoke-test table, "info" row: "4-bit group 64"). M is 1
+ * (decode) to 8 (an 8-row speculative verify block; Husky page, "Limits of
+ * plain writing and how editing is accelerated": 8-token blocks are verified at
+ * about 1.5x the cost of one token).
+ *
+ * Conventions shared by every call:
+ *   - Pointers named x, y, h, logits, residual, gamma, ws, packed and the
+ *     wq/scales/biases inputs of the packer are DEVICE pointers owned by the
+ *     caller. tf_qweight / tf_decoder_desc structs are HOST memory, read during
+ *     the call only.
+ *   - bf16 values are passed as uint16_t bit patterns. Activation matrices are
+ *     row-major with the stated leading dimension (elements).
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *     Calls are asynchronous on it: they enqueue kernels and return. They never
+ *     allocate, synchronise or print, so a sequence of calls can be captured
+ *     into a CUDA graph. Exceptions (they synchronise): tf_qweight_check,
+ *     tf_workspace_status.
+ *   - Workspaces: each run entry point has a *_workspace_bytes query. The
+ *     workspace must be zero-filled once before its first use (every call
+ *     leaves it in the state it found it); one workspace must not be used by
+ *     two calls that may run concurrently.
+ *   - Return value: TF_OK or a TF_E_* status. Host-side validation happens
+ *     before anything is enqueued; on error nothing is enqueued.
+ *     tf_last_error() gives a message for the calling thread's last error.
+ *     Device-side failures (a bounded wait that ran out) are recorded in the
+ *     workspace and read with tf_workspace_status.
+ */
+#ifndef TFQ_H
+#define TFQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define TF_OK 0
+#define TF_E_INVALID_ARG 1        /* null pointer, bad size, bad dtype, misaligned pointer */
+#define TF_E_UNSUPPORTED_SHAPE 2  /* shape outside what the kernels implement (e.g. M > 8) */
+#define TF_E_WORKSPACE_TOO_SMALL 3
+#define TF_E_BAD_PACK 4           /* descriptor / packed header mismatch, stale pack */
+#define TF_E_CUDA 5               /* a CUDA runtime call failed; see tf_last_error */
+#define TF_E_TIMEOUT 6            /* a bounded device-side wait gave up */
+
+#define TF_DTYPE_BF16 0
+#define TF_DTYPE_F32 1
+
+/* run flags */
+#define TF_RUN_PDL 1u  /* the caller asserts that the kernel enqueued just before
+                          this call on `stream` does not write this call's
+                          weights: the first kernel may then be launched with
+                          programmatic dependent launch and stream its weights
+                          while that kernel finishes. */
+
+#define TF_QWEIGHT_MAGIC 0x31515446u /* "TFQ1" */
+#define TF_PACK_VERSION 1u
+#define TF_PACK_HEADER_BYTES 256
+
+/* Host-side descriptor of a packed weight buffer, filled by tf_qlinear_pack. */
+typedef struct tf_qweight {
+    uint32_t magic;        /* TF_QWEIGHT_MAGIC once filled by tf_qlinear_pack */
+    uint32_t version;      /* TF_PACK_VERSION */
+    int32_t bits;          /* 4 or 8 */
+    int32_t group;         /* 64 */
+    int64_t batch;         /* number of matrices (experts); 1 for a plain projection */
+    int64_t N;             /* output rows per matrix */
+    int64_t K;             /* input columns per matrix */
+    int64_t n_pad;         /* N rounded up to a multiple of 16 */
+    int64_t tile_bytes;    /* bytes of one 16-row x 64-column tile (576 for 4-bit, 1088 for 8-bit) */
+    int64_t matrix_bytes;  /* bytes of one packed matrix (tiles only) */
+    const void* data;      /* device pointer: start of the packed buffer (header first) */
+} tf_qweight;
+
+/* ---------------------------------------------------------------- status */
+
+/* Name of a status code ("TF_OK", "TF_E_INVALID_ARG", ...). Never NULL. */
+const char* tf_status_str(int status);
+/* Message describing the calling thread's most recent error ("" if none). */
+const char* tf_last_error(void);
+/* Library version (major*10000 + minor*100 + patch). */
+int tf_version(void);
+
+/* ---------------------------------------------------------------- packing */
+
+/*
+ * Bytes of the packed buffer for `batch` matrices of N x K at `bits` with
+ * `group`. Returns 0 for an unsupported combination (bits not 4/8, group not
+ * 64, K not a multiple of 64, N < 1, batch < 1).
+ */
+size_t tf_qlinear_packed_bytes(int64_t batch, int64_t N, int64_t K, int bits, int group);
+
+/*
+ * Repack MLX-layout weights into the kernels' tile order (Husky page, "Four
+ * implementation elements of MSI": 4-bit weights are stored in the order the
+ * kernel reads them, so that nothing is converted at load time).
+ *   wq      uint32 [batch][N][K*bits/32]; element j of a word in bits [bits*j, bits*j+bits)
+ *   scales  bf16   [batch][N][K/group]
+ *   biases  bf16   [batch][N][K/group]
+ *   packed  output, `packed_bytes` >= tf_qlinear_packed_bytes(...), 16-byte aligned
+ *   desc    output host descriptor; desc->data = packed
+ * Requirements: bits in {4, 8}, group == 64, K % 64 == 0, N >= 1, batch >= 1.
+ * The kernel reads the inputs and writes `packed` on `stream`; the inputs may be
+ * freed once the stream has passed this point.
+ */
+int tf_qlinear_pack(const uint32_t* wq, const uint16_t* scales, const uint16_t* biases,
+                    int64_t batch, int64_t N, int64_t K, int bits, int group,
+                    void* packed, size_t packed_bytes, tf_qweight* desc, void* stream);
+
+/*
+ * Inverse of tf_qlinear_pack: write the MLX-layout arrays back out of a packed
+ * buffer (same shapes as the packer's inputs). Used to prove the packing is a
+ * lossless permutation.
+ */
+int tf_qlinear_unpack_debug(const tf_qweight* w, uint32_t* wq, uint16_t* scales, uint16_t* biases,
+                            void* stream);
+
+/*
+ * Read the header at w->data back to the host and compare it with the
+ * descriptor (magic, version, shape). Synchronises `stream`. TF_E_BAD_PACK on
+ * mismatch.
+ */
+int tf_qweight_check(const tf_qweight* w, void* stream);
+
+/* ---------------------------------------------------------------- projections */
+
+/*
+ * y[m][n] = residual[m][n] + sum_k xn[m][k] * w[n][k] for m < M, n < N, where
+ * xn = x, or, when rms_gamma != NULL, the RMSNorm prologue
+ * xn[m][k] = x[m][k] / sqrt(mean_k(x[m][k]^2) + rms_eps) * gamma[k], rounded to
+ * bf16 (Husky page, "Four implementation elements of MSI": the preceding
+ * normalisation is merged into each projection kernel).
+ *   w          packed weights (batch must be 1)
+ *   x          bf16 [M][ldx], ldx >= K, ldx a multiple of 8, 16-byte aligned
+ *   M          1..8
+ *   rms_gamma  bf16 [K] or NULL, 16-byte aligned (whole rows are staged on chip: K up to ~6000)
+ *   residual   bf16 [M][ldr] or NULL (ldr = N when given: residual is [M][N])
+ *   y          [M][N] of y_dtype (TF_DTYPE_BF16: round to nearest even; TF_DTYPE_F32)
+ *   ws         workspace of tf_qlinear_workspace_bytes(w, M) bytes
+ */
+size_t tf_qlinear_workspace_bytes(const tf_qweight* w, int64_t M);
+int tf_qlinear_run(const tf_qweight* w, const uint16_t* x, int64_t ldx, int64_t M,
+                   const uint16_t* rms_gamma, float rms_eps, const uint16_t* residual,
+                   void* y, int y_dtype, void* ws, size_t ws_bytes, unsigned flags, void* stream);
+
+/*
+ * Gate and up together with a SwiGLU epilogue (Husky page, "Four
+ * implementation elements of MSI": gate and up projections are processed
+ * together; the preceding normalisation is merged in):
+ *   h[m][n] = silu(g[m][n]) * u[m][n],  g = xn . gate^T,  u = xn . up^T,
+ *   silu(g) = g / (1 + exp(-g)); xn as in tf_qlinear_run.
+ *   gate, up   packed, same N and K, batch 1
+ *   h          bf16 [M][N]
+ */
+size_t tf_qmlp_gateup_workspace_bytes(const tf_qweight* gate, const tf_qweight* up, int64_t M);
+int tf_qmlp_gateup_run(const tf_qweight* gate, const tf_qweight* up, const uint16_t* x, int64_t ldx,
+                       int64_t M, const uint16_t* rms_gamma, float rms_eps, uint16_t* h,
+                       void* ws, size_t ws_bytes, unsigned flags, void* stream);
+
+/*
+ * Mixture-of-experts layer with per-row expert gathering (uzu page,
+ * "Internals 1" table, mlp row: MixtureOfExperts with a routing function):
+ *   idx[m][0..top_k) = the top_k experts by router logit (descending; equal
+ *                      logits: lower expert index first)
+ *   w[m][j]          = softmax over the top_k selected logits
+ *   y[m]             = sum_j w[m][j] * down_e(silu(gate_e x[m]) * up_e x[m]),  e = idx[m][j]
+ * Every selected expert's weights are read once per call, however many rows
+ * chose it; the weighted sum runs in slot order j (deterministic).
+ *   gate, up       packed, batch = E experts of [I][H]
+ *   down           packed, batch = E experts of [H][I]
+ *   router_logits  fp32 [M][E]
+ *   x              bf16 [M][H] (row stride H)
+ *   y              bf16 [M][H]
+ *   topk_idx       int32 [M][top_k] out
+ *   topk_w         fp32  [M][top_k] out
+ * Limits: 1 <= M <= 8, 1 <= top_k <= 8, E <= 1024.
+ */
+size_t tf_qmoe_workspace_bytes(const tf_qweight* gate, const tf_qweight* up, const tf_qweight* down,
+                               int64_t M, int top_k);
+int tf_qmoe_run(const tf_qweight* gate, const tf_qweight* up, const tf_qweight* down,
+                const float* router_logits, int64_t M, int top_k, const uint16_t* x, uint16_t* y,
+                int32_t* topk_idx, float* topk_w, void* ws, size_t ws_bytes, unsigned flags,
+                void* stream);
+
+/* ---------------------------------------------------------------- decoder step */
+
+/* One decoder layer's projections; gammas are bf16 [d_model] device pointers. */
+typedef struct tf_decoder_layer {
+    tf_qweight qkv;             /* [q_dim + 2*kv_dim][d_model] : q | k | v */
+    tf_qweight o;               /* [d_model][q_dim] */
+    tf_qweight gate;            /* [d_ff][d_model] */
+    tf_qweight up;              /* [d_ff][d_model] */
+    tf_qweight down;            /* [d_model][d_ff] */
+    const uint16_t* attn_norm;  /* RMSNorm gamma ahead of qkv */
+    const uint16_t* mlp_norm;   /* RMSNorm gamma ahead of gate/up */
+} tf_decoder_layer;
+
+typedef struct tf_decoder_desc {
+    int32_t n_layers;
+    int64_t d_model, d_ff, q_dim, kv_dim, vocab;
+    float eps;                        /* RMSNorm epsilon */
+    const tf_decoder_layer* layers;   /* HOST array [n_layers] */
+    const uint16_t* final_norm;       /* bf16 [d_model] */
+    tf_qweight readout;               /* [vocab][d_model] (tied embedding) */
+} tf_decoder_desc;
+
+/*
+ * The per-token weight stream of a dense decoder, attention excluded (Husky
+ * page, "Four implementation elements of MSI": a layer is four consecutive
+ * kernels; "Experiments with a full-step megakernel": what pays is overlapping
+ * the next stage's weight loads with the current stage). Per layer, in order:
+ *   qkv = rmsnorm(h, attn_norm) . Wqkv^T            [M][q_dim + 2 kv_dim]
+ *   h1  = h + qkv[:, :q_dim] . Wo^T                  (q stands in for the attention output)
+ *   a   = silu(rmsnorm(h1, mlp_norm) . Wg^T) * (rmsnorm(h1, mlp_norm) . Wu^T)
+ *   h   = h1 + a . Wd^T
+ * then logits = rmsnorm(h, final_norm) . Wreadout^T.
+ *   x        bf16 [M][d_model], the residual stream entering layer 0
+ *   logits   bf16 [M][vocab]
+ *   debug    NULL, or bf16 scratch of tf_decode_step_debug_elems(d, M) elements
+ *            that receives every intermediate: per layer [qkv | h1 | a | h]
+ *            blocks of M x (q_dim+2kv_dim), M x d_model, M x d_ff, M x d_model.
+ */
+size_t tf_decode_step_workspace_bytes(const tf_decoder_desc* d, int64_t M);
+size_t tf_decode_step_debug_elems(const tf_decoder_desc* d, int64_t M);
+int tf_decode_step_run(const tf_decoder_desc* d, const uint16_t* x, int64_t M, uint16_t* logits,
+                       void* ws, size_t ws_bytes, uint16_t* debug, unsigned flags, void* stream);
+
+/* ---------------------------------------------------------------- diagnostics */
+
+/*
+ * Read the device status word of a workspace (offset 0): TF_OK, or the status
+ * of a device-side failure (TF_E_TIMEOUT) recorded by a call that used it,
+ * which is then cleared. Synchronises `stream`.
+ */
+int tf_workspace_status(void* ws, void* stream);
+
+/*
+ * Run one kernel whose bounded wait on a shared-memory barrier is never
+ * satisfied, with a limit of `limit_ns` nanoseconds, so that the timeout path
+ * can be exercised without hanging the GPU. Records TF_E_TIMEOUT in `ws` (read
+ * it with tf_workspace_status). `ws` needs 256 bytes.
+ */
+int tf_selftest_wait_timeout(void* ws, uint64_t limit_ns, void* stream);
+
+/*
+ * Tuning override for the launch planner: key is one of TF_TUNE_*; value < 0
+ * restores the planner's own choice. Process-wide; not thread-safe against
+ * concurrent run calls.
+ */
+#define TF_TUNE_ROWBLOCKS 0   /* 16-row blocks processed side by side per round (1, 2, 4, 8, 16) */
+#define TF_TUNE_SPLITK 1      /* K splits (must divide K / 64) */
+#define TF_TUNE_STAGE_GROUPS 2 /* 64-column groups per pipeline stage */
+#define TF_TUNE_STAGES 3      /* pipeline depth (ring slots per worker in warp mode) */
+#define TF_TUNE_WARPS 4       /* warp mode: consumer warps per CTA (1..16) */
+#define TF_TUNE_MODE 5        /* 1: lock-step teams, 2: warp workers */
+int tf_tune_set(int key, int value);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TFQ_H */

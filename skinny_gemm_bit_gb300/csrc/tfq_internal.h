@@ -1,0 +1,133 @@
+// Internal definitions shared by the CUDA translation units of libtfq.so.
+#pragma once
+
+#include <cstdint>
+#include <cstddef>
+#include <cuda_runtime.h>
+
+#include "tfq.h"
+
+namespace tfq {
+
+constexpr int kGroup = 64;
+constexpr int kRowsPerBlock = 16;             // rows of one tile (MMA M dimension)
+constexpr int kMaxM = 8;                      // activation rows (MMA N dimension)
+constexpr int kConsumerWarps = 16;            // compute warps per CTA (plus one producer warp)
+constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kMaxStages = 8;
+constexpr int kMaxSlots = 64;                 // MoE: distinct experts per call (M * top_k <= 64)
+constexpr uint64_t kDefaultWaitLimitNs = 2000000000ull;  // 2 s
+
+__host__ __device__ constexpr int tile_bytes_for(int bits) { return bits == 4 ? 576 : 1088; }
+__host__ __device__ constexpr int tile_q_bytes_for(int bits) { return bits == 4 ? 512 : 1024; }
+
+// Device header written at the start of every packed buffer.
+struct PackHeader {
+    uint32_t magic, version;
+    int32_t bits, group;
+    int64_t batch, N, K, n_pad, tile_bytes, matrix_bytes;
+    uint8_t reserved[TF_PACK_HEADER_BYTES - 8 * 8];
+};
+static_assert(sizeof(PackHeader) == TF_PACK_HEADER_BYTES, "header size");
+
+// MoE routing table, written by the router kernel into the workspace.
+struct MoeSlot {
+    int32_t expert;
+    int32_t count;           // rows routed to this expert (1..8)
+    int32_t rows[kMaxM];     // activation row of each column
+    int32_t js[kMaxM];       // top-k slot of each column
+};
+struct MoeMeta {
+    int32_t n_active;
+    int32_t pad[15];
+    MoeSlot slot[kMaxSlots];
+    int32_t inv[kMaxM * 8];  // (m, j) -> slot * 8 + column
+    float w[kMaxM * 8];      // routing weight of (m, j)
+};
+
+// Everything the projection kernel needs; passed by value as a grid constant.
+struct QProjParams {
+    const uint8_t* w0;       // first tile of matrix 0 (gate, or the only matrix)
+    const uint8_t* w1;       // first tile of matrix 1 (up), dual mode
+    int64_t matrix_bytes;    // expert stride (MoE)
+    int n_rb;                // 16-row blocks per matrix
+    int groups;              // K / 64
+    int S;                   // K splits (S divides groups)
+    int Gs;                  // groups per split
+    int N;                   // valid output rows
+    int K;
+    const uint16_t* x;
+    int64_t ldx;
+    int M;                   // activation rows (non-MoE)
+    int64_t x_slot_stride;   // MoE, gather == 0: x offset of a problem (elements)
+    int gather;              // MoE: x row of column j is meta->slot[p].rows[j]
+    const uint16_t* gamma;   // RMSNorm weight or nullptr
+    float eps;
+    const uint16_t* residual;
+    int64_t ldr;
+    void* y;
+    int64_t ldy;
+    int y_f32;
+    int64_t y_slot_stride;   // MoE: y offset of a problem (elements)
+    const MoeMeta* meta;     // MoE routing table or nullptr
+    int P;                   // problems (1 unless MoE, whose count comes from meta)
+    int C;                   // CTAs in the persistent grid
+    int aligned;             // 1: CTAs take whole row blocks; 0: stream-K shares of the units
+    int kmax;                // partial slots per (problem, split, row block)
+    int cg;                  // groups per pipeline stage
+    int nst;                 // pipeline stages
+    int segmax;              // capacity of a CTA's segment list
+    float* partials;
+    int* counters;
+    int* status;             // device status word
+    uint64_t limit_ns;       // bound of every wait
+    int red_off, seg_off, round_off, last_off, xraw_off, x_rs, stage_off;  // shared-memory layout (bytes)
+    // warp mode: active consumer warps, pending capacity per warp, second activation buffer
+    int nw, pw, xsum1_off, xraw1_off;
+};
+
+struct Plan {
+    int mode;  // 0: teams in lock-step (latency-bound calls), 1: warp workers (bandwidth-bound calls)
+    int KW, R, S, Gs, cg, nst, C, aligned, kmax, segmax, slots;
+    int red_off, seg_off, round_off, last_off, xraw_off, x_rs, stage_off;
+    int nw, pw, xsum1_off, xraw1_off;
+    size_t smem;
+    size_t ws_partials;      // bytes
+    size_t ws_counters;      // bytes
+};
+
+// host helpers (tfq_api.cu)
+void set_error(const char* fmt, ...);
+int device_sms();
+// k_full: K when the activation rows are staged whole (RMSNorm prologue), else 0;
+// rows: activation rows to allocate shared memory for (8 for MoE).
+Plan plan_qproj(int n_rb, int groups, int mats, int bits, int slots, int k_full, int rows);
+
+// launchers (tfq_qproj_b*_*.cu, one instantiation unit per bit width and matrix count)
+cudaError_t launch_qproj_b4_single(bool moe, const Plan& plan, const QProjParams& p, cudaStream_t stream, bool pdl);
+cudaError_t launch_qproj_b4_dual(bool moe, const Plan& plan, const QProjParams& p, cudaStream_t stream, bool pdl);
+cudaError_t launch_qproj_b8_single(bool moe, const Plan& plan, const QProjParams& p, cudaStream_t stream, bool pdl);
+cudaError_t launch_qproj_b8_dual(bool moe, const Plan& plan, const QProjParams& p, cudaStream_t stream, bool pdl);
+
+inline cudaError_t launch_qproj(int bits, bool dual, bool moe, const Plan& plan, const QProjParams& p,
+                                cudaStream_t stream, bool pdl)
+{
+    if (bits == 4)
+        return dual ? launch_qproj_b4_dual(moe, plan, p, stream, pdl) : launch_qproj_b4_single(moe, plan, p, stream, pdl);
+    return dual ? launch_qproj_b8_dual(moe, plan, p, stream, pdl) : launch_qproj_b8_single(moe, plan, p, stream, pdl);
+}
+
+// pack kernels (tfq_pack.cu)
+cudaError_t launch_pack(const uint32_t* wq, const uint16_t* s, const uint16_t* b, int64_t batch, int64_t N,
+                        int64_t K, int bits, uint8_t* packed, cudaStream_t stream);
+cudaError_t launch_unpack(const uint8_t* packed, int64_t batch, int64_t N, int64_t K, int bits, uint32_t* wq,
+                          uint16_t* s, uint16_t* b, cudaStream_t stream);
+
+// MoE helpers (tfq_moe.cu)
+cudaError_t launch_moe_route(const float* logits, int M, int E, int top_k, int32_t* idx, float* w, MoeMeta* meta,
+                             cudaStream_t stream, bool pdl);
+cudaError_t launch_moe_combine(const MoeMeta* meta, const float* o, int M, int top_k, int H, uint16_t* y,
+                               cudaStream_t stream);
+cudaError_t launch_timeout_probe(int* status, uint64_t limit_ns, cudaStream_t stream);
+
+}  // namespace tfq

@@ -1,0 +1,197 @@
+// Repacking of MLX affine quantised weights into the projection kernel's tile order.
+//
+// A tile is 16 output rows x 64 input columns (one quantisation group). Its code
+// bytes are laid out so that lane l of a warp loads, with one 16-byte (4-bit) or
+// two 16-byte (8-bit) shared-memory loads, exactly the A fragments it needs for
+// the four m16n8k16 MMAs that cover the 64 columns; the scales and biases of the
+// 16 rows follow as 8 pairs (row i, row i+8), which is what a lane's accumulator
+// fragment needs. Rows past N are zero (code 0, scale 0, bias 0).
+//
+// MMA A-fragment (row-major 16x16, bf16): register r of lane l = (gi = l/4, t = l%4)
+// holds rows gi + 8*(r&1) and columns 2t + 8*(r>>1) + {0, 1}.
+//
+// 4-bit: word kb of lane l holds the 8 codes of k-block kb; code p of the word
+//   (bits 4p..4p+3) is row gi + 8*(p&1), column 2t + (p>>2) + 8*((p>>1)&1), so
+//   that ((w >> 4r) & 0x000F000F) yields register r as two codes.
+// 8-bit: words 2kb + jp of lane l; byte bp is row gi + 8*(bp&1), column
+//   2t + 8*jp + (bp>>1). The low nibbles of a word give registers 2jp, 2jp+1 of
+//   the "low" fragment, the high nibbles the same registers of the "high" one.
+#include "tfq_internal.h"
+
+namespace tfq {
+namespace {
+
+__device__ __forceinline__ uint32_t code_at(const uint32_t* wq_row, int64_t k, int bits)
+{
+    const int per = 32 / bits;
+    const uint32_t word = wq_row[k / per];
+    return (word >> (bits * (int)(k % per))) & ((1u << bits) - 1u);
+}
+
+__global__ void pack_kernel(const uint32_t* __restrict__ wq, const uint16_t* __restrict__ sc,
+                            const uint16_t* __restrict__ bi, int64_t batch, int64_t N, int64_t K, int bits,
+                            uint8_t* __restrict__ packed, PackHeader hdr)
+{
+    const int64_t G = K / kGroup;
+    const int64_t n_rb = (N + kRowsPerBlock - 1) / kRowsPerBlock;
+    const int tile_words = tile_bytes_for(bits) / 4;
+    const int q_words = tile_q_bytes_for(bits) / 4;
+    const int64_t words_per_row = K * bits / 32;
+    const int64_t total = batch * n_rb * G * tile_words;
+    uint32_t* out = reinterpret_cast<uint32_t*>(packed + TF_PACK_HEADER_BYTES);
+
+    if (blockIdx.x == 0 && threadIdx.x == 0)
+        *reinterpret_cast<PackHeader*>(packed) = hdr;
+
+    for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
+         idx += (int64_t)gridDim.x * blockDim.x) {
+        const int wi = (int)(idx % tile_words);
+        const int64_t tile = idx / tile_words;
+        const int64_t g = tile % G;
+        const int64_t rb = (tile / G) % n_rb;
+        const int64_t b = tile / (G * n_rb);
+        const uint32_t* wq_b = wq + b * N * words_per_row;
+        uint32_t word = 0;
+        if (wi < q_words) {
+            if (bits == 4) {
+                const int lane = wi >> 2, kb = wi & 3, gi = lane >> 2, t = lane & 3;
+                for (int p = 0; p < 8; ++p) {
+                    const int64_t row = rb * kRowsPerBlock + gi + 8 * (p & 1);
+                    const int64_t k = g * kGroup + kb * 16 + 2 * t + (p >> 2) + 8 * ((p >> 1) & 1);
+                    if (row < N)
+                        word |= code_at(wq_b + row * words_per_row, k, 4) << (4 * p);
+                }
+            } else {
+                const int lane = wi >> 3, kb = (wi >> 1) & 3, jp = wi & 1, gi = lane >> 2, t = lane & 3;
+                for (int bp = 0; bp < 4; ++bp) {
+                    const int64_t row = rb * kRowsPerBlock + gi + 8 * (bp & 1);
+                    const int64_t k = g * kGroup + kb * 16 + 2 * t + 8 * jp + (bp >> 1);
+                    if (row < N)
+                        word |= code_at(wq_b + row * words_per_row, k, 8) << (8 * bp);
+                }
+            }
+        } else {
+            const int j = wi - q_words;     // 0..15
+            const int gi = j >> 1;
+            const uint16_t* src = (j & 1) ? bi : sc;
+            const int64_t row_lo = rb * kRowsPerBlock + gi, row_hi = row_lo + 8;
+            const uint32_t lo = row_lo < N ? src[(b * N + row_lo) * G + g] : 0u;
+            const uint32_t hi = row_hi < N ? src[(b * N + row_hi) * G + g] : 0u;
+            word = lo | (hi << 16);
+        }
+        out[idx] = word;
+    }
+}
+
+// Locate element (row rr of its 16-row block, column kk of its 64-column group)
+// inside a tile: returns the word index and the bit shift of its code.
+__device__ __forceinline__ void locate(int rr, int kk, int bits, int& word, int& shift)
+{
+    const int kb = kk >> 4, c = kk & 15, half = c & 1, t = (c & 7) >> 1, gi = rr & 7;
+    const int lane = gi * 4 + t;
+    if (bits == 4) {
+        const int p = (rr >> 3) + 2 * (c >> 3) + 4 * half;
+        word = lane * 4 + kb;
+        shift = 4 * p;
+    } else {
+        const int jp = c >> 3;
+        const int bp = (rr >> 3) | (half << 1);
+        word = lane * 8 + kb * 2 + jp;
+        shift = 8 * bp;
+    }
+}
+
+__global__ void unpack_codes_kernel(const uint8_t* __restrict__ packed, int64_t batch, int64_t N, int64_t K,
+                                    int bits, uint32_t* __restrict__ wq)
+{
+    const int64_t G = K / kGroup;
+    const int64_t n_rb = (N + kRowsPerBlock - 1) / kRowsPerBlock;
+    const int per = 32 / bits;
+    const int64_t words_per_row = K / per;
+    const int64_t total = batch * N * words_per_row;
+    const int tile_words = tile_bytes_for(bits) / 4;
+    const uint32_t* tiles = reinterpret_cast<const uint32_t*>(packed + TF_PACK_HEADER_BYTES);
+    for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
+         idx += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t j = idx % words_per_row;
+        const int64_t row = (idx / words_per_row) % N;
+        const int64_t b = idx / (words_per_row * N);
+        uint32_t out = 0;
+        for (int i = 0; i < per; ++i) {
+            const int64_t k = j * per + i;
+            int w, sh;
+            locate((int)(row % kRowsPerBlock), (int)(k % kGroup), bits, w, sh);
+            const int64_t tile = (b * n_rb + row / kRowsPerBlock) * G + k / kGroup;
+            const uint32_t code = (tiles[tile * tile_words + w] >> sh) & ((1u << bits) - 1u);
+            out |= code << (bits * i);
+        }
+        wq[idx] = out;
+    }
+}
+
+__global__ void unpack_scales_kernel(const uint8_t* __restrict__ packed, int64_t batch, int64_t N, int64_t K,
+                                     int bits, uint16_t* __restrict__ sc, uint16_t* __restrict__ bi)
+{
+    const int64_t G = K / kGroup;
+    const int64_t n_rb = (N + kRowsPerBlock - 1) / kRowsPerBlock;
+    const int64_t total = batch * N * G;
+    const int tile_words = tile_bytes_for(bits) / 4;
+    const int q_words = tile_q_bytes_for(bits) / 4;
+    const uint32_t* tiles = reinterpret_cast<const uint32_t*>(packed + TF_PACK_HEADER_BYTES);
+    for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
+         idx += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t g = idx % G;
+        const int64_t row = (idx / G) % N;
+        const int64_t b = idx / (G * N);
+        const int rr = (int)(row % kRowsPerBlock);
+        const int64_t tile = (b * n_rb + row / kRowsPerBlock) * G + g;
+        const uint32_t* tw = tiles + tile * tile_words + q_words;
+        const int sh = (rr >> 3) * 16;
+        sc[idx] = (uint16_t)(tw[2 * (rr & 7)] >> sh);
+        bi[idx] = (uint16_t)(tw[2 * (rr & 7) + 1] >> sh);
+    }
+}
+
+int grid_for(int64_t total, int threads)
+{
+    int64_t blocks = (total + threads - 1) / threads;
+    if (blocks > 65535LL * 32)
+        blocks = 65535LL * 32;
+    return (int)(blocks < 1 ? 1 : blocks);
+}
+
+}  // namespace
+
+cudaError_t launch_pack(const uint32_t* wq, const uint16_t* s, const uint16_t* b, int64_t batch, int64_t N,
+                        int64_t K, int bits, uint8_t* packed, cudaStream_t stream)
+{
+    PackHeader h{};
+    h.magic = TF_QWEIGHT_MAGIC;
+    h.version = TF_PACK_VERSION;
+    h.bits = bits;
+    h.group = kGroup;
+    h.batch = batch;
+    h.N = N;
+    h.K = K;
+    h.n_pad = (N + kRowsPerBlock - 1) / kRowsPerBlock * kRowsPerBlock;
+    h.tile_bytes = tile_bytes_for(bits);
+    h.matrix_bytes = h.n_pad / kRowsPerBlock * (K / kGroup) * h.tile_bytes;
+    const int64_t total = batch * (h.n_pad / kRowsPerBlock) * (K / kGroup) * (tile_bytes_for(bits) / 4);
+    pack_kernel<<<grid_for(total, 256), 256, 0, stream>>>(wq, s, b, batch, N, K, bits, packed, h);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_unpack(const uint8_t* packed, int64_t batch, int64_t N, int64_t K, int bits, uint32_t* wq,
+                          uint16_t* s, uint16_t* b, cudaStream_t stream)
+{
+    const int64_t words = batch * N * (K * bits / 32);
+    unpack_codes_kernel<<<grid_for(words, 256), 256, 0, stream>>>(packed, batch, N, K, bits, wq);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess)
+        return e;
+    const int64_t groups = batch * N * (K / kGroup);
+    unpack_scales_kernel<<<grid_for(groups, 256), 256, 0, stream>>>(packed, batch, N, K, bits, s, b);
+    return cudaGetLastError();
+}
+
+}  // namespace tfq

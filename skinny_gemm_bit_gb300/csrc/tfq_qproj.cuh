@@ -1,0 +1,1067 @@
+// The quantised projection kernel: y[m][n] = sum_k xn[m][k] * (s q + b)[n][k].
+//
+// Work is a linear sequence of 16-row x 64-column tiles ("units"), ordered by
+// problem (an MoE expert slot; one problem otherwise), K split, 16-row block,
+// group. The grid is persistent (at most one CTA per SM); each CTA takes one
+// contiguous range of it, either whole row blocks ("aligned", when that balances
+// within about 10 %) or an exact 1/C share of the units ("stream-K", cutting row
+// blocks anywhere). A CTA lists its segments (maximal runs inside one row block)
+// once, then walks them in rounds: R teams of KW warps, one segment per team.
+//
+//   producer warp   one lane streams the range's tiles (contiguous per row block
+//                   in the packed layout) into an nst-deep ring of shared-memory
+//                   stages with bulk async copies (TMA engine) completing on
+//                   mbarriers. It starts before the kernel waits on the previous
+//                   grid (programmatic dependent launch), so the weight stream
+//                   overlaps the previous kernel's tail, and it never stops
+//                   between rounds.
+//   consumer warps  (16) copy the activation rows of the current (problem,
+//                   split) into shared memory with bulk copies, normalise and
+//                   round them to bf16 when an RMSNorm is folded in, form the
+//                   per-group sums of the rounded values and lay each group out
+//                   in MMA B-fragment order. The KW warps of a team split the
+//                   groups of their segment. Per 16x64 tile: one 16-byte (4-bit) load gives a
+//                   lane its A fragments for four m16n8k16 MMAs; codes become
+//                   bf16 (128 + q) pairs with one LOP3 each; the group epilogue
+//                   folds scale and bias back in:
+//                      y += s * sum_k x (128 + q) + (b - 128 s) * sum_k x
+//                   which equals sum_k x (s q + b).
+//   reduction       the warps of a team are summed through shared memory in fixed
+//                   order. A segment that is a whole row block of an unsplit
+//                   problem is stored directly; any other contributes an fp32
+//                   partial to a workspace slot, and once the CTA has finished
+//                   its range the last contributor of each row block (a counter
+//                   per row block) sums the slots in (split, contributor) order,
+//                   zeroes them and its counter again, and stores: deterministic,
+//                   no float atomics, and the workspace is left as it was found.
+//
+// Every wait is bounded in wall time; a wait that runs out records TF_E_TIMEOUT
+// in the status word and the CTA leaves after draining its own copies.
+#pragma once
+
+#include "tfq_internal.h"
+#include "tfq_ptx.cuh"
+
+namespace tfq {
+
+struct QSmem {
+    static constexpr int kFullOff = 0;    // full[8]
+    static constexpr int kEmptyOff = 64;  // empty[8]
+    static constexpr int kXbarOff = 128;  // activation copy barrier
+    static constexpr int kFlagOff = 144;  // [0] abort
+    static constexpr int kInvOff = 160;   // inv_rms[8]
+    static constexpr int kRowOff = 192;   // activation row of each column [8]
+    static constexpr int kSlotOff = 256;  // MoE: per problem {expert, count} [kMaxSlots] then rows [kMaxSlots][8]
+    static constexpr int kSlotBytes = kMaxSlots * 8 + kMaxSlots * kMaxM * 4;
+    static constexpr int kXsumOff = kSlotOff + kSlotBytes;  // xsum[Gs][8] fp32, then the offsets in the params
+};
+
+// Bounded by the SM cycle counter (cheap to read, unlike the global timer);
+// limit_ns is converted at 2 cycles per ns, which over-estimates the wall time
+// only at clocks below 2 GHz.
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                              int* status, uint64_t limit_ns)
+{
+    if (mbar_try_wait(bar, parity))
+        return true;
+    const long long t0 = clock64();
+    const long long limit = (long long)(limit_ns * 2);
+    while (true) {
+        if (mbar_try_wait(bar, parity))
+            return true;
+        if (*abort_flag)
+            return false;
+        if (clock64() - t0 > limit) {
+            *abort_flag = 1;
+            atomicCAS(status, 0, TF_E_TIMEOUT);
+            return false;
+        }
+    }
+}
+
+__device__ __forceinline__ float warp_sum(float v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// One 16x64 tile against the B fragments (xa, xb) and group sums (xs) of its group.
+template <int BITS>
+__device__ __forceinline__ void tile_mac(const uint8_t* tile, int lane, const uint4& xa, const uint4& xb,
+                                         const float2& xs, float (&acc)[4])
+{
+    constexpr int QB = tile_q_bytes_for(BITS);
+    const uint2 sb = *reinterpret_cast<const uint2*>(tile + QB + (lane >> 2) * 8);
+    const float s_lo = bf16lo_f32(sb.x), s_hi = bf16hi_f32(sb.x);
+    const float b_lo = bf16lo_f32(sb.y), b_hi = bf16hi_f32(sb.y);
+    if constexpr (BITS == 4) {
+        const uint4 wv = *reinterpret_cast<const uint4*>(tile + lane * 16);
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
+        mma_bf16_16816(d, nib2_bf16(wv.x), nib2_bf16(wv.x >> 4), nib2_bf16(wv.x >> 8), nib2_bf16(wv.x >> 12),
+                       xa.x, xa.y);
+        mma_bf16_16816(d, nib2_bf16(wv.y), nib2_bf16(wv.y >> 4), nib2_bf16(wv.y >> 8), nib2_bf16(wv.y >> 12),
+                       xa.z, xa.w);
+        mma_bf16_16816(d, nib2_bf16(wv.z), nib2_bf16(wv.z >> 4), nib2_bf16(wv.z >> 8), nib2_bf16(wv.z >> 12),
+                       xb.x, xb.y);
+        mma_bf16_16816(d, nib2_bf16(wv.w), nib2_bf16(wv.w >> 4), nib2_bf16(wv.w >> 8), nib2_bf16(wv.w >> 12),
+                       xb.z, xb.w);
+        // sum_k x (s q + b) = s * sum_k x (128 + q) + (b - 128 s) * sum_k x
+        const float c_lo = fmaf(-128.f, s_lo, b_lo), c_hi = fmaf(-128.f, s_hi, b_hi);
+        acc[0] = fmaf(s_lo, d[0], fmaf(c_lo, xs.x, acc[0]));
+        acc[1] = fmaf(s_lo, d[1], fmaf(c_lo, xs.y, acc[1]));
+        acc[2] = fmaf(s_hi, d[2], fmaf(c_hi, xs.x, acc[2]));
+        acc[3] = fmaf(s_hi, d[3], fmaf(c_hi, xs.y, acc[3]));
+    } else {
+        // 8-bit code q = 16 hi + lo: two nibble MMAs per k block.
+        const uint4 w01 = *reinterpret_cast<const uint4*>(tile + lane * 32);
+        const uint4 w23 = *reinterpret_cast<const uint4*>(tile + lane * 32 + 16);
+        float dl[4] = {0.f, 0.f, 0.f, 0.f}, dh[4] = {0.f, 0.f, 0.f, 0.f};
+#define TFQ_KB8(w0, w1, b0, b1)                                                                             \
+    mma_bf16_16816(dl, nib2_bf16(w0), nib2_bf16((w0) >> 8), nib2_bf16(w1), nib2_bf16((w1) >> 8), b0, b1); \
+    mma_bf16_16816(dh, nib2_bf16((w0) >> 4), nib2_bf16((w0) >> 12), nib2_bf16((w1) >> 4), nib2_bf16((w1) >> 12), b0, b1);
+        TFQ_KB8(w01.x, w01.y, xa.x, xa.y)
+        TFQ_KB8(w01.z, w01.w, xa.z, xa.w)
+        TFQ_KB8(w23.x, w23.y, xb.x, xb.y)
+        TFQ_KB8(w23.z, w23.w, xb.z, xb.w)
+#undef TFQ_KB8
+        // sum_k x (s q + b) = s * (sum x (128+lo) + 16 sum x (128+hi)) + (b - 2176 s) * sum x
+        const float c_lo = fmaf(-2176.f, s_lo, b_lo), c_hi = fmaf(-2176.f, s_hi, b_hi);
+        acc[0] = fmaf(s_lo, fmaf(16.f, dh[0], dl[0]), fmaf(c_lo, xs.x, acc[0]));
+        acc[1] = fmaf(s_lo, fmaf(16.f, dh[1], dl[1]), fmaf(c_lo, xs.y, acc[1]));
+        acc[2] = fmaf(s_hi, fmaf(16.f, dh[2], dl[2]), fmaf(c_hi, xs.x, acc[2]));
+        acc[3] = fmaf(s_hi, fmaf(16.f, dh[3], dl[3]), fmaf(c_hi, xs.y, acc[3]));
+    }
+}
+
+// ---------------------------------------------------------------- activation staging
+//
+// A staged activation buffer holds rows rows[0..Mrows) of x, columns
+// [xg0 * 64, (xg0 + xgc) * 64), row stride p.x_rs bytes (= columns * 2 + 64, so
+// that a quarter-warp's B-fragment loads from two consecutive rows never share a
+// bank). After preparation, each (group, row) block of 32 words is in B-fragment
+// order: the lane (row m, t) of an m16n8k16 MMA finds its four k-block-0/1 words at
+// 4t..4t+3 and its k-block-2/3 words at 16+4t..16+4t+3. Word p = 8 kb + 4 j + t of
+// the natural order (columns 16 kb + 8 j + 2 t + {0,1}) moves to
+// 16 (kb >> 1) + 4 t + 2 (kb & 1) + j.
+
+// One thread: copy the rows into the buffer; completion on `bar`.
+__device__ __forceinline__ void x_issue(const QProjParams& p, uint8_t* buf, const int* rows, int Mrows, int64_t xbase,
+                                        int xg0, int xgc, uint64_t* bar)
+{
+    mbar_arrive_expect_tx(bar, (uint32_t)(Mrows * xgc * 128));
+    for (int m = 0; m < Mrows; ++m)
+        bulk_g2s_plain(buf + m * p.x_rs, p.x + xbase + (int64_t)rows[m] * p.ldx + (int64_t)xg0 * kGroup,
+                       (uint32_t)(xgc * 128), bar);
+}
+
+// Consumer warps (nwarps of them, named barrier bar_id): after the copy has landed,
+// RMSNorm statistics when gamma is set (the whole row is staged then), then for the
+// groups [g_lo, g_lo + ng) of the problem (staged from group xg0): normalise and
+// round to bf16 in place, group sums of the rounded values into xs[(g - g_lo) * 8 + m]
+// (zero for rows >= Mrows), and reorder to B-fragment order.
+__device__ __forceinline__ void x_prepare(const QProjParams& p, uint8_t* buf, int Mrows, int xg0, int g_lo, int ng,
+                                          float* xs, float* inv_rms, int cw, int lane, int nwarps, int bar_id)
+{
+    const bool norm = p.gamma != nullptr;
+    if (norm) {
+        for (int m = cw; m < Mrows; m += nwarps) {
+            const uint4* row = reinterpret_cast<const uint4*>(buf + m * p.x_rs);
+            float ss = 0.f;
+            for (int i = lane; i < p.K / 8; i += 32) {
+                const uint4 v = row[i];
+                const uint32_t vv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const float a = bf16lo_f32(vv[q]), b = bf16hi_f32(vv[q]);
+                    ss = fmaf(a, a, ss);
+                    ss = fmaf(b, b, ss);
+                }
+            }
+            ss = warp_sum(ss);
+            if (lane == 0)
+                inv_rms[m] = rsqrtf(ss / (float)p.K + p.eps);
+        }
+        named_bar_sync(bar_id, nwarps * 32);
+    }
+    // a lane handles one 8-column chunk cc = 2 kb + j of one (group, row)
+    for (int base = cw * 4; base < ng * kMaxM; base += nwarps * 4) {
+        const int pi = base + (lane >> 3);
+        const int cc = lane & 7;
+        const int gl = pi >> 3, m = pi & 7;
+        const bool valid = pi < ng * kMaxM;
+        const bool live = valid && m < Mrows;
+        float part = 0.f;
+        uint32_t vv[4] = {0u, 0u, 0u, 0u};
+        uint32_t* blk = reinterpret_cast<uint32_t*>(buf + m * p.x_rs + (g_lo - xg0 + gl) * 128);
+        if (live) {
+            const uint4 v = reinterpret_cast<const uint4*>(blk)[cc];
+            vv[0] = v.x;
+            vv[1] = v.y;
+            vv[2] = v.z;
+            vv[3] = v.w;
+            if (norm) {
+                const uint4 gv =
+                    __ldg(reinterpret_cast<const uint4*>(p.gamma + (int64_t)(g_lo + gl) * kGroup + cc * 8));
+                const uint32_t gg[4] = {gv.x, gv.y, gv.z, gv.w};
+                const float inv = inv_rms[m];
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    vv[q] = f32x2_to_bf16x2(bf16lo_f32(vv[q]) * inv * bf16lo_f32(gg[q]),
+                                            bf16hi_f32(vv[q]) * inv * bf16hi_f32(gg[q]));
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                part += bf16lo_f32(vv[q]) + bf16hi_f32(vv[q]);
+        }
+        part += __shfl_xor_sync(0xffffffffu, part, 4);
+        part += __shfl_xor_sync(0xffffffffu, part, 2);
+        part += __shfl_xor_sync(0xffffffffu, part, 1);
+        __syncwarp();  // every lane of the block has read it before any rewrites it
+        if (live) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                blk[16 * (cc >> 2) + 4 * q + (cc & 3)] = vv[q];
+        }
+        if (valid && cc == 0)
+            xs[gl * kMaxM + m] = part;
+    }
+    named_bar_sync(bar_id, nwarps * 32);
+}
+
+// The B fragments (xa: k blocks 0, 1; xb: k blocks 2, 3) of group g_rel of a buffer.
+__device__ __forceinline__ void x_frag(const uint8_t* buf, int x_rs, int gi, int tq, int g_rel, bool has_row, uint4& xa,
+                                       uint4& xb)
+{
+    if (has_row) {
+        const uint4* q = reinterpret_cast<const uint4*>(buf + gi * x_rs + g_rel * 128 + tq * 16);
+        xa = q[0];
+        xb = q[4];
+    } else {
+        xa = make_uint4(0u, 0u, 0u, 0u);
+        xb = xa;
+    }
+}
+
+// Final values of one lane's accumulator fragment (rows row0 + gi, row0 + gi + 8;
+// columns 2t, 2t + 1) -> outputs.
+template <bool DUAL, bool MOE>
+__device__ __forceinline__ void store_outputs(const QProjParams& p, int prob, int Mrows, int row0, int lane,
+                                              const float (&a0)[4], const float (&a1)[4])
+{
+    const int gi = lane >> 2, t = lane & 3;
+    const int64_t ybase = MOE ? (int64_t)prob * p.y_slot_stride : 0;
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+        const int n = row0 + gi + 8 * (v >> 1);
+        const int m = 2 * t + (v & 1);
+        if (n >= p.N || m >= Mrows)
+            continue;
+        float val;
+        if constexpr (DUAL) {
+            const float g = a0[v];
+            val = g / (1.f + expf(-g)) * a1[v];
+        } else {
+            val = a0[v];
+        }
+        if (!MOE && p.residual != nullptr)  // written by an earlier kernel: read through L2, not L1
+            val += __uint_as_float((uint32_t)__ldcg(p.residual + (int64_t)m * p.ldr + n) << 16);
+        const int64_t idx = ybase + (int64_t)m * p.ldy + n;
+        if (p.y_f32)
+            static_cast<float*>(p.y)[idx] = val;
+        else
+            static_cast<__nv_bfloat16*>(p.y)[idx] = __float2bfloat16_rn(val);
+    }
+}
+
+// Static partition of the unit sequence over the CTAs.
+//   aligned  : CTA c takes whole (problem, split, row-block) items [I c / C, I (c+1) / C)
+//   stream-K : CTA c takes units [U c / C, U (c+1) / C), cutting row blocks anywhere
+struct Part {
+    int64_t items, U;
+    int C;       // CTAs with work: min(grid, items or U)
+    int per_p;   // units per problem = n_rb * groups
+    int per_ps;  // units per (problem, split) = n_rb * Gs
+    int Gs;
+    bool aligned;
+    __device__ __forceinline__ int64_t start(int c) const
+    {
+        return aligned ? (items * c / C) * Gs : U * c / C;
+    }
+    __device__ __forceinline__ int cta_of(int64_t u) const { return (int)(((u + 1) * C - 1) / U); }
+    // CTAs contributing to the row block starting at unit f (stream-K only)
+    __device__ __forceinline__ int contributors(int64_t f) const { return cta_of(f + Gs - 1) - cta_of(f) + 1; }
+};
+
+constexpr int kBarConsumers = 15;  // named barrier of all consumer warps; 1..8 are team barriers
+
+template <int BITS, bool DUAL, bool MOE, int KW>
+__global__ void __launch_bounds__(kThreads, 1) qproj_kernel(const __grid_constant__ QProjParams p)
+{
+    constexpr int R = kConsumerWarps / KW;
+    constexpr int MATS = DUAL ? 2 : 1;
+    constexpr int TILE = tile_bytes_for(BITS);
+    constexpr int VALS = DUAL ? 8 : 4;
+    constexpr int NCT = kConsumerWarps * 32;
+
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + QSmem::kFullOff);
+    uint64_t* empty = reinterpret_cast<uint64_t*>(smem + QSmem::kEmptyOff);
+    uint64_t* xbar = reinterpret_cast<uint64_t*>(smem + QSmem::kXbarOff);
+    volatile int* flags = reinterpret_cast<volatile int*>(smem + QSmem::kFlagOff);  // [0] abort [1] snapshot
+    int* counts = reinterpret_cast<int*>(smem + QSmem::kFlagOff + 8);                // [0] segments [1] rounds
+    float* inv_rms = reinterpret_cast<float*>(smem + QSmem::kInvOff);
+    int* rowsel = reinterpret_cast<int*>(smem + QSmem::kRowOff);
+    int2* slot_ec = reinterpret_cast<int2*>(smem + QSmem::kSlotOff);                   // {expert, count}
+    int* slot_rows = reinterpret_cast<int*>(smem + QSmem::kSlotOff + kMaxSlots * 8);  // [slot][8]
+    float* xsum = reinterpret_cast<float*>(smem + QSmem::kXsumOff);
+    float* red = reinterpret_cast<float*>(smem + p.red_off);
+    int4* segs = reinterpret_cast<int4*>(smem + p.seg_off);      // {problem, split, row block, g0 << 16 | len}
+    int2* rounds = reinterpret_cast<int2*>(smem + p.round_off);  // {first segment, longest segment}
+    int* lastf = reinterpret_cast<int*>(smem + p.last_off);      // per segment: this CTA sums the row block
+    uint8_t* xraw = smem + p.xraw_off;
+    uint8_t* stages = smem + p.stage_off;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int c = blockIdx.x;
+    const int stage_bytes = MATS * R * p.cg * TILE;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < p.nst; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kConsumerWarps);
+        }
+        mbar_init(xbar, 1);
+        flags[0] = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    pdl_launch_dependents();
+
+    int P = p.P;
+    if constexpr (MOE) {
+        // the routing table comes from the previous kernel
+        pdl_wait();
+        P = __ldcg(&p.meta->n_active);
+        for (int i = threadIdx.x; i < P; i += blockDim.x) {
+            slot_ec[i] = make_int2(__ldcg(&p.meta->slot[i].expert), __ldcg(&p.meta->slot[i].count));
+            for (int j = 0; j < kMaxM; ++j)
+                slot_rows[i * kMaxM + j] = p.gather ? __ldcg(&p.meta->slot[i].rows[j]) : j;
+        }
+    }
+    Part pt;
+    pt.per_p = p.n_rb * p.groups;
+    pt.per_ps = p.n_rb * p.Gs;
+    pt.Gs = p.Gs;
+    pt.aligned = p.aligned != 0;
+    pt.items = (int64_t)P * p.S * p.n_rb;
+    pt.U = pt.items * p.Gs;
+    pt.C = (int)min((int64_t)p.C, max(pt.aligned ? pt.items : pt.U, (int64_t)1));
+    const int64_t u0 = c < pt.C ? pt.start(c) : 0, u1 = c < pt.C ? pt.start(c + 1) : 0;
+
+    // ---- this CTA's segments (maximal runs inside one row block) and rounds (up to R
+    // consecutive segments of one (problem, split)); built once, read by every warp
+    if (threadIdx.x == 0) {
+        int nseg = 0, nround = 0, rlen = 0, rp = -1, rs = -1, rmax = 0;
+        if (u0 < u1) {
+            const int uu = (int)u0;  // units fit in 30 bits (checked on the host)
+            int pp = uu / pt.per_p;
+            int rem = uu - pp * pt.per_p;
+            int ss = rem / pt.per_ps;
+            rem -= ss * pt.per_ps;
+            int rb = rem / p.Gs;
+            int gl = rem - rb * p.Gs;
+            int64_t u = u0;
+            while (u < u1 && nseg < p.segmax) {
+                const int len = (int)min((int64_t)(p.Gs - gl), u1 - u);
+                if (rlen == R || pp != rp || ss != rs) {
+                    if (nround > 0)
+                        rounds[nround - 1].y = rmax;
+                    rounds[nround++].x = nseg;
+                    rlen = 0;
+                    rmax = 0;
+                    rp = pp;
+                    rs = ss;
+                }
+                segs[nseg++] = make_int4(pp, ss, rb, (gl << 16) | len);
+                ++rlen;
+                rmax = max(rmax, len);
+                u += len;
+                gl = 0;
+                if (++rb == p.n_rb) {
+                    rb = 0;
+                    if (++ss == p.S) {
+                        ss = 0;
+                        ++pp;
+                    }
+                }
+            }
+            if (u < u1) {  // the host sizes the list; never expected
+                flags[0] = 1;
+                atomicCAS(p.status, 0, TF_E_TIMEOUT);
+            }
+            rounds[nround - 1].y = rmax;
+        }
+        rounds[nround].x = nseg;
+        counts[0] = nseg;
+        counts[1] = flags[0] ? 0 : nround;
+    }
+    __syncthreads();
+    const int nseg = counts[0], nround = counts[1];
+
+    // ------------------------------------------------------------ producer
+    if (warp == kConsumerWarps) {
+        if (lane == 0) {
+            const uint64_t pol = policy_evict_first();
+            int st_global = 0;
+            bool ok = true;
+            for (int t = 0; t < nround && ok; ++t) {
+                const int i0 = rounds[t].x, n = rounds[t + 1].x - i0, maxlen = rounds[t].y;
+                const int4 first = segs[i0];
+                const int64_t mbase = MOE ? (int64_t)slot_ec[first.x].x * p.matrix_bytes : 0;
+                for (int g = 0; g < maxlen; g += p.cg, ++st_global) {
+                    const int s = st_global % p.nst;
+                    const uint32_t ph = (st_global / p.nst) & 1u;
+                    if (!wait_or_abort(&empty[s], ph ^ 1u, flags, p.status, p.limit_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    uint32_t bytes = 0;
+                    for (int r = 0; r < n; ++r)
+                        bytes += (uint32_t)max(0, min(p.cg, (segs[i0 + r].w & 0xFFFF) - g)) * TILE;
+                    mbar_arrive_expect_tx(&full[s], bytes * MATS);
+                    uint8_t* sbase = stages + s * stage_bytes;
+                    for (int r = 0; r < n; ++r) {
+                        const int4 e = segs[i0 + r];
+                        const int cnt = min(p.cg, (e.w & 0xFFFF) - g);
+                        if (cnt <= 0)
+                            continue;
+                        const int64_t tile = (int64_t)e.z * p.groups + e.y * p.Gs + (e.w >> 16) + g;
+#pragma unroll
+                        for (int mat = 0; mat < MATS; ++mat) {
+                            const uint8_t* src = (mat ? p.w1 : p.w0) + mbase + tile * TILE;
+                            bulk_g2s(sbase + (mat * R + r) * p.cg * TILE, src, (uint32_t)(cnt * TILE), &full[s], pol);
+                        }
+                    }
+                }
+            }
+            // no copy may still be in flight when the CTA leaves
+            for (int q = max(0, st_global - p.nst); q < st_global; ++q)
+                wait_or_abort(&full[q % p.nst], (q / p.nst) & 1u, flags, p.status, p.limit_ns);
+        }
+        return;
+    }
+
+    // ------------------------------------------------------------ consumers
+    const int cw = warp;
+    const int r_me = cw / KW, kp = cw % KW;
+    const int gi = lane >> 2, tq = lane & 3;
+    if constexpr (!MOE)
+        pdl_wait();
+    const bool norm = p.gamma != nullptr;
+    bool alive = true;
+    int cur_p = -1, cur_s = -1, Mrows = p.M, xphase = 0, nstaged = 0, st_global = 0;
+
+    for (int t = 0; t < nround; ++t) {
+        const int i0 = rounds[t].x, n = rounds[t + 1].x - i0, maxlen = rounds[t].y;
+        const int4 first = segs[i0];
+
+        if (first.x != cur_p || first.y != cur_s) {
+            // ---- stage the activation rows of (problem, split): the whole row when an
+            // RMSNorm is folded in (its statistics need every column), else the split's groups
+            named_bar_sync(kBarConsumers, NCT);  // everyone is done with the previous rows
+            if (MOE)
+                Mrows = slot_ec[first.x].y;
+            if (threadIdx.x < kMaxM)
+                rowsel[threadIdx.x] = MOE ? slot_rows[first.x * kMaxM + threadIdx.x] : (int)threadIdx.x;
+            const int xg0 = norm ? 0 : first.y * p.Gs;
+            const int xgc = norm ? p.groups : p.Gs;
+            if (cw == 0) {
+                __syncwarp();
+                if (lane == 0 && !flags[0])
+                    x_issue(p, xraw, rowsel, Mrows, MOE && !p.gather ? (int64_t)first.x * p.x_slot_stride : 0, xg0, xgc,
+                            xbar);
+            }
+            bool ok = alive && wait_or_abort(xbar, (uint32_t)xphase, flags, p.status, p.limit_ns);
+            xphase ^= 1;
+            ++nstaged;
+            alive = __all_sync(0xffffffffu, ok);
+            x_prepare(p, xraw, Mrows, xg0, first.y * p.Gs, p.Gs, xsum, inv_rms, cw, lane, kConsumerWarps,
+                      kBarConsumers);
+            cur_p = first.x;
+            cur_s = first.y;
+        }
+
+        // ---- this team's segment of the round
+        int rb = 0, gs = 0, len = 0;
+        if (r_me < n) {
+            const int4 e = segs[i0 + r_me];
+            rb = e.z;
+            gs = e.w >> 16;
+            len = e.w & 0xFFFF;
+        }
+        const int xoff = norm ? first.y * p.Gs : 0;  // first group of the split inside the staged rows
+        const bool has_row = gi < Mrows;
+        float acc0[4] = {0.f, 0.f, 0.f, 0.f}, acc1[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int g = 0; g < maxlen; g += p.cg, ++st_global) {
+            const int s = st_global % p.nst;
+            const uint32_t ph = (st_global / p.nst) & 1u;
+            bool ok = alive && wait_or_abort(&full[s], ph, flags, p.status, p.limit_ns);
+            alive = __all_sync(0xffffffffu, ok);
+            const int cnt = alive ? min(p.cg, len - g) : 0;
+            const uint8_t* sbase = stages + s * stage_bytes;
+            for (int j = kp; j < cnt; j += KW) {
+                const int gl = gs + g + j;  // group within the split
+                uint4 xa, xb;
+                x_frag(xraw, p.x_rs, gi, tq, xoff + gl, has_row, xa, xb);
+                const float2 xs = *reinterpret_cast<const float2*>(xsum + gl * kMaxM + 2 * tq);
+                tile_mac<BITS>(sbase + (r_me * p.cg + j) * TILE, lane, xa, xb, xs, acc0);
+                if constexpr (DUAL)
+                    tile_mac<BITS>(sbase + ((R + r_me) * p.cg + j) * TILE, lane, xa, xb, xs, acc1);
+            }
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&empty[s]);
+        }
+
+        // ---- sum the KW warps of the team (team barrier: ids 1..R)
+        if constexpr (KW > 1) {
+            named_bar_sync(1 + r_me, KW * 32);  // the previous round's reads of red are done
+            float* mine = red + (cw * 32 + lane) * VALS;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                mine[i] = acc0[i];
+                if constexpr (DUAL)
+                    mine[4 + i] = acc1[i];
+            }
+            named_bar_sync(1 + r_me, KW * 32);
+            if (kp == 0) {
+                for (int q = 1; q < KW; ++q) {
+                    const float* other = red + ((cw + q) * 32 + lane) * VALS;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        acc0[i] += other[i];
+                        if constexpr (DUAL)
+                            acc1[i] += other[4 + i];
+                    }
+                }
+            }
+        }
+
+        // ---- whole row block of an unsplit problem: store; else an fp32 partial
+        if (alive && kp == 0 && r_me < n) {
+            const int Mr = MOE ? slot_ec[first.x].y : p.M;
+            if (p.S == 1 && len == p.groups) {
+                store_outputs<DUAL, MOE>(p, first.x, Mr, rb * kRowsPerBlock, lane, acc0, acc1);
+            } else {
+                int k = 0;
+                if (!pt.aligned) {
+                    const int64_t f = (int64_t)first.x * pt.per_p + (int64_t)first.y * pt.per_ps + (int64_t)rb * p.Gs;
+                    k = min(c - pt.cta_of(f), p.kmax - 1);  // k < kmax by construction
+                }
+                float4* dst = reinterpret_cast<float4*>(
+                    p.partials +
+                    (((((int64_t)first.x * p.S + first.y) * p.n_rb + rb) * p.kmax + k) * 32 + lane) * VALS);
+                __stcg(dst, make_float4(acc0[0], acc0[1], acc0[2], acc0[3]));
+                if constexpr (DUAL)
+                    __stcg(dst + 1, make_float4(acc1[0], acc1[1], acc1[2], acc1[3]));
+            }
+        }
+    }
+
+    // abort is decided once for the whole CTA: every consumer warp reads one snapshot
+    named_bar_sync(kBarConsumers, NCT);
+    if (threadIdx.x == 0)
+        flags[1] = flags[0];
+    named_bar_sync(kBarConsumers, NCT);
+    if (flags[1]) {
+        // a bounded wait gave up (the status word says so); no activation copy may
+        // be left in flight when the CTA leaves
+        if (cw == 0 && lane == 0 && nstaged > 0)
+            mbar_wait_bounded(xbar, (uint32_t)(xphase ^ 1), p.limit_ns);
+        return;
+    }
+
+    // ------------------------------------------------------------ last contributor of a row block sums it
+    auto is_partial = [&](const int4& e) { return !(p.S == 1 && (e.w & 0xFFFF) == p.groups); };
+    bool any = false;
+    for (int i = 0; i < nseg; ++i)
+        any |= is_partial(segs[i]);
+    if (!any)
+        return;
+    __threadfence();
+    named_bar_sync(kBarConsumers, NCT);
+    for (int i = threadIdx.x; i < nseg; i += NCT) {
+        const int4 e = segs[i];
+        int last = 0;
+        if (is_partial(e)) {
+            int expected = p.S;
+            if (!pt.aligned) {
+                expected = 0;
+                for (int s2 = 0; s2 < p.S; ++s2)
+                    expected += pt.contributors((int64_t)e.x * pt.per_p + (int64_t)s2 * pt.per_ps + (int64_t)e.z * p.Gs);
+            }
+            const int old = atomicAdd(&p.counters[(int64_t)e.x * p.n_rb + e.z], 1);
+            last = old == expected - 1;
+        }
+        lastf[i] = last;
+    }
+    named_bar_sync(kBarConsumers, NCT);
+    for (int i = cw; i < nseg; i += kConsumerWarps) {
+        if (!lastf[i])
+            continue;
+        const int4 e = segs[i];
+        __threadfence();
+        float t0[4] = {0.f, 0.f, 0.f, 0.f}, t1[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int s2 = 0; s2 < p.S; ++s2) {
+            const int kc = pt.aligned ? 1
+                                      : min(pt.contributors((int64_t)e.x * pt.per_p + (int64_t)s2 * pt.per_ps +
+                                                            (int64_t)e.z * p.Gs),
+                                            p.kmax);
+            for (int k = 0; k < kc; ++k) {
+                float4* src = reinterpret_cast<float4*>(
+                    p.partials + (((((int64_t)e.x * p.S + s2) * p.n_rb + e.z) * p.kmax + k) * 32 + lane) * VALS);
+                const float4 v = __ldcg(src);
+                __stcg(src, make_float4(0.f, 0.f, 0.f, 0.f));  // the workspace is left as it was found
+                t0[0] += v.x;
+                t0[1] += v.y;
+                t0[2] += v.z;
+                t0[3] += v.w;
+                if constexpr (DUAL) {
+                    const float4 w = __ldcg(src + 1);
+                    __stcg(src + 1, make_float4(0.f, 0.f, 0.f, 0.f));
+                    t1[0] += w.x;
+                    t1[1] += w.y;
+                    t1[2] += w.z;
+                    t1[3] += w.w;
+                }
+            }
+        }
+        const int Mr = MOE ? slot_ec[e.x].y : p.M;
+        store_outputs<DUAL, MOE>(p, e.x, Mr, e.z * kRowsPerBlock, lane, t0, t1);
+        if (lane == 0)
+            p.counters[(int64_t)e.x * p.n_rb + e.z] = 0;
+    }
+}
+
+// ---------------------------------------------------------------- warp mode
+//
+// For bandwidth-bound calls. The C x nw consumer warps of the grid are "workers";
+// worker v takes either whole (problem, split, row block) items [I v / W, I (v+1) / W)
+// or an exact stream-K share [U v / W, U (v+1) / W) of the units (W = C nw). A worker
+// walks its range row block by row block in chunks of T tiles; every chunk is one
+// bulk copy (two for gate + up) into one of the worker's own SW ring slots, issued
+// by lane w of the producer warp, so the workers of a CTA never wait for each other
+// (a slot is only ever waited on by its owner, at most one phase ahead). A
+// segment that is a whole row block of an unsplit problem is stored directly;
+// boundary segments become fp32 partials summed, after the CTA's workers are done,
+// by the last contributor of the row block.
+template <int BITS, bool DUAL, bool MOE>
+__global__ void __launch_bounds__(kThreads, 1) qproj_warp_kernel(const __grid_constant__ QProjParams p)
+{
+    constexpr int MATS = DUAL ? 2 : 1;
+    constexpr int TILE = tile_bytes_for(BITS);
+    constexpr int VALS = DUAL ? 8 : 4;
+    const int NW = p.nw;                 // active consumer warps
+    const int T = p.cg;                  // tiles per chunk
+    const int SW = p.nst;                // ring slots per worker
+    const int slot_bytes = MATS * T * TILE;
+
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint64_t* xbar = reinterpret_cast<uint64_t*>(smem + QSmem::kXbarOff);  // [2]
+    volatile int* flags = reinterpret_cast<volatile int*>(smem + QSmem::kFlagOff);
+    float* inv0 = reinterpret_cast<float*>(smem + QSmem::kInvOff);
+    int* rows0 = reinterpret_cast<int*>(smem + QSmem::kRowOff);
+    int2* slot_ec = reinterpret_cast<int2*>(smem + QSmem::kSlotOff);
+    int* slot_rows = reinterpret_cast<int*>(smem + QSmem::kSlotOff + kMaxSlots * 8);
+    float* xs0 = reinterpret_cast<float*>(smem + QSmem::kXsumOff);
+    float* xs1 = reinterpret_cast<float*>(smem + p.xsum1_off);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + p.red_off);  // [NW * SW]
+    uint64_t* empty = full + NW * SW;
+    float* inv1 = reinterpret_cast<float*>(smem + p.round_off);
+    int* rows1 = reinterpret_cast<int*>(smem + p.round_off + 32);
+    int* npend = reinterpret_cast<int*>(smem + p.round_off + 64);      // [16]
+    int4* pending = reinterpret_cast<int4*>(smem + p.seg_off);         // [NW][pw] {problem, row block, split, k}
+    int* lastf = reinterpret_cast<int*>(smem + p.last_off);            // [NW][pw]
+    uint8_t* xb0 = smem + p.xraw_off;
+    uint8_t* xb1 = smem + p.xraw1_off;
+    uint8_t* ring = smem + p.stage_off;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int c = blockIdx.x;
+    const bool norm = p.gamma != nullptr;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < NW * SW; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_init(&xbar[0], 1);
+        mbar_init(&xbar[1], 1);
+        flags[0] = 0;
+        fence_mbar_init();
+    }
+    if (threadIdx.x < 16)
+        npend[threadIdx.x] = 0;
+    __syncthreads();
+    pdl_launch_dependents();
+
+    int P = p.P;
+    if constexpr (MOE) {
+        pdl_wait();
+        P = __ldcg(&p.meta->n_active);
+        for (int i = threadIdx.x; i < P; i += blockDim.x) {
+            slot_ec[i] = make_int2(__ldcg(&p.meta->slot[i].expert), __ldcg(&p.meta->slot[i].count));
+            for (int j = 0; j < kMaxM; ++j)
+                slot_rows[i * kMaxM + j] = p.gather ? __ldcg(&p.meta->slot[i].rows[j]) : j;
+        }
+        __syncthreads();
+    }
+    Part pt;
+    pt.per_p = p.n_rb * p.groups;
+    pt.per_ps = p.n_rb * p.Gs;
+    pt.Gs = p.Gs;
+    pt.aligned = p.aligned != 0;
+    pt.items = (int64_t)P * p.S * p.n_rb;
+    pt.U = pt.items * p.Gs;
+    const int W = (int)min((int64_t)p.C * NW, max(pt.aligned ? pt.items : pt.U, (int64_t)1));
+    pt.C = W;  // the partition is over workers
+    auto wrange = [&](int v, int64_t& a, int64_t& b) {
+        if (v < W) {
+            a = pt.start(v);
+            b = pt.start(v + 1);
+        } else {
+            a = b = 0;
+        }
+    };
+    // runs (problem, split) of this CTA: at most two (the host sizes work so)
+    const int64_t ca = pt.start(min(c * NW, W)), cb = pt.start(min(c * NW + NW, W));
+    const int run0 = ca < cb ? (int)(ca / pt.per_ps) : 0;  // = problem * S + split
+    const int run1 = ca < cb ? (int)((cb - 1) / pt.per_ps) : 0;
+    const bool two = !norm && run1 != run0;
+    if (run1 > run0 + 1) {  // never expected: every thread sees it and the CTA leaves untouched
+        if (threadIdx.x == 0)
+            atomicCAS(p.status, 0, TF_E_TIMEOUT);
+        return;
+    }
+
+    // walk helper: unit u -> (problem, split, row block, group in split)
+    auto decomp = [&](int64_t u, int& pp, int& ss, int& rb, int& gl) {
+        const int uu = (int)u;
+        pp = uu / pt.per_p;
+        int rem = uu - pp * pt.per_p;
+        ss = rem / pt.per_ps;
+        rem -= ss * pt.per_ps;
+        rb = rem / p.Gs;
+        gl = rem - rb * p.Gs;
+    };
+
+    // ------------------------------------------------------------ producer: lane w feeds worker w
+    if (warp == kConsumerWarps) {
+        if (lane < NW && !flags[0]) {
+            const uint64_t pol = policy_evict_first();
+            int64_t u, u1;
+            wrange(c * NW + lane, u, u1);
+            int k = 0;
+            bool ok = true;
+            if (u < u1) {
+                int pp, ss, rb, gl;
+                decomp(u, pp, ss, rb, gl);
+                while (u < u1 && ok) {
+                    const int len = (int)min((int64_t)(p.Gs - gl), u1 - u);
+                    const int64_t mbase = MOE ? (int64_t)slot_ec[pp].x * p.matrix_bytes : 0;
+                    const int64_t tile0 = (int64_t)rb * p.groups + ss * p.Gs + gl;
+                    for (int g = 0; g < len; g += T, ++k) {
+                        const int cnt = min(T, len - g);
+                        const int s = lane * SW + k % SW;
+                        if (!wait_or_abort(&empty[s], ((k / SW) & 1u) ^ 1u, flags, p.status, p.limit_ns)) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(&full[s], (uint32_t)(MATS * cnt * TILE));
+#pragma unroll
+                        for (int mat = 0; mat < MATS; ++mat)
+                            bulk_g2s(ring + s * slot_bytes + mat * T * TILE,
+                                     (mat ? p.w1 : p.w0) + mbase + (tile0 + g) * TILE, (uint32_t)(cnt * TILE), &full[s],
+                                     pol);
+                    }
+                    u += len;
+                    gl = 0;
+                    if (++rb == p.n_rb) {
+                        rb = 0;
+                        if (++ss == p.S) {
+                            ss = 0;
+                            ++pp;
+                        }
+                    }
+                }
+            }
+            // no copy may still be in flight when the CTA leaves
+            for (int q = max(0, k - SW); q < k; ++q)
+                wait_or_abort(&full[lane * SW + q % SW], (q / SW) & 1u, flags, p.status, p.limit_ns);
+        }
+        return;
+    }
+
+    // ------------------------------------------------------------ consumers
+    const int cw = warp;
+    const int gi = lane >> 2, tq = lane & 3;
+    if constexpr (!MOE)
+        pdl_wait();
+
+    // stage the activations of the CTA's runs (once)
+    const int S = p.S;
+    int M0 = p.M, M1 = p.M;
+    if (MOE) {
+        M0 = slot_ec[run0 / S].y;
+        M1 = slot_ec[run1 / S].y;
+    }
+    if (threadIdx.x < kMaxM) {
+        rows0[threadIdx.x] = MOE ? slot_rows[(run0 / S) * kMaxM + threadIdx.x] : (int)threadIdx.x;
+        rows1[threadIdx.x] = MOE ? slot_rows[(run1 / S) * kMaxM + threadIdx.x] : (int)threadIdx.x;
+    }
+    const int xg0_0 = norm ? 0 : (run0 % S) * p.Gs, xg0_1 = (run1 % S) * p.Gs;
+    const int xgc = norm ? p.groups : p.Gs;
+    bool alive = ca < cb && !flags[0];
+    if (cw == 0) {
+        __syncwarp();
+        if (lane == 0 && alive) {
+            x_issue(p, xb0, rows0, M0, MOE && !p.gather ? (int64_t)(run0 / S) * p.x_slot_stride : 0, xg0_0, xgc,
+                    &xbar[0]);
+            if (two)
+                x_issue(p, xb1, rows1, M1, MOE && !p.gather ? (int64_t)(run1 / S) * p.x_slot_stride : 0, xg0_1, xgc,
+                        &xbar[1]);
+        }
+    }
+    if (alive) {
+        bool ok = wait_or_abort(&xbar[0], 0, flags, p.status, p.limit_ns);
+        if (two)
+            ok = ok && wait_or_abort(&xbar[1], 0, flags, p.status, p.limit_ns);
+        alive = __all_sync(0xffffffffu, ok);
+    }
+    x_prepare(p, xb0, M0, xg0_0, norm ? 0 : xg0_0, norm ? p.groups : p.Gs, xs0, inv0, cw, lane, kConsumerWarps,
+              kBarConsumers);
+    if (two)
+        x_prepare(p, xb1, M1, xg0_1, xg0_1, p.Gs, xs1, inv1, cw, lane, kConsumerWarps, kBarConsumers);
+
+    if (cw < NW && alive) {
+        int64_t u, u1;
+        wrange(c * NW + cw, u, u1);
+        const int v = c * NW + cw;
+        int k = 0, np = 0;
+        if (u < u1) {
+            int pp, ss, rb, gl;
+            decomp(u, pp, ss, rb, gl);
+            while (u < u1 && alive) {
+                const int len = (int)min((int64_t)(p.Gs - gl), u1 - u);
+                const bool b1 = two && (pp * S + ss) == run1;
+                const uint8_t* xb = b1 ? xb1 : xb0;
+                const float* xs = b1 ? xs1 : xs0;
+                const int Mr = MOE ? slot_ec[pp].y : p.M;
+                const bool has_row = gi < Mr;
+                const int grel0 = norm ? ss * p.Gs + gl : gl;  // group of the buffer at the segment start
+                float acc0[4] = {0.f, 0.f, 0.f, 0.f}, acc1[4] = {0.f, 0.f, 0.f, 0.f};
+                for (int g = 0; g < len; g += T, ++k) {
+                    const int cnt = min(T, len - g);
+                    const int s = cw * SW + k % SW;
+                    bool ok = wait_or_abort(&full[s], (k / SW) & 1u, flags, p.status, p.limit_ns);
+                    if (!__all_sync(0xffffffffu, ok)) {
+                        alive = false;
+                        break;
+                    }
+                    const uint8_t* sb = ring + s * slot_bytes;
+                    for (int j = 0; j < cnt; ++j) {
+                        uint4 xa, xbv;
+                        x_frag(xb, p.x_rs, gi, tq, grel0 + g + j, has_row, xa, xbv);
+                        const float2 xsv = *reinterpret_cast<const float2*>(
+                            xs + (norm ? ss * p.Gs + gl + g + j : gl + g + j) * kMaxM + 2 * tq);
+                        tile_mac<BITS>(sb + j * TILE, lane, xa, xbv, xsv, acc0);
+                        if constexpr (DUAL)
+                            tile_mac<BITS>(sb + (T + j) * TILE, lane, xa, xbv, xsv, acc1);
+                    }
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive(&empty[s]);
+                }
+                if (!alive)
+                    break;
+                if (S == 1 && len == p.groups) {
+                    store_outputs<DUAL, MOE>(p, pp, Mr, rb * kRowsPerBlock, lane, acc0, acc1);
+                } else if (np < p.pw) {
+                    int kk = 0;
+                    if (!pt.aligned) {
+                        const int64_t f = (int64_t)pp * pt.per_p + (int64_t)ss * pt.per_ps + (int64_t)rb * p.Gs;
+                        kk = min(v - pt.cta_of(f), p.kmax - 1);  // k < kmax by construction
+                    }
+                    float4* dst = reinterpret_cast<float4*>(
+                        p.partials + (((((int64_t)pp * S + ss) * p.n_rb + rb) * p.kmax + kk) * 32 + lane) * VALS);
+                    __stcg(dst, make_float4(acc0[0], acc0[1], acc0[2], acc0[3]));
+                    if constexpr (DUAL)
+                        __stcg(dst + 1, make_float4(acc1[0], acc1[1], acc1[2], acc1[3]));
+                    if (lane == 0)
+                        pending[cw * p.pw + np] = make_int4(pp, rb, 0, 0);
+                    ++np;
+                } else {  // the host sizes the list; never expected
+                    if (lane == 0) {
+                        flags[0] = 1;
+                        atomicCAS(p.status, 0, TF_E_TIMEOUT);
+                    }
+                    alive = false;
+                    break;
+                }
+                u += len;
+                gl = 0;
+                if (++rb == p.n_rb) {
+                    rb = 0;
+                    if (++ss == S) {
+                        ss = 0;
+                        ++pp;
+                    }
+                }
+            }
+        }
+        if (lane == 0)
+            npend[cw] = np;
+    }
+
+    // abort is decided once for the whole CTA
+    named_bar_sync(kBarConsumers, kConsumerWarps * 32);
+    if (threadIdx.x == 0)
+        flags[1] = flags[0];
+    named_bar_sync(kBarConsumers, kConsumerWarps * 32);
+    if (flags[1]) {
+        if (cw == 0 && lane == 0 && ca < cb) {  // no activation copy may be left in flight
+            mbar_wait_bounded(&xbar[0], 0, p.limit_ns);
+            if (two)
+                mbar_wait_bounded(&xbar[1], 0, p.limit_ns);
+        }
+        return;
+    }
+
+    // ------------------------------------------------------------ last contributor of a row block sums it
+    int total = 0;
+    for (int w = 0; w < NW; ++w)
+        total += npend[w];
+    if (total == 0)
+        return;
+    __threadfence();
+    named_bar_sync(kBarConsumers, kConsumerWarps * 32);
+    for (int i = threadIdx.x; i < NW * p.pw; i += kConsumerWarps * 32) {
+        const int w = i / p.pw, j = i % p.pw;
+        int last = 0;
+        if (j < npend[w]) {
+            const int4 e = pending[i];
+            int expected = S;
+            if (!pt.aligned) {
+                expected = 0;
+                for (int s2 = 0; s2 < S; ++s2)
+                    expected += pt.contributors((int64_t)e.x * pt.per_p + (int64_t)s2 * pt.per_ps + (int64_t)e.y * p.Gs);
+            }
+            const int old = atomicAdd(&p.counters[(int64_t)e.x * p.n_rb + e.y], 1);
+            last = old == expected - 1;
+        }
+        lastf[i] = last;
+    }
+    named_bar_sync(kBarConsumers, kConsumerWarps * 32);
+    for (int i = cw; i < NW * p.pw; i += kConsumerWarps) {
+        if (!lastf[i])
+            continue;
+        const int4 e = pending[i];
+        __threadfence();
+        float t0[4] = {0.f, 0.f, 0.f, 0.f}, t1[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int s2 = 0; s2 < S; ++s2) {
+            const int kc = pt.aligned ? 1
+                                      : min(pt.contributors((int64_t)e.x * pt.per_p + (int64_t)s2 * pt.per_ps +
+                                                            (int64_t)e.y * p.Gs),
+                                            p.kmax);
+            for (int kq = 0; kq < kc; ++kq) {
+                float4* src = reinterpret_cast<float4*>(
+                    p.partials + (((((int64_t)e.x * S + s2) * p.n_rb + e.y) * p.kmax + kq) * 32 + lane) * VALS);
+                const float4 a = __ldcg(src);
+                __stcg(src, make_float4(0.f, 0.f, 0.f, 0.f));  // the workspace is left as it was found
+                t0[0] += a.x;
+                t0[1] += a.y;
+                t0[2] += a.z;
+                t0[3] += a.w;
+                if constexpr (DUAL) {
+                    const float4 b = __ldcg(src + 1);
+                    __stcg(src + 1, make_float4(0.f, 0.f, 0.f, 0.f));
+                    t1[0] += b.x;
+                    t1[1] += b.y;
+                    t1[2] += b.z;
+                    t1[3] += b.w;
+                }
+            }
+        }
+        const int Mr = MOE ? slot_ec[e.x].y : p.M;
+        store_outputs<DUAL, MOE>(p, e.x, Mr, e.y * kRowsPerBlock, lane, t0, t1);
+        if (lane == 0)
+            p.counters[(int64_t)e.x * p.n_rb + e.y] = 0;
+    }
+}
+
+template <int BITS, bool DUAL, bool MOE>
+cudaError_t launch_qproj_warp(const Plan& plan, const QProjParams& p, cudaStream_t stream, bool pdl)
+{
+    auto kern = qproj_warp_kernel<BITS, DUAL, MOE>;
+    static bool configured = false;
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+        if (e != cudaSuccess)
+            return e;
+        configured = true;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)plan.C, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = plan.smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
+template <int BITS, bool DUAL, bool MOE, int KW>
+cudaError_t launch_qproj_kw(const Plan& plan, const QProjParams& p, cudaStream_t stream, bool pdl)
+{
+    auto kern = qproj_kernel<BITS, DUAL, MOE, KW>;
+    static bool configured = false;
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+        if (e != cudaSuccess)
+            return e;
+        configured = true;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)plan.C, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = plan.smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
+template <int BITS, bool DUAL, bool MOE>
+cudaError_t launch_qproj_t(const Plan& plan, const QProjParams& p, cudaStream_t stream, bool pdl)
+{
+    if (plan.mode == 1)
+        return launch_qproj_warp<BITS, DUAL, MOE>(plan, p, stream, pdl);
+    switch (plan.KW) {
+    case 1: return launch_qproj_kw<BITS, DUAL, MOE, 1>(plan, p, stream, pdl);
+    case 2: return launch_qproj_kw<BITS, DUAL, MOE, 2>(plan, p, stream, pdl);
+    case 4: return launch_qproj_kw<BITS, DUAL, MOE, 4>(plan, p, stream, pdl);
+    case 8: return launch_qproj_kw<BITS, DUAL, MOE, 8>(plan, p, stream, pdl);
+    case 16: return launch_qproj_kw<BITS, DUAL, MOE, 16>(plan, p, stream, pdl);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace tfq

@@ -1,0 +1,358 @@
+"""ctypes binding over libtfq.so (include/tfq.h), same names as the C ABI.
+
+Argument marshalling only: every step of the computation runs in the CUDA
+library. Tensors are torch tensors on a CUDA device; bf16 activations may be
+``torch.bfloat16`` or 16-bit integer tensors holding bf16 bit patterns. The
+library is required: importing this module without a built ``libtfq.so``
+raises, there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+TF_OK = 0
+TF_E_INVALID_ARG = 1
+TF_E_UNSUPPORTED_SHAPE = 2
+TF_E_WORKSPACE_TOO_SMALL = 3
+TF_E_BAD_PACK = 4
+TF_E_CUDA = 5
+TF_E_TIMEOUT = 6
+TF_DTYPE_BF16 = 0
+TF_DTYPE_F32 = 1
+TF_RUN_PDL = 1
+TF_TUNE_ROWBLOCKS = 0
+TF_TUNE_SPLITK = 1
+TF_TUNE_STAGE_GROUPS = 2
+TF_TUNE_STAGES = 3
+TF_TUNE_WARPS = 4
+TF_TUNE_MODE = 5
+
+P = ctypes.c_void_p
+I64 = ctypes.c_int64
+I32 = ctypes.c_int32
+SZ = ctypes.c_size_t
+
+
+class tf_qweight(ctypes.Structure):
+    _fields_ = [("magic", ctypes.c_uint32), ("version", ctypes.c_uint32), ("bits", I32), ("group", I32),
+                ("batch", I64), ("N", I64), ("K", I64), ("n_pad", I64), ("tile_bytes", I64),
+                ("matrix_bytes", I64), ("data", P)]
+
+
+class tf_decoder_layer(ctypes.Structure):
+    _fields_ = [("qkv", tf_qweight), ("o", tf_qweight), ("gate", tf_qweight), ("up", tf_qweight),
+                ("down", tf_qweight), ("attn_norm", P), ("mlp_norm", P)]
+
+
+class tf_decoder_desc(ctypes.Structure):
+    _fields_ = [("n_layers", I32), ("d_model", I64), ("d_ff", I64), ("q_dim", I64), ("kv_dim", I64),
+                ("vocab", I64), ("eps", ctypes.c_float), ("layers", ctypes.POINTER(tf_decoder_layer)),
+                ("final_norm", P), ("readout", tf_qweight)]
+
+
+class TfqError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"{status_str(status)}: {msg}")
+        self.status = status
+
+
+_lib = None
+
+# name -> (restype, argtypes); mirrors include/tfq.h
+_SIGS = {
+    "tf_status_str": (ctypes.c_char_p, [ctypes.c_int]),
+    "tf_last_error": (ctypes.c_char_p, []),
+    "tf_version": (ctypes.c_int, []),
+    "tf_qlinear_packed_bytes": (SZ, [I64, I64, I64, ctypes.c_int, ctypes.c_int]),
+    "tf_qlinear_pack": (ctypes.c_int, [P, P, P, I64, I64, I64, ctypes.c_int, ctypes.c_int, P, SZ,
+                                       ctypes.POINTER(tf_qweight), P]),
+    "tf_qlinear_unpack_debug": (ctypes.c_int, [ctypes.POINTER(tf_qweight), P, P, P, P]),
+    "tf_qweight_check": (ctypes.c_int, [ctypes.POINTER(tf_qweight), P]),
+    "tf_qlinear_workspace_bytes": (SZ, [ctypes.POINTER(tf_qweight), I64]),
+    "tf_qlinear_run": (ctypes.c_int, [ctypes.POINTER(tf_qweight), P, I64, I64, P, ctypes.c_float, P, P,
+                                      ctypes.c_int, P, SZ, ctypes.c_uint, P]),
+    "tf_qmlp_gateup_workspace_bytes": (SZ, [ctypes.POINTER(tf_qweight), ctypes.POINTER(tf_qweight), I64]),
+    "tf_qmlp_gateup_run": (ctypes.c_int, [ctypes.POINTER(tf_qweight), ctypes.POINTER(tf_qweight), P, I64, I64,
+                                          P, ctypes.c_float, P, P, SZ, ctypes.c_uint, P]),
+    "tf_qmoe_workspace_bytes": (SZ, [ctypes.POINTER(tf_qweight)] * 3 + [I64, ctypes.c_int]),
+    "tf_qmoe_run": (ctypes.c_int, [ctypes.POINTER(tf_qweight)] * 3 + [P, I64, ctypes.c_int, P, P, P, P, P, SZ,
+                                                                        ctypes.c_uint, P]),
+    "tf_decode_step_workspace_bytes": (SZ, [ctypes.POINTER(tf_decoder_desc), I64]),
+    "tf_decode_step_debug_elems": (SZ, [ctypes.POINTER(tf_decoder_desc), I64]),
+    "tf_decode_step_run": (ctypes.c_int, [ctypes.POINTER(tf_decoder_desc), P, I64, P, P, SZ, P, ctypes.c_uint,
+                                          P]),
+    "tf_workspace_status": (ctypes.c_int, [P, P]),
+    "tf_selftest_wait_timeout": (ctypes.c_int, [P, ctypes.c_uint64, P]),
+    "tf_tune_set": (ctypes.c_int, [ctypes.c_int, ctypes.c_int]),
+}
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def lib():
+    """Load libtfq.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        path = library_path()
+        if not os.path.exists(path):
+            raise RuntimeError(f"libtfq.so is not built ({path}); run skinny_gemm_bit_gb300.build.build()")
+        L = ctypes.CDLL(path)
+        for name, (res, args) in _SIGS.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = L
+    return _lib
+
+
+def status_str(status: int) -> str:
+    return lib().tf_status_str(status).decode()
+
+
+def last_error() -> str:
+    return lib().tf_last_error().decode()
+
+
+def _check(rc: int):
+    if rc != TF_OK:
+        raise TfqError(rc, last_error())
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def tune_set(key: int, value: int):
+    _check(lib().tf_tune_set(key, value))
+
+
+# ---------------------------------------------------------------------------- packing
+
+class QWeight:
+    """A packed weight buffer (device) and its host descriptor."""
+
+    def __init__(self, buf: torch.Tensor, desc: tf_qweight):
+        self.buf = buf
+        self.desc = desc
+
+    @property
+    def N(self):
+        return self.desc.N
+
+    @property
+    def K(self):
+        return self.desc.K
+
+    @property
+    def bits(self):
+        return self.desc.bits
+
+    @property
+    def batch(self):
+        return self.desc.batch
+
+    def weight_bytes(self) -> int:
+        """Algorithmic bytes of the codes, scales and biases (excluding row padding)."""
+        return int(self.batch * self.N * self.K * (self.bits / 8 + 4 / 64))
+
+
+def packed_bytes(batch: int, N: int, K: int, bits: int, group: int = 64) -> int:
+    return lib().tf_qlinear_packed_bytes(batch, N, K, bits, group)
+
+
+def _as_dev(a, dtype, device):
+    if isinstance(a, torch.Tensor):
+        return a.to(device=device).contiguous()
+    import numpy as np
+    arr = np.ascontiguousarray(a)
+    if arr.dtype == np.uint32:
+        arr = arr.view(np.int32)
+    elif arr.dtype == np.uint16:
+        arr = arr.view(np.int16)
+    return torch.from_numpy(arr).to(device=device)
+
+
+def tf_qlinear_pack(wq, scales, biases, bits: int, device="cuda", stream=None) -> QWeight:
+    """Pack MLX-layout weights ([B,] N, K*bits/32 uint32; [B,] N, K/64 bf16) into a QWeight."""
+    wq = _as_dev(wq, torch.int32, device)
+    scales = _as_dev(scales, torch.int16, device)
+    biases = _as_dev(biases, torch.int16, device)
+    batched = wq.dim() == 3
+    batch = wq.shape[0] if batched else 1
+    N = wq.shape[-2]
+    K = wq.shape[-1] * 32 // bits
+    nbytes = packed_bytes(batch, N, K, bits)
+    if nbytes == 0:
+        raise TfqError(TF_E_UNSUPPORTED_SHAPE, f"unsupported packing N={N} K={K} bits={bits}")
+    buf = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    desc = tf_qweight()
+    _check(lib().tf_qlinear_pack(_ptr(wq), _ptr(scales), _ptr(biases), batch, N, K, bits, 64, _ptr(buf), nbytes,
+                                 ctypes.byref(desc), _stream(stream)))
+    torch.cuda.current_stream().synchronize() if stream is None else stream.synchronize()
+    return QWeight(buf, desc)
+
+
+def tf_qlinear_unpack_debug(w: QWeight, stream=None):
+    """(wq int32, scales int16, biases int16) in MLX layout, read back out of the packed buffer."""
+    dev = w.buf.device
+    lead = (w.batch,) if w.batch > 1 else ()
+    wq = torch.empty(lead + (w.N, w.K * w.bits // 32), dtype=torch.int32, device=dev)
+    s = torch.empty(lead + (w.N, w.K // 64), dtype=torch.int16, device=dev)
+    b = torch.empty_like(s)
+    _check(lib().tf_qlinear_unpack_debug(ctypes.byref(w.desc), _ptr(wq), _ptr(s), _ptr(b), _stream(stream)))
+    return wq, s, b
+
+
+def tf_qweight_check(w: QWeight, stream=None):
+    _check(lib().tf_qweight_check(ctypes.byref(w.desc), _stream(stream)))
+
+
+# ---------------------------------------------------------------------------- workspaces
+
+def workspace(nbytes: int, device="cuda") -> torch.Tensor:
+    """A zero-filled workspace (256-byte aligned by the caching allocator)."""
+    return torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
+def tf_qlinear_workspace_bytes(w: QWeight, M: int = 8) -> int:
+    return lib().tf_qlinear_workspace_bytes(ctypes.byref(w.desc), M)
+
+
+def tf_qmlp_gateup_workspace_bytes(gate: QWeight, up: QWeight, M: int = 8) -> int:
+    return lib().tf_qmlp_gateup_workspace_bytes(ctypes.byref(gate.desc), ctypes.byref(up.desc), M)
+
+
+def tf_qmoe_workspace_bytes(gate: QWeight, up: QWeight, down: QWeight, M: int, top_k: int) -> int:
+    return lib().tf_qmoe_workspace_bytes(ctypes.byref(gate.desc), ctypes.byref(up.desc), ctypes.byref(down.desc),
+                                         M, top_k)
+
+
+def tf_workspace_status(ws: torch.Tensor, stream=None) -> int:
+    return lib().tf_workspace_status(_ptr(ws), _stream(stream))
+
+
+def tf_selftest_wait_timeout(ws: torch.Tensor, limit_ns: int, stream=None):
+    _check(lib().tf_selftest_wait_timeout(_ptr(ws), limit_ns, _stream(stream)))
+
+
+# ---------------------------------------------------------------------------- projections
+
+def _rows(x: torch.Tensor):
+    if x.dim() != 2:
+        raise ValueError("activations must be 2-D [M, K]")
+    return x.shape[0], x.stride(0)
+
+
+def tf_qlinear_run(w: QWeight, x: torch.Tensor, gamma=None, eps: float = 1e-6, residual=None, out=None,
+                   out_dtype=torch.bfloat16, ws=None, flags: int = 0, stream=None) -> torch.Tensor:
+    """y = (residual +) rmsnorm?(x) . dequant(W)^T for x [M, K] (M <= 8)."""
+    M, ldx = _rows(x)
+    if out is None:
+        out = torch.empty((M, w.N), dtype=out_dtype, device=x.device)
+    ydt = TF_DTYPE_F32 if out.dtype == torch.float32 else TF_DTYPE_BF16
+    if ws is None:
+        ws = workspace(tf_qlinear_workspace_bytes(w, M), x.device)
+    _check(lib().tf_qlinear_run(ctypes.byref(w.desc), _ptr(x), ldx, M, _ptr(gamma), eps, _ptr(residual), _ptr(out),
+                                ydt, _ptr(ws), ws.numel(), flags, _stream(stream)))
+    return out
+
+
+def tf_qmlp_gateup_run(gate: QWeight, up: QWeight, x: torch.Tensor, gamma=None, eps: float = 1e-6, out=None,
+                       ws=None, flags: int = 0, stream=None) -> torch.Tensor:
+    """h = silu(xn . G^T) * (xn . U^T), xn = rmsnorm(x) when gamma is given."""
+    M, ldx = _rows(x)
+    if out is None:
+        out = torch.empty((M, gate.N), dtype=torch.bfloat16, device=x.device)
+    if ws is None:
+        ws = workspace(tf_qmlp_gateup_workspace_bytes(gate, up, M), x.device)
+    _check(lib().tf_qmlp_gateup_run(ctypes.byref(gate.desc), ctypes.byref(up.desc), _ptr(x), ldx, M, _ptr(gamma),
+                                    eps, _ptr(out), _ptr(ws), ws.numel(), flags, _stream(stream)))
+    return out
+
+
+def tf_qmoe_run(gate: QWeight, up: QWeight, down: QWeight, logits: torch.Tensor, x: torch.Tensor, top_k: int,
+                out=None, idx=None, wts=None, ws=None, flags: int = 0, stream=None):
+    """(y [M, H] bf16, topk_idx [M, k] int32, topk_w [M, k] fp32)."""
+    M = x.shape[0]
+    dev = x.device
+    if out is None:
+        out = torch.empty((M, gate.K), dtype=torch.bfloat16, device=dev)
+    if idx is None:
+        idx = torch.empty((M, top_k), dtype=torch.int32, device=dev)
+    if wts is None:
+        wts = torch.empty((M, top_k), dtype=torch.float32, device=dev)
+    if ws is None:
+        ws = workspace(tf_qmoe_workspace_bytes(gate, up, down, M, top_k), dev)
+    _check(lib().tf_qmoe_run(ctypes.byref(gate.desc), ctypes.byref(up.desc), ctypes.byref(down.desc), _ptr(logits),
+                             M, top_k, _ptr(x), _ptr(out), _ptr(idx), _ptr(wts), _ptr(ws), ws.numel(), flags,
+                             _stream(stream)))
+    return out, idx, wts
+
+
+# ---------------------------------------------------------------------------- decoder step
+
+class Decoder:
+    """Packed weights of a dense decoder's projections and the host descriptor over them."""
+
+    def __init__(self, layers, final_norm: torch.Tensor, readout: QWeight, d_model: int, d_ff: int, q_dim: int,
+                 kv_dim: int, eps: float = 1e-6):
+        self.layers = layers            # list of dicts: qkv, o, gate, up, down (QWeight), attn_norm, mlp_norm
+        self.final_norm = final_norm
+        self.readout = readout
+        arr = (tf_decoder_layer * max(1, len(layers)))()
+        for i, L in enumerate(layers):
+            arr[i].qkv = L["qkv"].desc
+            arr[i].o = L["o"].desc
+            arr[i].gate = L["gate"].desc
+            arr[i].up = L["up"].desc
+            arr[i].down = L["down"].desc
+            arr[i].attn_norm = L["attn_norm"].data_ptr()
+            arr[i].mlp_norm = L["mlp_norm"].data_ptr()
+        self._arr = arr
+        d = tf_decoder_desc()
+        d.n_layers = len(layers)
+        d.d_model, d.d_ff, d.q_dim, d.kv_dim, d.vocab = d_model, d_ff, q_dim, kv_dim, readout.N
+        d.eps = eps
+        d.layers = ctypes.cast(arr, ctypes.POINTER(tf_decoder_layer))
+        d.final_norm = final_norm.data_ptr()
+        d.readout = readout.desc
+        self.desc = d
+
+    def weight_bytes(self) -> int:
+        total = self.readout.weight_bytes()
+        for L in self.layers:
+            total += sum(L[k].weight_bytes() for k in ("qkv", "o", "gate", "up", "down"))
+        return total
+
+
+def tf_decode_step_workspace_bytes(dec: Decoder, M: int) -> int:
+    return lib().tf_decode_step_workspace_bytes(ctypes.byref(dec.desc), M)
+
+
+def tf_decode_step_debug_elems(dec: Decoder, M: int) -> int:
+    return lib().tf_decode_step_debug_elems(ctypes.byref(dec.desc), M)
+
+
+def tf_decode_step_run(dec: Decoder, x: torch.Tensor, out=None, ws=None, debug=None, flags: int = 0,
+                       stream=None) -> torch.Tensor:
+    """logits [M, vocab] bf16 of one decoder step over the residual stream x [M, d_model]."""
+    M = x.shape[0]
+    if out is None:
+        out = torch.empty((M, dec.readout.N), dtype=torch.bfloat16, device=x.device)
+    if ws is None:
+        ws = workspace(tf_decode_step_workspace_bytes(dec, M), x.device)
+    _check(lib().tf_decode_step_run(ctypes.byref(dec.desc), _ptr(x), M, _ptr(out), _ptr(ws), ws.numel(),
+                                    _ptr(debug), flags, _stream(stream)))
+    return out
