@@ -93,6 +93,7 @@ void fill_common(QProjParams& p, const Plan& pl, void* ws, uint8_t* scratch)
     p.pw = pl.pw;
     p.xsum1_off = pl.xsum1_off;
     p.xraw1_off = pl.xraw1_off;
+    p.gamma_off = pl.gamma_off;
     p.xraw_off = pl.xraw_off;
     p.x_rs = pl.x_rs;
     p.stage_off = pl.stage_off;
@@ -207,7 +208,8 @@ Plan plan_qproj(int n_rb, int groups, int mats, int bits, int slots, int k_full,
     pl.seg_off = (int)align_up(pl.red_off + (size_t)kConsumerWarps * 32 * vals * 4, 128);
     pl.round_off = (int)align_up(pl.seg_off + (size_t)pl.segmax * 16, 128);
     pl.last_off = (int)align_up(pl.round_off + (size_t)(pl.segmax + 1) * 8, 128);
-    pl.xraw_off = (int)align_up(pl.last_off + (size_t)pl.segmax * 4, 128);
+    pl.gamma_off = (int)align_up(pl.last_off + (size_t)pl.segmax * 4, 128);
+    pl.xraw_off = (int)align_up(pl.gamma_off + (size_t)std::max(k_full, 0) * 2, 128);
     const int xcols = k_full > 0 ? k_full : pl.Gs * kGroup;
     pl.x_rs = xcols * 2 + 64;
     pl.stage_off = (int)align_up(pl.xraw_off + (size_t)rows * pl.x_rs, 128);
@@ -218,6 +220,43 @@ Plan plan_qproj(int n_rb, int groups, int mats, int bits, int slots, int k_full,
         nst = std::min(g_tune[TF_TUNE_STAGES], nst);
     pl.nst = std::max(nst, 1);
     pl.smem = pl.stage_off + (size_t)pl.nst * stage;
+
+    // ---- small calls (latency-bound): light teams, one whole item per CTA, the item
+    // fetched in one stage, small enough for several CTAs (and the next kernel's) per SM
+    const bool light_ok = S == 1 && items <= 4LL * sms && (double)U * tile * mats <= 8.0 * 1024 * 1024;
+    bool light = light_ok && g_tune[TF_TUNE_MODE] <= 0;
+    if (g_tune[TF_TUNE_MODE] == 3)
+        light = light_ok;
+    if (light) {
+        pl.nw = 8;
+        pl.C = (int)std::max<int64_t>(items, 1);
+        pl.aligned = 1;
+        pl.kmax = 1;
+        pl.segmax = 1;
+        int KW = 8;
+        while (KW > 1 && pl.Gs < 2 * KW)
+            KW /= 2;
+        pl.KW = KW;
+        pl.R = 8 / KW;
+        pl.cg = pl.Gs;
+        pl.nst = 1;
+        const size_t stage = (size_t)mats * pl.R * pl.cg * tile;
+        const size_t fixed = 256 + kMaxSlots * 8 + kMaxSlots * kMaxM * 4;
+        pl.red_off = (int)align_up(fixed + (size_t)pl.Gs * kMaxM * 4, 128);
+        pl.seg_off = (int)align_up(pl.red_off + (size_t)8 * 32 * vals * 4, 128);
+        pl.round_off = (int)align_up(pl.seg_off + 16, 128);
+        pl.last_off = (int)align_up(pl.round_off + 16, 128);
+        pl.gamma_off = (int)align_up(pl.last_off + 4, 128);
+        pl.xraw_off = (int)align_up(pl.gamma_off + (size_t)std::max(k_full, 0) * 2, 128);
+        const int xcols = k_full > 0 ? k_full : pl.Gs * kGroup;
+        pl.x_rs = xcols * 2 + 64;
+        pl.stage_off = (int)align_up(pl.xraw_off + (size_t)rows * pl.x_rs, 128);
+        pl.smem = pl.stage_off + stage;
+        pl.ws_counters = 0;
+        pl.ws_partials = 0;
+        return pl;
+    }
+    pl.nw = kConsumerWarps;
 
     // ---- bandwidth-bound calls: warp workers with private ring slots
     const int nw = g_tune[TF_TUNE_WARPS] > 0 ? std::min(g_tune[TF_TUNE_WARPS], kConsumerWarps) : kConsumerWarps;
@@ -261,7 +300,8 @@ Plan plan_qproj(int n_rb, int groups, int mats, int bits, int slots, int k_full,
         pl.round_off = (int)align_up(pl.red_off + (size_t)2 * nw * kMaxStages * 8, 128);  // inv1, rows1, npend
         pl.seg_off = (int)align_up(pl.round_off + 128, 128);                              // pending
         pl.last_off = (int)align_up(pl.seg_off + (size_t)nw * pl.pw * 16, 128);
-        pl.xraw_off = (int)align_up(pl.last_off + (size_t)nw * pl.pw * 4, 128);
+        pl.gamma_off = (int)align_up(pl.last_off + (size_t)nw * pl.pw * 4, 128);
+        pl.xraw_off = (int)align_up(pl.gamma_off + (size_t)std::max(k_full, 0) * 2, 128);
         const int xcols = norm ? k_full : pl.Gs * kGroup;
         pl.x_rs = xcols * 2 + 64;
         pl.xraw1_off = (int)align_up(pl.xraw_off + (size_t)rows * pl.x_rs, 128);

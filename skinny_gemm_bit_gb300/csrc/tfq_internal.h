@@ -84,13 +84,14 @@ struct QProjParams {
     int red_off, seg_off, round_off, last_off, xraw_off, x_rs, stage_off;  // shared-memory layout (bytes)
     // warp mode: active consumer warps, pending capacity per warp, second activation buffer
     int nw, pw, xsum1_off, xraw1_off;
+    int gamma_off;  // staged RMSNorm weight (K bf16)
 };
 
 struct Plan {
     int mode;  // 0: teams in lock-step (latency-bound calls), 1: warp workers (bandwidth-bound calls)
     int KW, R, S, Gs, cg, nst, C, aligned, kmax, segmax, slots;
     int red_off, seg_off, round_off, last_off, xraw_off, x_rs, stage_off;
-    int nw, pw, xsum1_off, xraw1_off;
+    int nw, pw, xsum1_off, xraw1_off, gamma_off;
     size_t smem;
     size_t ws_partials;      // bytes
     size_t ws_counters;      // bytes

@@ -146,14 +146,18 @@ __device__ __forceinline__ void tile_mac(const uint8_t* tile, int lane, const ui
 // the natural order (columns 16 kb + 8 j + 2 t + {0,1}) moves to
 // 16 (kb >> 1) + 4 t + 2 (kb & 1) + j.
 
-// One thread: copy the rows into the buffer; completion on `bar`.
-__device__ __forceinline__ void x_issue(const QProjParams& p, uint8_t* buf, const int* rows, int Mrows, int64_t xbase,
-                                        int xg0, int xgc, uint64_t* bar)
+// One thread: copy the rows into the buffer (and, with an RMSNorm, gamma into
+// gbuf); completion on `bar`.
+__device__ __forceinline__ void x_issue(const QProjParams& p, uint8_t* buf, uint8_t* gbuf, const int* rows, int Mrows,
+                                        int64_t xbase, int xg0, int xgc, uint64_t* bar)
 {
-    mbar_arrive_expect_tx(bar, (uint32_t)(Mrows * xgc * 128));
+    const bool norm = p.gamma != nullptr;
+    mbar_arrive_expect_tx(bar, (uint32_t)(Mrows * xgc * 128 + (norm ? p.K * 2 : 0)));
     for (int m = 0; m < Mrows; ++m)
         bulk_g2s_plain(buf + m * p.x_rs, p.x + xbase + (int64_t)rows[m] * p.ldx + (int64_t)xg0 * kGroup,
                        (uint32_t)(xgc * 128), bar);
+    if (norm)
+        bulk_g2s_plain(gbuf, p.gamma, (uint32_t)(p.K * 2), bar);
 }
 
 // Consumer warps (nwarps of them, named barrier bar_id): after the copy has landed,
@@ -161,37 +165,41 @@ __device__ __forceinline__ void x_issue(const QProjParams& p, uint8_t* buf, cons
 // groups [g_lo, g_lo + ng) of the problem (staged from group xg0): normalise and
 // round to bf16 in place, group sums of the rounded values into xs[(g - g_lo) * 8 + m]
 // (zero for rows >= Mrows), and reorder to B-fragment order.
-__device__ __forceinline__ void x_prepare(const QProjParams& p, uint8_t* buf, int Mrows, int xg0, int g_lo, int ng,
-                                          float* xs, float* inv_rms, int cw, int lane, int nwarps, int bar_id)
+__device__ __forceinline__ void x_prepare(const QProjParams& p, uint8_t* buf, const uint8_t* gbuf, int Mrows, int xg0,
+                                          int g_lo, int ng, float* xs, float* inv_rms, int cw, int lane, int nwarps,
+                                          int bar_id)
 {
     const bool norm = p.gamma != nullptr;
     if (norm) {
         for (int m = cw; m < Mrows; m += nwarps) {
             const uint4* row = reinterpret_cast<const uint4*>(buf + m * p.x_rs);
-            float ss = 0.f;
+            float sq[4] = {0.f, 0.f, 0.f, 0.f};
             for (int i = lane; i < p.K / 8; i += 32) {
                 const uint4 v = row[i];
                 const uint32_t vv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     const float a = bf16lo_f32(vv[q]), b = bf16hi_f32(vv[q]);
-                    ss = fmaf(a, a, ss);
-                    ss = fmaf(b, b, ss);
+                    sq[q] = fmaf(b, b, fmaf(a, a, sq[q]));
                 }
             }
-            ss = warp_sum(ss);
+            float ss = warp_sum((sq[0] + sq[1]) + (sq[2] + sq[3]));
             if (lane == 0)
                 inv_rms[m] = rsqrtf(ss / (float)p.K + p.eps);
         }
         named_bar_sync(bar_id, nwarps * 32);
     }
-    // a lane handles one 8-column chunk cc = 2 kb + j of one (group, row)
-    for (int base = cw * 4; base < ng * kMaxM; base += nwarps * 4) {
+    // group sums of the rows that are not there are zero
+    for (int i = cw * 32 + lane; i < ng * kMaxM; i += nwarps * 32)
+        if ((i & 7) >= Mrows)
+            xs[i] = 0.f;
+    // a lane handles one 8-column chunk cc = 2 kb + j of one (group, live row)
+    for (int base = cw * 4; base < ng * Mrows; base += nwarps * 4) {
         const int pi = base + (lane >> 3);
         const int cc = lane & 7;
-        const int gl = pi >> 3, m = pi & 7;
-        const bool valid = pi < ng * kMaxM;
-        const bool live = valid && m < Mrows;
+        const int gl = pi / Mrows, m = pi - gl * Mrows;
+        const bool valid = pi < ng * Mrows;
+        const bool live = valid;
         float part = 0.f;
         uint32_t vv[4] = {0u, 0u, 0u, 0u};
         uint32_t* blk = reinterpret_cast<uint32_t*>(buf + m * p.x_rs + (g_lo - xg0 + gl) * 128);
@@ -202,8 +210,7 @@ __device__ __forceinline__ void x_prepare(const QProjParams& p, uint8_t* buf, in
             vv[2] = v.z;
             vv[3] = v.w;
             if (norm) {
-                const uint4 gv =
-                    __ldg(reinterpret_cast<const uint4*>(p.gamma + (int64_t)(g_lo + gl) * kGroup + cc * 8));
+                const uint4 gv = *reinterpret_cast<const uint4*>(gbuf + ((g_lo + gl) * kGroup + cc * 8) * 2);
                 const uint32_t gg[4] = {gv.x, gv.y, gv.z, gv.w};
                 const float inv = inv_rms[m];
 #pragma unroll
@@ -296,14 +303,15 @@ struct Part {
 
 constexpr int kBarConsumers = 15;  // named barrier of all consumer warps; 1..8 are team barriers
 
-template <int BITS, bool DUAL, bool MOE, int KW>
-__global__ void __launch_bounds__(kThreads, 1) qproj_kernel(const __grid_constant__ QProjParams p)
+// Light teams (NWT = 8) run two CTAs per SM (and leave room for the next kernel's).
+template <int BITS, bool DUAL, bool MOE, int KW, int NWT>
+__global__ void __launch_bounds__((NWT + 1) * 32, NWT == 8 ? 2 : 1) qproj_kernel(const __grid_constant__ QProjParams p)
 {
-    constexpr int R = kConsumerWarps / KW;
+    constexpr int R = NWT / KW;
     constexpr int MATS = DUAL ? 2 : 1;
     constexpr int TILE = tile_bytes_for(BITS);
     constexpr int VALS = DUAL ? 8 : 4;
-    constexpr int NCT = kConsumerWarps * 32;
+    constexpr int NCT = NWT * 32;
 
     extern __shared__ __align__(128) uint8_t smem[];
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + QSmem::kFullOff);
@@ -330,7 +338,7 @@ __global__ void __launch_bounds__(kThreads, 1) qproj_kernel(const __grid_constan
     if (threadIdx.x == 0) {
         for (int s = 0; s < p.nst; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], kConsumerWarps);
+            mbar_init(&empty[s], NWT);
         }
         mbar_init(xbar, 1);
         flags[0] = 0;
@@ -358,7 +366,16 @@ __global__ void __launch_bounds__(kThreads, 1) qproj_kernel(const __grid_constan
     pt.items = (int64_t)P * p.S * p.n_rb;
     pt.U = pt.items * p.Gs;
     pt.C = (int)min((int64_t)p.C, max(pt.aligned ? pt.items : pt.U, (int64_t)1));
-    const int64_t u0 = c < pt.C ? pt.start(c) : 0, u1 = c < pt.C ? pt.start(c + 1) : 0;
+    int64_t u0 = 0, u1 = 0;
+    if (c < pt.C) {  // CTAs past the work (fewer MoE slots active than planned for) stay idle
+        if (pt.aligned && pt.C == pt.items) {  // one item per CTA: no division
+            u0 = (int64_t)c * p.Gs;
+            u1 = u0 + p.Gs;
+        } else {
+            u0 = pt.start(c);
+            u1 = pt.start(c + 1);
+        }
+    }
 
     // ---- this CTA's segments (maximal runs inside one row block) and rounds (up to R
     // consecutive segments of one (problem, split)); built once, read by every warp
@@ -366,12 +383,18 @@ __global__ void __launch_bounds__(kThreads, 1) qproj_kernel(const __grid_constan
         int nseg = 0, nround = 0, rlen = 0, rp = -1, rs = -1, rmax = 0;
         if (u0 < u1) {
             const int uu = (int)u0;  // units fit in 30 bits (checked on the host)
-            int pp = uu / pt.per_p;
-            int rem = uu - pp * pt.per_p;
-            int ss = rem / pt.per_ps;
-            rem -= ss * pt.per_ps;
-            int rb = rem / p.Gs;
-            int gl = rem - rb * p.Gs;
+            int pp = 0, ss = 0, rb, gl;
+            if (pt.items == p.n_rb && pt.aligned && pt.C == pt.items) {  // one row block per CTA
+                rb = c;
+                gl = 0;
+            } else {
+                pp = uu / pt.per_p;
+                int rem = uu - pp * pt.per_p;
+                ss = rem / pt.per_ps;
+                rem -= ss * pt.per_ps;
+                rb = rem / p.Gs;
+                gl = rem - rb * p.Gs;
+            }
             int64_t u = u0;
             while (u < u1 && nseg < p.segmax) {
                 const int len = (int)min((int64_t)(p.Gs - gl), u1 - u);
@@ -411,7 +434,7 @@ __global__ void __launch_bounds__(kThreads, 1) qproj_kernel(const __grid_constan
     const int nseg = counts[0], nround = counts[1];
 
     // ------------------------------------------------------------ producer
-    if (warp == kConsumerWarps) {
+    if (warp == NWT) {
         if (lane == 0) {
             const uint64_t pol = policy_evict_first();
             int st_global = 0;
@@ -480,14 +503,14 @@ __global__ void __launch_bounds__(kThreads, 1) qproj_kernel(const __grid_constan
             if (cw == 0) {
                 __syncwarp();
                 if (lane == 0 && !flags[0])
-                    x_issue(p, xraw, rowsel, Mrows, MOE && !p.gather ? (int64_t)first.x * p.x_slot_stride : 0, xg0, xgc,
-                            xbar);
+                    x_issue(p, xraw, smem + p.gamma_off, rowsel, Mrows,
+                            MOE && !p.gather ? (int64_t)first.x * p.x_slot_stride : 0, xg0, xgc, xbar);
             }
             bool ok = alive && wait_or_abort(xbar, (uint32_t)xphase, flags, p.status, p.limit_ns);
             xphase ^= 1;
             ++nstaged;
             alive = __all_sync(0xffffffffu, ok);
-            x_prepare(p, xraw, Mrows, xg0, first.y * p.Gs, p.Gs, xsum, inv_rms, cw, lane, kConsumerWarps,
+            x_prepare(p, xraw, smem + p.gamma_off, Mrows, xg0, first.y * p.Gs, p.Gs, xsum, inv_rms, cw, lane, NWT,
                       kBarConsumers);
             cur_p = first.x;
             cur_s = first.y;
@@ -570,6 +593,11 @@ __global__ void __launch_bounds__(kThreads, 1) qproj_kernel(const __grid_constan
         }
     }
 
+    if (p.S == 1 && pt.aligned) {  // every segment was a whole row block, stored above
+        if (flags[0] && cw == 0 && lane == 0 && nstaged > 0)
+            mbar_wait_bounded(xbar, (uint32_t)(xphase ^ 1), p.limit_ns);  // no copy left in flight
+        return;
+    }
     // abort is decided once for the whole CTA: every consumer warp reads one snapshot
     named_bar_sync(kBarConsumers, NCT);
     if (threadIdx.x == 0)
@@ -608,7 +636,7 @@ __global__ void __launch_bounds__(kThreads, 1) qproj_kernel(const __grid_constan
         lastf[i] = last;
     }
     named_bar_sync(kBarConsumers, NCT);
-    for (int i = cw; i < nseg; i += kConsumerWarps) {
+    for (int i = cw; i < nseg; i += NWT) {
         if (!lastf[i])
             continue;
         const int4 e = segs[i];
@@ -827,11 +855,11 @@ __global__ void __launch_bounds__(kThreads, 1) qproj_warp_kernel(const __grid_co
     if (cw == 0) {
         __syncwarp();
         if (lane == 0 && alive) {
-            x_issue(p, xb0, rows0, M0, MOE && !p.gather ? (int64_t)(run0 / S) * p.x_slot_stride : 0, xg0_0, xgc,
-                    &xbar[0]);
+            x_issue(p, xb0, smem + p.gamma_off, rows0, M0, MOE && !p.gather ? (int64_t)(run0 / S) * p.x_slot_stride : 0,
+                    xg0_0, xgc, &xbar[0]);
             if (two)
-                x_issue(p, xb1, rows1, M1, MOE && !p.gather ? (int64_t)(run1 / S) * p.x_slot_stride : 0, xg0_1, xgc,
-                        &xbar[1]);
+                x_issue(p, xb1, nullptr, rows1, M1, MOE && !p.gather ? (int64_t)(run1 / S) * p.x_slot_stride : 0, xg0_1,
+                        xgc, &xbar[1]);
         }
     }
     if (alive) {
@@ -840,10 +868,10 @@ __global__ void __launch_bounds__(kThreads, 1) qproj_warp_kernel(const __grid_co
             ok = ok && wait_or_abort(&xbar[1], 0, flags, p.status, p.limit_ns);
         alive = __all_sync(0xffffffffu, ok);
     }
-    x_prepare(p, xb0, M0, xg0_0, norm ? 0 : xg0_0, norm ? p.groups : p.Gs, xs0, inv0, cw, lane, kConsumerWarps,
-              kBarConsumers);
+    x_prepare(p, xb0, smem + p.gamma_off, M0, xg0_0, norm ? 0 : xg0_0, norm ? p.groups : p.Gs, xs0, inv0, cw, lane,
+              kConsumerWarps, kBarConsumers);
     if (two)
-        x_prepare(p, xb1, M1, xg0_1, xg0_1, p.Gs, xs1, inv1, cw, lane, kConsumerWarps, kBarConsumers);
+        x_prepare(p, xb1, nullptr, M1, xg0_1, xg0_1, p.Gs, xs1, inv1, cw, lane, kConsumerWarps, kBarConsumers);
 
     if (cw < NW && alive) {
         int64_t u, u1;
@@ -1025,10 +1053,10 @@ cudaError_t launch_qproj_warp(const Plan& plan, const QProjParams& p, cudaStream
     return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
-template <int BITS, bool DUAL, bool MOE, int KW>
+template <int BITS, bool DUAL, bool MOE, int KW, int NWT>
 cudaError_t launch_qproj_kw(const Plan& plan, const QProjParams& p, cudaStream_t stream, bool pdl)
 {
-    auto kern = qproj_kernel<BITS, DUAL, MOE, KW>;
+    auto kern = qproj_kernel<BITS, DUAL, MOE, KW, NWT>;
     static bool configured = false;
     if (!configured) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
@@ -1038,7 +1066,7 @@ cudaError_t launch_qproj_kw(const Plan& plan, const QProjParams& p, cudaStream_t
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)plan.C, 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.blockDim = dim3((NWT + 1) * 32, 1, 1);
     cfg.dynamicSmemBytes = plan.smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -1054,12 +1082,21 @@ cudaError_t launch_qproj_t(const Plan& plan, const QProjParams& p, cudaStream_t 
 {
     if (plan.mode == 1)
         return launch_qproj_warp<BITS, DUAL, MOE>(plan, p, stream, pdl);
+    if (plan.nw == 8) {  // light teams: one item per CTA, several CTAs per SM
+        switch (plan.KW) {
+        case 1: return launch_qproj_kw<BITS, DUAL, MOE, 1, 8>(plan, p, stream, pdl);
+        case 2: return launch_qproj_kw<BITS, DUAL, MOE, 2, 8>(plan, p, stream, pdl);
+        case 4: return launch_qproj_kw<BITS, DUAL, MOE, 4, 8>(plan, p, stream, pdl);
+        case 8: return launch_qproj_kw<BITS, DUAL, MOE, 8, 8>(plan, p, stream, pdl);
+        default: return cudaErrorInvalidValue;
+        }
+    }
     switch (plan.KW) {
-    case 1: return launch_qproj_kw<BITS, DUAL, MOE, 1>(plan, p, stream, pdl);
-    case 2: return launch_qproj_kw<BITS, DUAL, MOE, 2>(plan, p, stream, pdl);
-    case 4: return launch_qproj_kw<BITS, DUAL, MOE, 4>(plan, p, stream, pdl);
-    case 8: return launch_qproj_kw<BITS, DUAL, MOE, 8>(plan, p, stream, pdl);
-    case 16: return launch_qproj_kw<BITS, DUAL, MOE, 16>(plan, p, stream, pdl);
+    case 1: return launch_qproj_kw<BITS, DUAL, MOE, 1, 16>(plan, p, stream, pdl);
+    case 2: return launch_qproj_kw<BITS, DUAL, MOE, 2, 16>(plan, p, stream, pdl);
+    case 4: return launch_qproj_kw<BITS, DUAL, MOE, 4, 16>(plan, p, stream, pdl);
+    case 8: return launch_qproj_kw<BITS, DUAL, MOE, 8, 16>(plan, p, stream, pdl);
+    case 16: return launch_qproj_kw<BITS, DUAL, MOE, 16, 16>(plan, p, stream, pdl);
     default: return cudaErrorInvalidValue;
     }
 }
