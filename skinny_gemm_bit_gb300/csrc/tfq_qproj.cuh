@@ -227,9 +227,15 @@ __device__ __forceinline__ void x_prepare(const QProjParams& p, uint8_t* buf, co
         part += __shfl_xor_sync(0xffffffffu, part, 1);
         __syncwarp();  // every lane of the block has read it before any rewrites it
         if (live) {
+            // the four (group, row) blocks of a warp start their four stores at different
+            // words q, so that each store instruction covers all 32 banks once
+            const int rot = lane >> 3;
 #pragma unroll
-            for (int q = 0; q < 4; ++q)
-                blk[16 * (cc >> 2) + 4 * q + (cc & 3)] = vv[q];
+            for (int j = 0; j < 4; ++j) {
+                const int q = (j + rot) & 3;
+                const uint32_t v = q == 0 ? vv[0] : q == 1 ? vv[1] : q == 2 ? vv[2] : vv[3];
+                blk[16 * (cc >> 2) + 4 * q + (cc & 3)] = v;
+            }
         }
         if (valid && cc == 0)
             xs[gl * kMaxM + m] = part;
@@ -292,14 +298,95 @@ struct Part {
     int per_ps;  // units per (problem, split) = n_rb * Gs
     int Gs;
     bool aligned;
+    // floor(a c / C) for 0 <= c <= C <= 2^16 in 32-bit arithmetic
+    __device__ __forceinline__ static uint32_t muldiv(uint32_t a, uint32_t c, uint32_t C)
+    {
+        const uint32_t q = a / C, r = a - q * C;
+        return q * c + r * c / C;
+    }
     __device__ __forceinline__ int64_t start(int c) const
     {
-        return aligned ? (items * c / C) * Gs : U * c / C;
+        return aligned ? (int64_t)muldiv((uint32_t)items, (uint32_t)c, (uint32_t)C) * Gs
+                       : (int64_t)muldiv((uint32_t)U, (uint32_t)c, (uint32_t)C);
     }
-    __device__ __forceinline__ int cta_of(int64_t u) const { return (int)(((u + 1) * C - 1) / U); }
+    float inv_U;  // 1 / U, for the quotient estimate below
+    // floor(((u + 1) C - 1) / U): the quotient is at most C, so a float estimate is within
+    // one of it; two integer comparisons make it exact
+    __device__ __forceinline__ int cta_of(int64_t u) const
+    {
+        const int64_t n = (u + 1) * C - 1;
+        int q = (int)((float)n * inv_U);
+        if ((int64_t)(q + 1) * U <= n)
+            ++q;
+        else if ((int64_t)q * U > n)
+            --q;
+        return q;
+    }
     // CTAs contributing to the row block starting at unit f (stream-K only)
     __device__ __forceinline__ int contributors(int64_t f) const { return cta_of(f + Gs - 1) - cta_of(f) + 1; }
 };
+
+// Sum of the fp32 partial slots of row block rb of problem prob, in (split,
+// contributor) order, zeroing every slot read (the workspace is left as it was
+// found). Loads are issued several slots at a time before any is used, so the L2
+// round trips overlap.
+template <bool DUAL>
+__device__ __forceinline__ void sum_partials(const QProjParams& p, const Part& pt, int prob, int rb, int lane,
+                                             float (&t0)[4], float (&t1)[4])
+{
+    constexpr int VALS = DUAL ? 8 : 4;
+    constexpr int B = 4;
+    auto kc_of = [&](int s2) {
+        return pt.aligned ? 1
+                          : min(pt.contributors((int64_t)prob * pt.per_p + (int64_t)s2 * pt.per_ps + (int64_t)rb * p.Gs),
+                                p.kmax);
+    };
+    int s2 = 0, kq = 0, kc = kc_of(0);
+    while (s2 < p.S) {
+        float4* src[B];
+        bool valid[B];
+#pragma unroll
+        for (int j = 0; j < B; ++j) {
+            valid[j] = s2 < p.S;
+            src[j] = nullptr;
+            if (valid[j]) {
+                src[j] = reinterpret_cast<float4*>(
+                    p.partials + (((((int64_t)prob * p.S + s2) * p.n_rb + rb) * p.kmax + kq) * 32 + lane) * VALS);
+                if (++kq == kc) {
+                    kq = 0;
+                    if (++s2 < p.S)
+                        kc = kc_of(s2);
+                }
+            }
+        }
+        float4 a[B], b[B];
+#pragma unroll
+        for (int j = 0; j < B; ++j) {
+            if (valid[j]) {
+                a[j] = __ldcg(src[j]);
+                if constexpr (DUAL)
+                    b[j] = __ldcg(src[j] + 1);
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < B; ++j) {
+            if (valid[j]) {
+                __stcg(src[j], make_float4(0.f, 0.f, 0.f, 0.f));
+                t0[0] += a[j].x;
+                t0[1] += a[j].y;
+                t0[2] += a[j].z;
+                t0[3] += a[j].w;
+                if constexpr (DUAL) {
+                    __stcg(src[j] + 1, make_float4(0.f, 0.f, 0.f, 0.f));
+                    t1[0] += b[j].x;
+                    t1[1] += b[j].y;
+                    t1[2] += b[j].z;
+                    t1[3] += b[j].w;
+                }
+            }
+        }
+    }
+}
 
 constexpr int kBarConsumers = 15;  // named barrier of all consumer warps; 1..8 are team barriers
 
@@ -365,6 +452,7 @@ __global__ void __launch_bounds__((NWT + 1) * 32, NWT == 8 ? 2 : 1) qproj_kernel
     pt.aligned = p.aligned != 0;
     pt.items = (int64_t)P * p.S * p.n_rb;
     pt.U = pt.items * p.Gs;
+    pt.inv_U = 1.f / (float)max(pt.U, (int64_t)1);
     pt.C = (int)min((int64_t)p.C, max(pt.aligned ? pt.items : pt.U, (int64_t)1));
     int64_t u0 = 0, u1 = 0;
     if (c < pt.C) {  // CTAs past the work (fewer MoE slots active than planned for) stay idle
@@ -377,58 +465,61 @@ __global__ void __launch_bounds__((NWT + 1) * 32, NWT == 8 ? 2 : 1) qproj_kernel
         }
     }
 
-    // ---- this CTA's segments (maximal runs inside one row block) and rounds (up to R
-    // consecutive segments of one (problem, split)); built once, read by every warp
-    if (threadIdx.x == 0) {
-        int nseg = 0, nround = 0, rlen = 0, rp = -1, rs = -1, rmax = 0;
-        if (u0 < u1) {
-            const int uu = (int)u0;  // units fit in 30 bits (checked on the host)
-            int pp = 0, ss = 0, rb, gl;
-            if (pt.items == p.n_rb && pt.aligned && pt.C == pt.items) {  // one row block per CTA
-                rb = c;
-                gl = 0;
-            } else {
-                pp = uu / pt.per_p;
-                int rem = uu - pp * pt.per_p;
-                ss = rem / pt.per_ps;
-                rem -= ss * pt.per_ps;
-                rb = rem / p.Gs;
-                gl = rem - rb * p.Gs;
+    // ---- this CTA's segments (maximal runs inside one (problem, split, row block)) and
+    // rounds (up to R consecutive segments of one (problem, split)), built by warp 0 with
+    // a lane per segment and read by every warp
+    if (warp == 0) {
+        int nseg = 0, nround = 0;
+        if (u0 < u1 && pt.items == p.n_rb && pt.aligned && pt.C == pt.items) {  // row block c, whole
+            nseg = 1;
+            nround = 1;
+            if (lane == 0) {
+                segs[0] = make_int4(0, 0, c, p.Gs);
+                rounds[0] = make_int2(0, p.Gs);
             }
-            int64_t u = u0;
-            while (u < u1 && nseg < p.segmax) {
-                const int len = (int)min((int64_t)(p.Gs - gl), u1 - u);
-                if (rlen == R || pp != rp || ss != rs) {
-                    if (nround > 0)
-                        rounds[nround - 1].y = rmax;
-                    rounds[nround++].x = nseg;
-                    rlen = 0;
-                    rmax = 0;
-                    rp = pp;
-                    rs = ss;
-                }
-                segs[nseg++] = make_int4(pp, ss, rb, (gl << 16) | len);
-                ++rlen;
-                rmax = max(rmax, len);
-                u += len;
-                gl = 0;
-                if (++rb == p.n_rb) {
-                    rb = 0;
-                    if (++ss == p.S) {
-                        ss = 0;
-                        ++pp;
-                    }
+        } else if (u0 < u1) {
+            const int Gs = p.Gs, a0 = (int)u0, a1 = (int)u1;  // units fit in 30 bits (checked on the host)
+            const int b0 = a0 / Gs;                            // (problem, split, row block) flattened
+            nseg = (a1 - 1) / Gs - b0 + 1;
+            if (nseg > p.segmax) {  // the host sizes the list; never expected
+                nseg = 0;
+                if (lane == 0) {
+                    flags[0] = 1;
+                    atomicCAS(p.status, 0, TF_E_TIMEOUT);
                 }
             }
-            if (u < u1) {  // the host sizes the list; never expected
-                flags[0] = 1;
-                atomicCAS(p.status, 0, TF_E_TIMEOUT);
+            for (int i0 = 0; i0 < nseg; i0 += 32) {
+                const int i = i0 + lane;
+                bool starts = false;
+                if (i < nseg) {
+                    const int idx = b0 + i;
+                    const int key = idx / p.n_rb, rb = idx - key * p.n_rb;
+                    const int pp = key / p.S, ss = key - pp * p.S;
+                    const int lo = max(a0, idx * Gs), hi = min(a1, (idx + 1) * Gs);
+                    segs[i] = make_int4(pp, ss, rb, ((lo - idx * Gs) << 16) | (hi - lo));
+                    // a round starts every R segments of the CTA's run of one (problem, split)
+                    starts = (idx - max(key * p.n_rb, b0)) % R == 0;
+                }
+                const unsigned bal = __ballot_sync(0xffffffffu, starts);
+                if (starts)
+                    rounds[nround + __popc(bal & ((1u << lane) - 1u))].x = i;
+                nround += __popc(bal);
             }
-            rounds[nround - 1].y = rmax;
+            __syncwarp();
+            for (int t = lane; t < nround; t += 32) {  // longest segment of each round
+                const int e = t + 1 < nround ? rounds[t + 1].x : nseg;
+                int m = 0;
+                for (int i = rounds[t].x; i < e; ++i)
+                    m = max(m, segs[i].w & 0xFFFF);
+                rounds[t].y = m;
+            }
         }
-        rounds[nround].x = nseg;
-        counts[0] = nseg;
-        counts[1] = flags[0] ? 0 : nround;
+        __syncwarp();
+        if (lane == 0) {
+            rounds[nround].x = nseg;
+            counts[0] = nseg;
+            counts[1] = flags[0] ? 0 : nround;
+        }
     }
     __syncthreads();
     const int nseg = counts[0], nround = counts[1];
@@ -551,22 +642,26 @@ __global__ void __launch_bounds__((NWT + 1) * 32, NWT == 8 ? 2 : 1) qproj_kernel
         // ---- sum the KW warps of the team (team barrier: ids 1..R)
         if constexpr (KW > 1) {
             named_bar_sync(1 + r_me, KW * 32);  // the previous round's reads of red are done
-            float* mine = red + (cw * 32 + lane) * VALS;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                mine[i] = acc0[i];
-                if constexpr (DUAL)
-                    mine[4 + i] = acc1[i];
-            }
+            // one float4 per lane and matrix, the lanes of a warp side by side (no bank conflicts)
+            float4* red4 = reinterpret_cast<float4*>(red);
+            red4[cw * 32 + lane] = make_float4(acc0[0], acc0[1], acc0[2], acc0[3]);
+            if constexpr (DUAL)
+                red4[NWT * 32 + cw * 32 + lane] = make_float4(acc1[0], acc1[1], acc1[2], acc1[3]);
             named_bar_sync(1 + r_me, KW * 32);
             if (kp == 0) {
+                const float4* red4 = reinterpret_cast<const float4*>(red);
                 for (int q = 1; q < KW; ++q) {
-                    const float* other = red + ((cw + q) * 32 + lane) * VALS;
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        acc0[i] += other[i];
-                        if constexpr (DUAL)
-                            acc1[i] += other[4 + i];
+                    const float4 o0 = red4[(cw + q) * 32 + lane];
+                    acc0[0] += o0.x;
+                    acc0[1] += o0.y;
+                    acc0[2] += o0.z;
+                    acc0[3] += o0.w;
+                    if constexpr (DUAL) {
+                        const float4 o1 = red4[NWT * 32 + (cw + q) * 32 + lane];
+                        acc1[0] += o1.x;
+                        acc1[1] += o1.y;
+                        acc1[2] += o1.z;
+                        acc1[3] += o1.w;
                     }
                 }
             }
@@ -642,30 +737,7 @@ __global__ void __launch_bounds__((NWT + 1) * 32, NWT == 8 ? 2 : 1) qproj_kernel
         const int4 e = segs[i];
         __threadfence();
         float t0[4] = {0.f, 0.f, 0.f, 0.f}, t1[4] = {0.f, 0.f, 0.f, 0.f};
-        for (int s2 = 0; s2 < p.S; ++s2) {
-            const int kc = pt.aligned ? 1
-                                      : min(pt.contributors((int64_t)e.x * pt.per_p + (int64_t)s2 * pt.per_ps +
-                                                            (int64_t)e.z * p.Gs),
-                                            p.kmax);
-            for (int k = 0; k < kc; ++k) {
-                float4* src = reinterpret_cast<float4*>(
-                    p.partials + (((((int64_t)e.x * p.S + s2) * p.n_rb + e.z) * p.kmax + k) * 32 + lane) * VALS);
-                const float4 v = __ldcg(src);
-                __stcg(src, make_float4(0.f, 0.f, 0.f, 0.f));  // the workspace is left as it was found
-                t0[0] += v.x;
-                t0[1] += v.y;
-                t0[2] += v.z;
-                t0[3] += v.w;
-                if constexpr (DUAL) {
-                    const float4 w = __ldcg(src + 1);
-                    __stcg(src + 1, make_float4(0.f, 0.f, 0.f, 0.f));
-                    t1[0] += w.x;
-                    t1[1] += w.y;
-                    t1[2] += w.z;
-                    t1[3] += w.w;
-                }
-            }
-        }
+        sum_partials<DUAL>(p, pt, e.x, e.z, lane, t0, t1);
         const int Mr = MOE ? slot_ec[e.x].y : p.M;
         store_outputs<DUAL, MOE>(p, e.x, Mr, e.z * kRowsPerBlock, lane, t0, t1);
         if (lane == 0)
@@ -753,6 +825,7 @@ __global__ void __launch_bounds__(kThreads, 1) qproj_warp_kernel(const __grid_co
     pt.aligned = p.aligned != 0;
     pt.items = (int64_t)P * p.S * p.n_rb;
     pt.U = pt.items * p.Gs;
+    pt.inv_U = 1.f / (float)max(pt.U, (int64_t)1);
     const int W = (int)min((int64_t)p.C * NW, max(pt.aligned ? pt.items : pt.U, (int64_t)1));
     pt.C = W;  // the partition is over workers
     auto wrange = [&](int v, int64_t& a, int64_t& b) {
@@ -998,30 +1071,7 @@ __global__ void __launch_bounds__(kThreads, 1) qproj_warp_kernel(const __grid_co
         const int4 e = pending[i];
         __threadfence();
         float t0[4] = {0.f, 0.f, 0.f, 0.f}, t1[4] = {0.f, 0.f, 0.f, 0.f};
-        for (int s2 = 0; s2 < S; ++s2) {
-            const int kc = pt.aligned ? 1
-                                      : min(pt.contributors((int64_t)e.x * pt.per_p + (int64_t)s2 * pt.per_ps +
-                                                            (int64_t)e.y * p.Gs),
-                                            p.kmax);
-            for (int kq = 0; kq < kc; ++kq) {
-                float4* src = reinterpret_cast<float4*>(
-                    p.partials + (((((int64_t)e.x * S + s2) * p.n_rb + e.y) * p.kmax + kq) * 32 + lane) * VALS);
-                const float4 a = __ldcg(src);
-                __stcg(src, make_float4(0.f, 0.f, 0.f, 0.f));  // the workspace is left as it was found
-                t0[0] += a.x;
-                t0[1] += a.y;
-                t0[2] += a.z;
-                t0[3] += a.w;
-                if constexpr (DUAL) {
-                    const float4 b = __ldcg(src + 1);
-                    __stcg(src + 1, make_float4(0.f, 0.f, 0.f, 0.f));
-                    t1[0] += b.x;
-                    t1[1] += b.y;
-                    t1[2] += b.z;
-                    t1[3] += b.w;
-                }
-            }
-        }
+        sum_partials<DUAL>(p, pt, e.x, e.y, lane, t0, t1);
         const int Mr = MOE ? slot_ec[e.x].y : p.M;
         store_outputs<DUAL, MOE>(p, e.x, Mr, e.y * kRowsPerBlock, lane, t0, t1);
         if (lane == 0)
