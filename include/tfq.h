@@ -156,6 +156,36 @@ int tf_qlinear_run(const tf_qweight* w, const uint16_t* x, int64_t ldx, int64_t 
                    void* y, int y_dtype, void* ws, size_t ws_bytes, unsigned flags, void* stream);
 
 /*
+ * tf_qlinear_run without a workspace argument: the same projection, the same
+ * kernels and the same results, with the split-K scratch (status word, arrival
+ * counters, fp32 partial slots) taken from one fixed 4 MiB device array inside
+ * the library (one per device) instead of caller memory. The pages have no
+ * counterpart; it exists for callers that cannot allocate device memory where
+ * they make the call: code running inside an allocator or memory-pool callback,
+ * a path that has reserved all of its memory up front and must never reach an
+ * allocator, or a host without access to a device allocator. This call itself
+ * allocates nothing.
+ *   Arguments: as tf_qlinear_run, minus ws / ws_bytes.
+ *   Limit: shapes whose tf_qlinear_workspace_bytes exceeds 4 MiB are refused
+ *          with TF_E_WORKSPACE_TOO_SMALL (nothing enqueued); every shape whose
+ *          K splits need at most that much is served (e.g. K=12800, N=2560).
+ *   First call on a device: looks up the array's device address
+ *          (cudaGetSymbolAddress, with that device current), which may load the
+ *          library's device code; make that first call before any stream
+ *          capture begins.
+ *   Sharing: every call on a device uses the same array. The array starts at
+ *          zero and each call leaves it at zero, so it needs no clearing; but two
+ *          calls that may run at the same time on one device (different streams,
+ *          or host threads) race on it and must not overlap. A device-side wait
+ *          that gives up records TF_E_TIMEOUT in the array, where this call cannot
+ *          report it, and may leave the split-K slots dirty; use tf_qlinear_run
+ *          with a workspace where such failures must be observed.
+ */
+int tf_qlinear_run_noalloc(const tf_qweight* w, const uint16_t* x, int64_t ldx, int64_t M,
+                           const uint16_t* rms_gamma, float rms_eps, const uint16_t* residual,
+                           void* y, int y_dtype, unsigned flags, void* stream);
+
+/*
  * Gate and up together with a SwiGLU epilogue (Husky page, "Four
  * implementation elements of MSI": gate and up projections are processed
  * together; the preceding normalisation is merged in):

@@ -324,6 +324,19 @@ Plan plan_qproj(int n_rb, int groups, int mats, int bits, int slots, int k_full,
     return pl;
 }
 
+// For the other translation units of the library: set the calling thread's error
+// message and return the status; validate a descriptor as every entry point does.
+int report_error(int status, const char* fmt, ...)
+{
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_last_error, sizeof g_last_error, fmt, ap);
+    va_end(ap);
+    return status;
+}
+
+int validate_desc(const tf_qweight* w, const char* name) { return check_desc(w, name); }
+
 }  // namespace tfq
 
 using namespace tfq;

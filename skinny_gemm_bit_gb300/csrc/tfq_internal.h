@@ -104,6 +104,10 @@ int device_sms();
 // rows: activation rows to allocate shared memory for (8 for MoE).
 Plan plan_qproj(int n_rb, int groups, int mats, int bits, int slots, int k_full, int rows);
 
+// Error reporting and descriptor validation shared by the entry points (tfq_api.cu).
+int report_error(int status, const char* fmt, ...);
+int validate_desc(const tf_qweight* w, const char* name);
+
 // launchers (tfq_qproj_b*_*.cu, one instantiation unit per bit width and matrix count)
 cudaError_t launch_qproj_b4_single(bool moe, const Plan& plan, const QProjParams& p, cudaStream_t stream, bool pdl);
 cudaError_t launch_qproj_b4_dual(bool moe, const Plan& plan, const QProjParams& p, cudaStream_t stream, bool pdl);

@@ -25,6 +25,8 @@ TF_E_TIMEOUT = 6
 TF_DTYPE_BF16 = 0
 TF_DTYPE_F32 = 1
 TF_RUN_PDL = 1
+TF_QWEIGHT_MAGIC = 0x31515446
+TF_PACK_VERSION = 1
 TF_TUNE_ROWBLOCKS = 0
 TF_TUNE_SPLITK = 1
 TF_TUNE_STAGE_GROUPS = 2
@@ -76,6 +78,8 @@ _SIGS = {
     "tf_qlinear_workspace_bytes": (SZ, [ctypes.POINTER(tf_qweight), I64]),
     "tf_qlinear_run": (ctypes.c_int, [ctypes.POINTER(tf_qweight), P, I64, I64, P, ctypes.c_float, P, P,
                                       ctypes.c_int, P, SZ, ctypes.c_uint, P]),
+    "tf_qlinear_run_noalloc": (ctypes.c_int, [ctypes.POINTER(tf_qweight), P, I64, I64, P, ctypes.c_float, P, P,
+                                              ctypes.c_int, ctypes.c_uint, P]),
     "tf_qmlp_gateup_workspace_bytes": (SZ, [ctypes.POINTER(tf_qweight), ctypes.POINTER(tf_qweight), I64]),
     "tf_qmlp_gateup_run": (ctypes.c_int, [ctypes.POINTER(tf_qweight), ctypes.POINTER(tf_qweight), P, I64, I64,
                                           P, ctypes.c_float, P, P, SZ, ctypes.c_uint, P]),
@@ -266,6 +270,18 @@ def tf_qlinear_run(w: QWeight, x: torch.Tensor, gamma=None, eps: float = 1e-6, r
         ws = workspace(tf_qlinear_workspace_bytes(w, M), x.device)
     _check(lib().tf_qlinear_run(ctypes.byref(w.desc), _ptr(x), ldx, M, _ptr(gamma), eps, _ptr(residual), _ptr(out),
                                 ydt, _ptr(ws), ws.numel(), flags, _stream(stream)))
+    return out
+
+
+def tf_qlinear_run_noalloc(w: QWeight, x: torch.Tensor, gamma=None, eps: float = 1e-6, residual=None, out=None,
+                           out_dtype=torch.bfloat16, flags: int = 0, stream=None) -> torch.Tensor:
+    """tf_qlinear_run with the library's fixed scratch array instead of a workspace."""
+    M, ldx = _rows(x)
+    if out is None:
+        out = torch.empty((M, w.N), dtype=out_dtype, device=x.device)
+    ydt = TF_DTYPE_F32 if out.dtype == torch.float32 else TF_DTYPE_BF16
+    _check(lib().tf_qlinear_run_noalloc(ctypes.byref(w.desc), _ptr(x), ldx, M, _ptr(gamma), eps, _ptr(residual),
+                                        _ptr(out), ydt, flags, _stream(stream)))
     return out
 
 
