@@ -294,7 +294,8 @@ int tf_selftest_wait_timeout(void* ws, uint64_t limit_ns, void* stream);
 #define TF_TUNE_STAGE_GROUPS 2 /* 64-column groups per pipeline stage */
 #define TF_TUNE_STAGES 3      /* pipeline depth (ring slots per worker in warp mode) */
 #define TF_TUNE_WARPS 4       /* warp mode: consumer warps per CTA (1..16) */
-#define TF_TUNE_MODE 5        /* 1: lock-step teams, 2: warp workers, 3: light teams (one item per CTA) */
+#define TF_TUNE_MODE 5        /* 1: lock-step teams, 2: warp workers, 3: light teams (one item per CTA),
+                                 4: light teams with bulk-copied (not register-loaded) activations */
 int tf_tune_set(int key, int value);
 
 #ifdef __cplusplus

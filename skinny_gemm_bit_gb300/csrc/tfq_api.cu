@@ -94,6 +94,7 @@ void fill_common(QProjParams& p, const Plan& pl, void* ws, uint8_t* scratch)
     p.xsum1_off = pl.xsum1_off;
     p.xraw1_off = pl.xraw1_off;
     p.gamma_off = pl.gamma_off;
+    p.x_direct = pl.x_direct;
     p.xraw_off = pl.xraw_off;
     p.x_rs = pl.x_rs;
     p.stage_off = pl.stage_off;
@@ -225,7 +226,7 @@ Plan plan_qproj(int n_rb, int groups, int mats, int bits, int slots, int k_full,
     // fetched in one stage, small enough for several CTAs (and the next kernel's) per SM
     const bool light_ok = S == 1 && items <= 4LL * sms && (double)U * tile * mats <= 8.0 * 1024 * 1024;
     bool light = light_ok && g_tune[TF_TUNE_MODE] <= 0;
-    if (g_tune[TF_TUNE_MODE] == 3)
+    if (g_tune[TF_TUNE_MODE] == 3 || g_tune[TF_TUNE_MODE] == 4)
         light = light_ok;
     if (light) {
         pl.nw = 8;
@@ -254,6 +255,9 @@ Plan plan_qproj(int n_rb, int groups, int mats, int bits, int slots, int k_full,
         pl.smem = pl.stage_off + stage;
         pl.ws_counters = 0;
         pl.ws_partials = 0;
+        // plain rows (one problem) come straight from global memory: with an RMSNorm the
+        // row must fit four 8-column chunks per lane (K <= 1024)
+        pl.x_direct = slots == 1 && (k_full == 0 || k_full <= 1024) && g_tune[TF_TUNE_MODE] != 4 ? 1 : 0;
         return pl;
     }
     pl.nw = kConsumerWarps;

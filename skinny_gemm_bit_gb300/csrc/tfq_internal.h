@@ -85,6 +85,7 @@ struct QProjParams {
     // warp mode: active consumer warps, pending capacity per warp, second activation buffer
     int nw, pw, xsum1_off, xraw1_off;
     int gamma_off;  // staged RMSNorm weight (K bf16)
+    int x_direct;   // activations loaded straight into registers (unsplit calls), not by bulk copy
 };
 
 struct Plan {
@@ -92,6 +93,7 @@ struct Plan {
     int KW, R, S, Gs, cg, nst, C, aligned, kmax, segmax, slots;
     int red_off, seg_off, round_off, last_off, xraw_off, x_rs, stage_off;
     int nw, pw, xsum1_off, xraw1_off, gamma_off;
+    int x_direct;
     size_t smem;
     size_t ws_partials;      // bytes
     size_t ws_counters;      // bytes

@@ -243,6 +243,126 @@ __device__ __forceinline__ void x_prepare(const QProjParams& p, uint8_t* buf, co
     named_bar_sync(bar_id, nwarps * 32);
 }
 
+// Activations of an unsplit call staged straight from global memory (where the
+// previous kernel left them, so loads bypass L1) through registers: every 8-column
+// chunk c of row m is rounded (and normalised) in registers, summed over its group
+// by the 8 lanes that hold the group, and stored in B-fragment order at
+// buf + m * x_rs + (c / 8) * 128; group sums go to xs[g * 8 + m] (zero for rows >=
+// Mrows). With an RMSNorm a warp owns a row (K <= 1024: four chunks a lane), so
+// the row's sum of squares is a warp reduction; without one, (row, chunk) items
+// are spread over all consumer threads, four loads in flight per thread.
+__device__ __forceinline__ void x_put_chunk(uint8_t* buf, int x_rs, float* xs, int m, int c, bool valid,
+                                            const uint32_t (&vv)[4], int lane)
+{
+    float part = 0.f;
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+        part += bf16lo_f32(vv[q]) + bf16hi_f32(vv[q]);
+    part += __shfl_xor_sync(0xffffffffu, part, 4);
+    part += __shfl_xor_sync(0xffffffffu, part, 2);
+    part += __shfl_xor_sync(0xffffffffu, part, 1);
+    if (!valid)
+        return;
+    const int cc = c & 7;
+    uint32_t* blk = reinterpret_cast<uint32_t*>(buf + m * x_rs + (c >> 3) * 128);
+    const int rot = lane >> 3;  // the four 8-lane groups of a warp start at different words
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const int q = (j + rot) & 3;
+        const uint32_t v = q == 0 ? vv[0] : q == 1 ? vv[1] : q == 2 ? vv[2] : vv[3];
+        blk[16 * (cc >> 2) + 4 * q + (cc & 3)] = v;
+    }
+    if (cc == 0)
+        xs[(c >> 3) * kMaxM + m] = part;
+}
+
+__device__ __forceinline__ void x_direct(const QProjParams& p, uint8_t* buf, int Mrows, float* xs, float* ss_part,
+                                         int cw, int lane, int nwarps, int bar_id)
+{
+    const int nch = p.groups * 8;  // 8-column chunks per row
+    for (int i = cw * 32 + lane; i < p.groups * kMaxM; i += nwarps * 32)
+        if ((i & 7) >= Mrows)
+            xs[i] = 0.f;
+    if (p.gamma != nullptr) {
+        // WPR warps per row (the largest power of two with WPR * Mrows <= nwarps), each
+        // on a run of cpw chunks (a multiple of 8, at most 4 per lane since K <= 1024);
+        // the row's sum of squares is the WPR warp sums added in warp order
+        int WPR = 1;
+        while (2 * WPR * Mrows <= nwarps)
+            WPR *= 2;
+        const int m = cw / WPR, sub = cw - m * WPR;
+        const int cpw = ((nch + WPR - 1) / WPR + 7) / 8 * 8;
+        const bool row_warp = m < Mrows;  // warp-uniform
+        const int c0 = sub * cpw, c1 = min(nch, c0 + cpw);
+        const uint4* g4 = reinterpret_cast<const uint4*>(p.gamma);
+        const uint4* x4 = reinterpret_cast<const uint4*>(p.x + (int64_t)(row_warp ? m : 0) * p.ldx);
+        uint4 v[4], gv[4];
+        float sq[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int c = c0 + j * 32 + lane;
+            const bool ok = row_warp && c < c1;
+            v[j] = ok ? __ldcg(x4 + c) : make_uint4(0u, 0u, 0u, 0u);
+            gv[j] = ok ? __ldg(g4 + c) : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint32_t vv[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float a = bf16lo_f32(vv[q]), b = bf16hi_f32(vv[q]);
+                sq[q] = fmaf(b, b, fmaf(a, a, sq[q]));
+            }
+        }
+        const float wsum = warp_sum((sq[0] + sq[1]) + (sq[2] + sq[3]));
+        if (row_warp && lane == 0)
+            ss_part[cw] = wsum;
+        named_bar_sync(bar_id, nwarps * 32);
+        if (row_warp) {
+            float ss = 0.f;
+            for (int w = 0; w < WPR; ++w)
+                ss += ss_part[m * WPR + w];
+            const float inv = rsqrtf(ss / (float)p.K + p.eps);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int c = c0 + j * 32 + lane;
+                const uint32_t xv[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+                const uint32_t gg[4] = {gv[j].x, gv[j].y, gv[j].z, gv[j].w};
+                uint32_t vv[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    vv[q] = f32x2_to_bf16x2(bf16lo_f32(xv[q]) * inv * bf16lo_f32(gg[q]),
+                                            bf16hi_f32(xv[q]) * inv * bf16hi_f32(gg[q]));
+                if (c0 + j * 32 < c1)  // warp-uniform
+                    x_put_chunk(buf, p.x_rs, xs, m, c, c < c1, vv, lane);
+            }
+        }
+    } else {
+        const int items = Mrows * nch, T = nwarps * 32;
+        for (int base = 0; base < items; base += 4 * T) {
+            uint4 v[4];
+            int mm[4], cc[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int i = base + j * T + cw * 32 + lane;
+                mm[j] = i / nch;
+                cc[j] = i - mm[j] * nch;
+                v[j] = i < items ? __ldcg(reinterpret_cast<const uint4*>(p.x + (int64_t)mm[j] * p.ldx) + cc[j])
+                                 : make_uint4(0u, 0u, 0u, 0u);
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int i0 = base + j * T + cw * 32;  // warp-uniform
+                if (i0 < items) {
+                    const uint32_t vv[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+                    x_put_chunk(buf, p.x_rs, xs, mm[j], cc[j], i0 + lane < items, vv, lane);
+                }
+            }
+        }
+    }
+    named_bar_sync(bar_id, nwarps * 32);
+}
+
 // The B fragments (xa: k blocks 0, 1; xb: k blocks 2, 3) of group g_rel of a buffer.
 __device__ __forceinline__ void x_frag(const uint8_t* buf, int x_rs, int gi, int tq, int g_rel, bool has_row, uint4& xa,
                                        uint4& xb)
@@ -587,22 +707,26 @@ __global__ void __launch_bounds__((NWT + 1) * 32, NWT == 8 ? 2 : 1) qproj_kernel
             named_bar_sync(kBarConsumers, NCT);  // everyone is done with the previous rows
             if (MOE)
                 Mrows = slot_ec[first.x].y;
-            if (threadIdx.x < kMaxM)
-                rowsel[threadIdx.x] = MOE ? slot_rows[first.x * kMaxM + threadIdx.x] : (int)threadIdx.x;
-            const int xg0 = norm ? 0 : first.y * p.Gs;
-            const int xgc = norm ? p.groups : p.Gs;
-            if (cw == 0) {
-                __syncwarp();
-                if (lane == 0 && !flags[0])
-                    x_issue(p, xraw, smem + p.gamma_off, rowsel, Mrows,
-                            MOE && !p.gather ? (int64_t)first.x * p.x_slot_stride : 0, xg0, xgc, xbar);
+            if (!MOE && p.x_direct) {  // unsplit plain rows: no bulk copy, no wait
+                x_direct(p, xraw, Mrows, xsum, red, cw, lane, NWT, kBarConsumers);
+            } else {
+                if (threadIdx.x < kMaxM)
+                    rowsel[threadIdx.x] = MOE ? slot_rows[first.x * kMaxM + threadIdx.x] : (int)threadIdx.x;
+                const int xg0 = norm ? 0 : first.y * p.Gs;
+                const int xgc = norm ? p.groups : p.Gs;
+                if (cw == 0) {
+                    __syncwarp();
+                    if (lane == 0 && !flags[0])
+                        x_issue(p, xraw, smem + p.gamma_off, rowsel, Mrows,
+                                MOE && !p.gather ? (int64_t)first.x * p.x_slot_stride : 0, xg0, xgc, xbar);
+                }
+                bool ok = alive && wait_or_abort(xbar, (uint32_t)xphase, flags, p.status, p.limit_ns);
+                xphase ^= 1;
+                ++nstaged;
+                alive = __all_sync(0xffffffffu, ok);
+                x_prepare(p, xraw, smem + p.gamma_off, Mrows, xg0, first.y * p.Gs, p.Gs, xsum, inv_rms, cw, lane, NWT,
+                          kBarConsumers);
             }
-            bool ok = alive && wait_or_abort(xbar, (uint32_t)xphase, flags, p.status, p.limit_ns);
-            xphase ^= 1;
-            ++nstaged;
-            alive = __all_sync(0xffffffffu, ok);
-            x_prepare(p, xraw, smem + p.gamma_off, Mrows, xg0, first.y * p.Gs, p.Gs, xsum, inv_rms, cw, lane, NWT,
-                      kBarConsumers);
             cur_p = first.x;
             cur_s = first.y;
         }

@@ -297,12 +297,14 @@ def test_shared_workspace_across_shapes_is_left_clean(T):
             assert int(ws.count_nonzero()) == 0
 
 
-@pytest.mark.parametrize("mode", [1, 2, 3])
+@pytest.mark.parametrize("mode", [1, 2, 3, 4])
 @pytest.mark.parametrize("M,K,N,bits,dual", [(8, 12800, 2560, 4, False), (1, 1024, 18992, 4, False),
                                               (3, 2048, 4096, 8, False), (8, 1024, 3072, 4, True),
                                               (2, 640, 6000, 4, True)])
 def test_both_schedules_match(T, mode, M, K, N, bits, dual):
     # mode 1: lock-step teams; mode 2: warp workers with private ring slots; mode 3: light teams
+    # (activations loaded straight into registers where eligible); mode 4: light teams with
+    # bulk-copied activations
     rng = np.random.default_rng(M * 7 + N)
     x = synth.activations(rng, M, K)
     w = synth.quant_weights(rng, N, K, bits)
