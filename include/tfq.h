@@ -296,6 +296,8 @@ int tf_selftest_wait_timeout(void* ws, uint64_t limit_ns, void* stream);
 #define TF_TUNE_WARPS 4       /* warp mode: consumer warps per CTA (1..16) */
 #define TF_TUNE_MODE 5        /* 1: lock-step teams, 2: warp workers, 3: light teams (one item per CTA),
                                  4: light teams with bulk-copied (not register-loaded) activations */
+#define TF_TUNE_CHAIN 6       /* tf_decode_step_run: 1 = one kernel per projection instead of the
+                                 single persistent kernel for the whole step */
 int tf_tune_set(int key, int value);
 
 #ifdef __cplusplus

@@ -12,7 +12,7 @@ namespace tfq {
 
 namespace {
 thread_local char g_last_error[512] = "";
-int g_tune[6] = {-1, -1, -1, -1, -1, -1};
+int g_tune[7] = {-1, -1, -1, -1, -1, -1, -1};
 int g_sms_cache[64] = {0};
 
 constexpr size_t kStatusBytes = 256;
@@ -212,7 +212,7 @@ Plan plan_qproj(int n_rb, int groups, int mats, int bits, int slots, int k_full,
     pl.gamma_off = (int)align_up(pl.last_off + (size_t)pl.segmax * 4, 128);
     pl.xraw_off = (int)align_up(pl.gamma_off + (size_t)std::max(k_full, 0) * 2, 128);
     const int xcols = k_full > 0 ? k_full : pl.Gs * kGroup;
-    pl.x_rs = xcols * 2 + 64;
+    pl.x_rs = xcols * 2 + 16;
     pl.stage_off = (int)align_up(pl.xraw_off + (size_t)rows * pl.x_rs, 128);
     const size_t budget = 227 * 1024;
     int nst = budget > pl.stage_off + stage ? (int)((budget - pl.stage_off) / stage) : 1;
@@ -250,7 +250,7 @@ Plan plan_qproj(int n_rb, int groups, int mats, int bits, int slots, int k_full,
         pl.gamma_off = (int)align_up(pl.last_off + 4, 128);
         pl.xraw_off = (int)align_up(pl.gamma_off + (size_t)std::max(k_full, 0) * 2, 128);
         const int xcols = k_full > 0 ? k_full : pl.Gs * kGroup;
-        pl.x_rs = xcols * 2 + 64;
+        pl.x_rs = xcols * 2 + 16;
         pl.stage_off = (int)align_up(pl.xraw_off + (size_t)rows * pl.x_rs, 128);
         pl.smem = pl.stage_off + stage;
         pl.ws_counters = 0;
@@ -307,7 +307,7 @@ Plan plan_qproj(int n_rb, int groups, int mats, int bits, int slots, int k_full,
         pl.gamma_off = (int)align_up(pl.last_off + (size_t)nw * pl.pw * 4, 128);
         pl.xraw_off = (int)align_up(pl.gamma_off + (size_t)std::max(k_full, 0) * 2, 128);
         const int xcols = norm ? k_full : pl.Gs * kGroup;
-        pl.x_rs = xcols * 2 + 64;
+        pl.x_rs = xcols * 2 + 16;
         pl.xraw1_off = (int)align_up(pl.xraw_off + (size_t)rows * pl.x_rs, 128);
         pl.stage_off = (int)align_up(pl.xraw1_off + (two_bufs ? (size_t)rows * pl.x_rs : 0), 128);
         const size_t budget = 227 * 1024;
@@ -367,7 +367,7 @@ int tf_version(void) { return 1 * 10000 + 0 * 100 + 0; }
 
 int tf_tune_set(int key, int value)
 {
-    if (key < 0 || key > 5)
+    if (key < 0 || key > 6)
         return fail(TF_E_INVALID_ARG, "tf_tune_set: unknown key %d", key);
     if (key == TF_TUNE_ROWBLOCKS && value > 0 && value != 1 && value != 2 && value != 4 && value != 8 && value != 16)
         return fail(TF_E_INVALID_ARG, "tf_tune_set: row blocks per round must be 1, 2, 4, 8 or 16");
@@ -700,7 +700,7 @@ int tf_qmoe_run(const tf_qweight* gate, const tf_qweight* up, const tf_qweight* 
 namespace {
 struct StepLayout {
     Plan p_qkv, p_o, p_gu, p_dn, p_ro;
-    size_t act, red, total;
+    size_t bar, act, red, total;
     size_t qkv_e, h_e, a_e;  // elements per activation buffer
 };
 
@@ -753,7 +753,8 @@ StepLayout step_layout(const tf_decoder_desc* d, int64_t M)
     L.h_e = (size_t)kMaxM * D;
     L.a_e = (size_t)kMaxM * F;
     (void)M;
-    L.act = kStatusBytes;
+    L.bar = kStatusBytes;  // stage arrival counters of the single-kernel step: 4 per layer + 2
+    L.act = align_up(L.bar + (size_t)(4 * d->n_layers + 2) * sizeof(unsigned), 256);
     // qkv | h1 | a | h ping | h pong
     const size_t act_bytes = (L.qkv_e + L.h_e + L.a_e + 2 * L.h_e) * sizeof(uint16_t) + 5 * 256;
     L.red = align_up(L.act + act_bytes, 256);
@@ -816,9 +817,70 @@ int tf_decode_step_run(const tf_decoder_desc* d, const uint16_t* x, int64_t M, u
     hp_ws[0] = reinterpret_cast<uint16_t*>(align_up(reinterpret_cast<uintptr_t>(a_ws + L.a_e), 256));
     hp_ws[1] = reinterpret_cast<uint16_t*>(align_up(reinterpret_cast<uintptr_t>(hp_ws[0] + L.h_e), 256));
 
+    const size_t per_layer = (size_t)M * (QKV + D + F + D);
+
+    // ---- the whole step as one persistent kernel, when the shapes allow it
+    int bits = d->readout.bits;
+    bool chain = g_tune[TF_TUNE_CHAIN] != 1 && d->n_layers <= kChainMaxLayers && D <= 1024 &&
+                 std::max<int64_t>(D, std::max<int64_t>(Q, F)) <= (int64_t)kChainMaxGroups * kGroup &&
+                 d->vocab <= INT32_MAX;
+    for (int l = 0; chain && l < d->n_layers; ++l) {
+        const tf_decoder_layer& Ly = d->layers[l];
+        chain = Ly.qkv.bits == bits && Ly.o.bits == bits && Ly.gate.bits == bits && Ly.up.bits == bits &&
+                Ly.down.bits == bits;
+    }
+    ChainParams cp{};
+    size_t chain_smem_bytes = 0;
+    if (chain) {
+        chain_smem_bytes = chain_smem(bits, (int)std::max<int64_t>(D, std::max<int64_t>(Q, F)), &cp.nst, &cp.x_rs,
+                                      &cp.xsum_off, &cp.red_off, &cp.xraw_off, &cp.ring_off);
+        chain = cp.nst >= 2 && chain_fits(bits, chain_smem_bytes);
+    }
+    if (chain) {
+        cp.L = d->n_layers;
+        cp.M = (int)M;
+        cp.D = (int)D;
+        cp.F = (int)F;
+        cp.Q = (int)Q;
+        cp.KV = (int)KV;
+        cp.V = (int)d->vocab;
+        cp.eps = d->eps;
+        cp.C = device_sms();
+        cp.limit_ns = kDefaultWaitLimitNs;
+        cp.x = x;
+        cp.logits = logits;
+        cp.final_norm = d->final_norm;
+        cp.readout = tiles_of(&d->readout);
+        if (debug != nullptr) {
+            cp.buf[0] = debug;
+            cp.buf[1] = debug + M * QKV;
+            cp.buf[2] = debug + M * (QKV + D);
+            cp.buf[3] = debug + M * (QKV + D + F);
+            for (int r = 0; r < 4; ++r)
+                cp.lstride[r] = (int64_t)per_layer;
+        } else {
+            cp.buf[0] = qkv_ws;
+            cp.buf[1] = h1_ws;
+            cp.buf[2] = a_ws;
+            cp.buf[3] = hp_ws[0];
+            cp.astride[3] = hp_ws[1] - hp_ws[0];
+        }
+        cp.bar = reinterpret_cast<unsigned*>(wsb + L.bar);
+        cp.status = static_cast<int*>(ws);
+        for (int l = 0; l < d->n_layers; ++l) {
+            const tf_decoder_layer& Ly = d->layers[l];
+            cp.layer[l] = ChainLayerW{tiles_of(&Ly.qkv), tiles_of(&Ly.o), tiles_of(&Ly.gate), tiles_of(&Ly.up),
+                                      tiles_of(&Ly.down), Ly.attn_norm, Ly.mlp_norm};
+        }
+        const cudaError_t e = launch_chain(bits, cp, chain_smem_bytes, s);
+        if (e != cudaSuccess)
+            return cuda_fail(e, "tf_decode_step_run: single-kernel step");
+        return TF_OK;
+    }
+
+    // ---- one kernel per projection
     bool pdl = (flags & TF_RUN_PDL) != 0;
     const uint16_t* h = x;
-    const size_t per_layer = (size_t)M * (QKV + D + F + D);
     for (int l = 0; l < d->n_layers; ++l) {
         const tf_decoder_layer& Ly = d->layers[l];
         uint16_t *qkv, *h1, *a, *h2;

@@ -99,6 +99,42 @@ struct Plan {
     size_t ws_counters;      // bytes
 };
 
+// ---------------------------------------------------------------- decoder-step megakernel
+
+constexpr int kChainMaxLayers = 48;   // layer table carried in the kernel parameters
+constexpr int kChainMaxGroups = 48;   // K up to 3072 per stage
+constexpr int kChainSlotTiles = 32;   // tiles per ring slot
+
+struct ChainLayerW {
+    const uint8_t *qkv, *o, *gate, *up, *down;  // packed tiles (past the header)
+    const uint16_t *attn_norm, *mlp_norm;
+};
+
+struct ChainParams {
+    int L, M, D, F, Q, KV;
+    int V;
+    float eps;
+    int C;                                         // CTAs (all co-resident)
+    int nst, x_rs, xsum_off, red_off, xraw_off, ring_off;  // shared-memory layout
+    uint64_t limit_ns;
+    const uint16_t* x;                             // residual stream entering layer 0, [M][D]
+    uint16_t* logits;                              // [M][V]
+    const uint16_t* final_norm;
+    const uint8_t* readout;
+    // activation buffers by role (0 qkv, 1 h1, 2 a, 3 h): layer l uses
+    // buf[r] + l * lstride[r] + (l & 1) * astride[r] (elements)
+    uint16_t* buf[4];
+    int64_t lstride[4], astride[4];
+    unsigned* bar;                                 // [4 L + 2] stage arrival counters (zero, left zero)
+    int* status;
+    ChainLayerW layer[kChainMaxLayers];
+};
+
+// tfq_chain.cu
+cudaError_t launch_chain(int bits, const ChainParams& p, size_t smem, cudaStream_t stream);
+bool chain_fits(int bits, size_t smem);  // cooperative launch possible, one CTA per SM fits
+size_t chain_smem(int bits, int kmax, int* nst, int* x_rs, int* xsum_off, int* red_off, int* xraw_off, int* ring_off);
+
 // host helpers (tfq_api.cu)
 void set_error(const char* fmt, ...);
 int device_sms();

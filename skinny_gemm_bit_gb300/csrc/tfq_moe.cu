@@ -37,7 +37,7 @@ __global__ void __launch_bounds__(kRouteThreads) moe_route_kernel(const float* _
             const int e = lane + 32 * i;
             vals[i] = e < E ? __ldcg(l + e) : 0.f;
         }
-        float sel_val[8];
+        float top = 0.f, mine = 0.f;  // the largest selected logit; lane j: the j-th one
         for (int j = 0; j < top_k; ++j) {
             float bv = 0.f;
             int be = -1;
@@ -60,20 +60,33 @@ __global__ void __launch_bounds__(kRouteThreads) moe_route_kernel(const float* _
             }
             if ((be & 31) == lane)
                 taken |= 1u << (be >> 5);
-            sel_val[j] = bv;
+            if (j == 0)
+                top = bv;
+            if (lane == j)
+                mine = bv;
             if (lane == 0)
                 sel[warp * 8 + j] = be;
         }
-        if (lane == 0) {
-            double den = 0.0;
-            for (int j = 0; j < top_k; ++j)
-                den += exp((double)sel_val[j] - (double)sel_val[0]);
-            for (int j = 0; j < top_k; ++j) {
-                const float w = (float)(exp((double)sel_val[j] - (double)sel_val[0]) / den);
-                idx_out[warp * top_k + j] = sel[warp * 8 + j];
-                w_out[warp * top_k + j] = w;
-                meta->w[warp * 8 + j] = w;
-            }
+        // softmax over the selected logits: lane j takes exp(l_j - l_0) <= 1 (the k
+        // exponentials run side by side; 2 ulp each), every lane adds them in ascending j
+        // with Knuth's TwoSum, so the denominator is exact to about 2^-48 as the pair
+        // (s, c), and lane j divides its own: w = e / s * (1 - c / s)
+        const float ex = lane < top_k ? expf(mine - top) : 0.f;
+        float s_hi = 0.f, s_lo = 0.f;
+        for (int j = 0; j < top_k; ++j) {
+            const float a = __shfl_sync(0xffffffffu, ex, j);
+            const float t = s_hi + a;
+            const float bp = t - s_hi;
+            s_lo += (s_hi - (t - bp)) + (a - bp);
+            s_hi = t;
+        }
+        __syncwarp();
+        if (lane < top_k) {
+            const float q = ex / s_hi;
+            const float w = fmaf(-q, s_lo / s_hi, q);
+            idx_out[warp * top_k + lane] = sel[warp * 8 + lane];
+            w_out[warp * top_k + lane] = w;
+            meta->w[warp * 8 + lane] = w;
         }
     }
     __syncthreads();

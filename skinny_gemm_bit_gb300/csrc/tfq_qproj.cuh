@@ -138,13 +138,10 @@ __device__ __forceinline__ void tile_mac(const uint8_t* tile, int lane, const ui
 // ---------------------------------------------------------------- activation staging
 //
 // A staged activation buffer holds rows rows[0..Mrows) of x, columns
-// [xg0 * 64, (xg0 + xgc) * 64), row stride p.x_rs bytes (= columns * 2 + 64, so
-// that a quarter-warp's B-fragment loads from two consecutive rows never share a
-// bank). After preparation, each (group, row) block of 32 words is in B-fragment
-// order: the lane (row m, t) of an m16n8k16 MMA finds its four k-block-0/1 words at
-// 4t..4t+3 and its k-block-2/3 words at 16+4t..16+4t+3. Word p = 8 kb + 4 j + t of
-// the natural order (columns 16 kb + 8 j + 2 t + {0,1}) moves to
-// 16 (kb >> 1) + 4 t + 2 (kb & 1) + j.
+// [xg0 * 64, (xg0 + xgc) * 64), in natural (row-major) order with row stride
+// p.x_rs bytes = columns * 2 + 16: the 16-byte pieces of the 8 rows at one column
+// then fall in 8 different bank groups, so the ldmatrix that builds the MMA's B
+// fragments (8 rows x 16 bytes per matrix) is conflict-free.
 
 // One thread: copy the rows into the buffer (and, with an RMSNorm, gamma into
 // gbuf); completion on `bar`.
@@ -163,8 +160,8 @@ __device__ __forceinline__ void x_issue(const QProjParams& p, uint8_t* buf, uint
 // Consumer warps (nwarps of them, named barrier bar_id): after the copy has landed,
 // RMSNorm statistics when gamma is set (the whole row is staged then), then for the
 // groups [g_lo, g_lo + ng) of the problem (staged from group xg0): normalise and
-// round to bf16 in place, group sums of the rounded values into xs[(g - g_lo) * 8 + m]
-// (zero for rows >= Mrows), and reorder to B-fragment order.
+// round to bf16 in place (with an RMSNorm), and group sums of the values used into
+// xs[(g - g_lo) * 8 + m] (zero for rows >= Mrows).
 __device__ __forceinline__ void x_prepare(const QProjParams& p, uint8_t* buf, const uint8_t* gbuf, int Mrows, int xg0,
                                           int g_lo, int ng, float* xs, float* inv_rms, int cw, int lane, int nwarps,
                                           int bar_id)
@@ -193,22 +190,17 @@ __device__ __forceinline__ void x_prepare(const QProjParams& p, uint8_t* buf, co
     for (int i = cw * 32 + lane; i < ng * kMaxM; i += nwarps * 32)
         if ((i & 7) >= Mrows)
             xs[i] = 0.f;
-    // a lane handles one 8-column chunk cc = 2 kb + j of one (group, live row)
+    // a lane handles one 8-column chunk cc of one (group, live row)
     for (int base = cw * 4; base < ng * Mrows; base += nwarps * 4) {
         const int pi = base + (lane >> 3);
         const int cc = lane & 7;
         const int gl = pi / Mrows, m = pi - gl * Mrows;
         const bool valid = pi < ng * Mrows;
-        const bool live = valid;
         float part = 0.f;
-        uint32_t vv[4] = {0u, 0u, 0u, 0u};
-        uint32_t* blk = reinterpret_cast<uint32_t*>(buf + m * p.x_rs + (g_lo - xg0 + gl) * 128);
-        if (live) {
-            const uint4 v = reinterpret_cast<const uint4*>(blk)[cc];
-            vv[0] = v.x;
-            vv[1] = v.y;
-            vv[2] = v.z;
-            vv[3] = v.w;
+        if (valid) {
+            uint4* chunk = reinterpret_cast<uint4*>(buf + m * p.x_rs + (g_lo - xg0 + gl) * 128) + cc;
+            uint4 v = *chunk;
+            uint32_t vv[4] = {v.x, v.y, v.z, v.w};
             if (norm) {
                 const uint4 gv = *reinterpret_cast<const uint4*>(gbuf + ((g_lo + gl) * kGroup + cc * 8) * 2);
                 const uint32_t gg[4] = {gv.x, gv.y, gv.z, gv.w};
@@ -217,6 +209,7 @@ __device__ __forceinline__ void x_prepare(const QProjParams& p, uint8_t* buf, co
                 for (int q = 0; q < 4; ++q)
                     vv[q] = f32x2_to_bf16x2(bf16lo_f32(vv[q]) * inv * bf16lo_f32(gg[q]),
                                             bf16hi_f32(vv[q]) * inv * bf16hi_f32(gg[q]));
+                *chunk = make_uint4(vv[0], vv[1], vv[2], vv[3]);
             }
 #pragma unroll
             for (int q = 0; q < 4; ++q)
@@ -225,18 +218,6 @@ __device__ __forceinline__ void x_prepare(const QProjParams& p, uint8_t* buf, co
         part += __shfl_xor_sync(0xffffffffu, part, 4);
         part += __shfl_xor_sync(0xffffffffu, part, 2);
         part += __shfl_xor_sync(0xffffffffu, part, 1);
-        __syncwarp();  // every lane of the block has read it before any rewrites it
-        if (live) {
-            // the four (group, row) blocks of a warp start their four stores at different
-            // words q, so that each store instruction covers all 32 banks once
-            const int rot = lane >> 3;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int q = (j + rot) & 3;
-                const uint32_t v = q == 0 ? vv[0] : q == 1 ? vv[1] : q == 2 ? vv[2] : vv[3];
-                blk[16 * (cc >> 2) + 4 * q + (cc & 3)] = v;
-            }
-        }
         if (valid && cc == 0)
             xs[gl * kMaxM + m] = part;
     }
@@ -245,14 +226,13 @@ __device__ __forceinline__ void x_prepare(const QProjParams& p, uint8_t* buf, co
 
 // Activations of an unsplit call staged straight from global memory (where the
 // previous kernel left them, so loads bypass L1) through registers: every 8-column
-// chunk c of row m is rounded (and normalised) in registers, summed over its group
-// by the 8 lanes that hold the group, and stored in B-fragment order at
-// buf + m * x_rs + (c / 8) * 128; group sums go to xs[g * 8 + m] (zero for rows >=
-// Mrows). With an RMSNorm a warp owns a row (K <= 1024: four chunks a lane), so
+// chunk c of row m is (normalised, rounded and) summed over its group by the 8 lanes
+// that hold the group, and stored at buf + m * x_rs + c * 16; group sums go to
+// xs[g * 8 + m] (zero for rows >= Mrows). With an RMSNorm a warp owns a row (K <= 1024: four chunks a lane), so
 // the row's sum of squares is a warp reduction; without one, (row, chunk) items
 // are spread over all consumer threads, four loads in flight per thread.
 __device__ __forceinline__ void x_put_chunk(uint8_t* buf, int x_rs, float* xs, int m, int c, bool valid,
-                                            const uint32_t (&vv)[4], int lane)
+                                            const uint32_t (&vv)[4])
 {
     float part = 0.f;
 #pragma unroll
@@ -263,27 +243,26 @@ __device__ __forceinline__ void x_put_chunk(uint8_t* buf, int x_rs, float* xs, i
     part += __shfl_xor_sync(0xffffffffu, part, 1);
     if (!valid)
         return;
-    const int cc = c & 7;
-    uint32_t* blk = reinterpret_cast<uint32_t*>(buf + m * x_rs + (c >> 3) * 128);
-    const int rot = lane >> 3;  // the four 8-lane groups of a warp start at different words
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const int q = (j + rot) & 3;
-        const uint32_t v = q == 0 ? vv[0] : q == 1 ? vv[1] : q == 2 ? vv[2] : vv[3];
-        blk[16 * (cc >> 2) + 4 * q + (cc & 3)] = v;
-    }
-    if (cc == 0)
+    *reinterpret_cast<uint4*>(buf + m * x_rs + c * 16) = make_uint4(vv[0], vv[1], vv[2], vv[3]);
+    if ((c & 7) == 0)
         xs[(c >> 3) * kMaxM + m] = part;
 }
 
-__device__ __forceinline__ void x_direct(const QProjParams& p, uint8_t* buf, int Mrows, float* xs, float* ss_part,
-                                         int cw, int lane, int nwarps, int bar_id)
+// The rows x[m][0, K) (m < Mrows, row stride ldx) of an unsplit call; gamma != NULL
+// folds the RMSNorm in (K <= 1024); fragments at buf (row stride x_rs).
+// NB: loads a thread keeps in flight at once on the path without an RMSNorm (rounded
+// up to whole sets of kMaxM rows).
+template <int NB = 4>
+__device__ __forceinline__ void x_direct_raw(const uint16_t* x, int64_t ldx, int K, const uint16_t* gamma, float eps,
+                                             int x_rs, uint8_t* buf, int Mrows, float* xs, float* ss_part, int cw,
+                                             int lane, int nwarps, int bar_id)
 {
-    const int nch = p.groups * 8;  // 8-column chunks per row
-    for (int i = cw * 32 + lane; i < p.groups * kMaxM; i += nwarps * 32)
+    const int groups = K / kGroup;
+    const int nch = groups * 8;  // 8-column chunks per row
+    for (int i = cw * 32 + lane; i < groups * kMaxM; i += nwarps * 32)
         if ((i & 7) >= Mrows)
             xs[i] = 0.f;
-    if (p.gamma != nullptr) {
+    if (gamma != nullptr) {
         // WPR warps per row (the largest power of two with WPR * Mrows <= nwarps), each
         // on a run of cpw chunks (a multiple of 8, at most 4 per lane since K <= 1024);
         // the row's sum of squares is the WPR warp sums added in warp order
@@ -294,8 +273,8 @@ __device__ __forceinline__ void x_direct(const QProjParams& p, uint8_t* buf, int
         const int cpw = ((nch + WPR - 1) / WPR + 7) / 8 * 8;
         const bool row_warp = m < Mrows;  // warp-uniform
         const int c0 = sub * cpw, c1 = min(nch, c0 + cpw);
-        const uint4* g4 = reinterpret_cast<const uint4*>(p.gamma);
-        const uint4* x4 = reinterpret_cast<const uint4*>(p.x + (int64_t)(row_warp ? m : 0) * p.ldx);
+        const uint4* g4 = reinterpret_cast<const uint4*>(gamma);
+        const uint4* x4 = reinterpret_cast<const uint4*>(x + (int64_t)(row_warp ? m : 0) * ldx);
         uint4 v[4], gv[4];
         float sq[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -322,9 +301,11 @@ __device__ __forceinline__ void x_direct(const QProjParams& p, uint8_t* buf, int
             float ss = 0.f;
             for (int w = 0; w < WPR; ++w)
                 ss += ss_part[m * WPR + w];
-            const float inv = rsqrtf(ss / (float)p.K + p.eps);
+            const float inv = rsqrtf(ss / (float)K + eps);
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
+                if (c0 + j * 32 >= c1)  // warp-uniform
+                    break;
                 const int c = c0 + j * 32 + lane;
                 const uint32_t xv[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
                 const uint32_t gg[4] = {gv[j].x, gv[j].y, gv[j].z, gv[j].w};
@@ -333,29 +314,31 @@ __device__ __forceinline__ void x_direct(const QProjParams& p, uint8_t* buf, int
                 for (int q = 0; q < 4; ++q)
                     vv[q] = f32x2_to_bf16x2(bf16lo_f32(xv[q]) * inv * bf16lo_f32(gg[q]),
                                             bf16hi_f32(xv[q]) * inv * bf16hi_f32(gg[q]));
-                if (c0 + j * 32 < c1)  // warp-uniform
-                    x_put_chunk(buf, p.x_rs, xs, m, c, c < c1, vv, lane);
+                x_put_chunk(buf, x_rs, xs, m, c, c < c1, vv);
             }
         }
     } else {
-        const int items = Mrows * nch, T = nwarps * 32;
-        for (int base = 0; base < items; base += 4 * T) {
-            uint4 v[4];
-            int mm[4], cc[4];
+        // thread t takes chunks c = t, t + T, ... of every row: NB loads in flight
+        const int T = nwarps * 32;
+        for (int c_base = 0; c_base < nch; c_base += T * ((NB + kMaxM - 1) / kMaxM)) {
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int i = base + j * T + cw * 32 + lane;
-                mm[j] = i / nch;
-                cc[j] = i - mm[j] * nch;
-                v[j] = i < items ? __ldcg(reinterpret_cast<const uint4*>(p.x + (int64_t)mm[j] * p.ldx) + cc[j])
-                                 : make_uint4(0u, 0u, 0u, 0u);
-            }
+            for (int jc = 0; jc < (NB + kMaxM - 1) / kMaxM; ++jc) {
+                const int c_w = c_base + jc * T + cw * 32;  // warp-uniform
+                if (c_w >= nch)
+                    break;
+                const int c = c_w + lane;
+                uint4 v[kMaxM];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int i0 = base + j * T + cw * 32;  // warp-uniform
-                if (i0 < items) {
-                    const uint32_t vv[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
-                    x_put_chunk(buf, p.x_rs, xs, mm[j], cc[j], i0 + lane < items, vv, lane);
+                for (int m = 0; m < kMaxM; ++m)
+                    v[m] = (m < Mrows && c < nch)
+                               ? __ldcg(reinterpret_cast<const uint4*>(x + (int64_t)m * ldx) + c)
+                               : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+                for (int m = 0; m < kMaxM; ++m) {
+                    if (m >= Mrows)  // uniform
+                        break;
+                    const uint32_t vv[4] = {v[m].x, v[m].y, v[m].z, v[m].w};
+                    x_put_chunk(buf, x_rs, xs, m, c, c < nch, vv);
                 }
             }
         }
@@ -363,15 +346,31 @@ __device__ __forceinline__ void x_direct(const QProjParams& p, uint8_t* buf, int
     named_bar_sync(bar_id, nwarps * 32);
 }
 
-// The B fragments (xa: k blocks 0, 1; xb: k blocks 2, 3) of group g_rel of a buffer.
-__device__ __forceinline__ void x_frag(const uint8_t* buf, int x_rs, int gi, int tq, int g_rel, bool has_row, uint4& xa,
+__device__ __forceinline__ void x_direct(const QProjParams& p, uint8_t* buf, int Mrows, float* xs, float* ss_part,
+                                         int cw, int lane, int nwarps, int bar_id)
+{
+    x_direct_raw<4>(p.x, p.ldx, p.K, p.gamma, p.eps, p.x_rs, buf, Mrows, xs, ss_part, cw, lane, nwarps, bar_id);
+}
+
+// The B fragments (xa: k blocks 0, 1; xb: k blocks 2, 3) of group g_rel of a buffer,
+// by two ldmatrix of four 8x8 matrices each (warp-wide: every lane must call it):
+// lane l gives the address of row l % 8 of matrix l / 8 (columns 8 (l / 8) .. + 7 of
+// the half group), and receives in register i the pair (row l / 4, columns 2 (l % 4),
+// +1) of matrix i, which is its B-fragment word. Only rows < mrows are staged (and
+// addressed: the others point at row 0); their fragments read as zero.
+__device__ __forceinline__ void x_frag(const uint8_t* buf, int x_rs, int gi, int tq, int g_rel, int mrows, uint4& xa,
                                        uint4& xb)
 {
-    if (has_row) {
-        const uint4* q = reinterpret_cast<const uint4*>(buf + gi * x_rs + g_rel * 128 + tq * 16);
-        xa = q[0];
-        xb = q[4];
-    } else {
+    const int lane = gi * 4 + tq;
+    const int r = (lane & 7) < mrows ? (lane & 7) : 0;
+    const uint32_t a = smem_u32(buf + r * x_rs + g_rel * 128 + (lane >> 3) * 16);
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(xa.x), "=r"(xa.y), "=r"(xa.z), "=r"(xa.w)
+                 : "r"(a));
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(xb.x), "=r"(xb.y), "=r"(xb.z), "=r"(xb.w)
+                 : "r"(a + 64));
+    if (gi >= mrows) {
         xa = make_uint4(0u, 0u, 0u, 0u);
         xb = xa;
     }
@@ -680,9 +679,10 @@ __global__ void __launch_bounds__((NWT + 1) * 32, NWT == 8 ? 2 : 1) qproj_kernel
                     }
                 }
             }
-            // no copy may still be in flight when the CTA leaves
+            // no copy may still be in flight when the CTA leaves (also after an abort:
+            // copies complete by themselves, so this wait ignores the abort flag)
             for (int q = max(0, st_global - p.nst); q < st_global; ++q)
-                wait_or_abort(&full[q % p.nst], (q / p.nst) & 1u, flags, p.status, p.limit_ns);
+                mbar_wait_bounded(&full[q % p.nst], (q / p.nst) & 1u, p.limit_ns);
         }
         return;
     }
@@ -740,7 +740,6 @@ __global__ void __launch_bounds__((NWT + 1) * 32, NWT == 8 ? 2 : 1) qproj_kernel
             len = e.w & 0xFFFF;
         }
         const int xoff = norm ? first.y * p.Gs : 0;  // first group of the split inside the staged rows
-        const bool has_row = gi < Mrows;
         float acc0[4] = {0.f, 0.f, 0.f, 0.f}, acc1[4] = {0.f, 0.f, 0.f, 0.f};
         for (int g = 0; g < maxlen; g += p.cg, ++st_global) {
             const int s = st_global % p.nst;
@@ -752,7 +751,7 @@ __global__ void __launch_bounds__((NWT + 1) * 32, NWT == 8 ? 2 : 1) qproj_kernel
             for (int j = kp; j < cnt; j += KW) {
                 const int gl = gs + g + j;  // group within the split
                 uint4 xa, xb;
-                x_frag(xraw, p.x_rs, gi, tq, xoff + gl, has_row, xa, xb);
+                x_frag(xraw, p.x_rs, gi, tq, xoff + gl, Mrows, xa, xb);
                 const float2 xs = *reinterpret_cast<const float2*>(xsum + gl * kMaxM + 2 * tq);
                 tile_mac<BITS>(sbase + (r_me * p.cg + j) * TILE, lane, xa, xb, xs, acc0);
                 if constexpr (DUAL)
@@ -1022,9 +1021,9 @@ __global__ void __launch_bounds__(kThreads, 1) qproj_warp_kernel(const __grid_co
                     }
                 }
             }
-            // no copy may still be in flight when the CTA leaves
+            // no copy may still be in flight when the CTA leaves (also after an abort)
             for (int q = max(0, k - SW); q < k; ++q)
-                wait_or_abort(&full[lane * SW + q % SW], (q / SW) & 1u, flags, p.status, p.limit_ns);
+                mbar_wait_bounded(&full[lane * SW + q % SW], (q / SW) & 1u, p.limit_ns);
         }
         return;
     }
@@ -1084,7 +1083,6 @@ __global__ void __launch_bounds__(kThreads, 1) qproj_warp_kernel(const __grid_co
                 const uint8_t* xb = b1 ? xb1 : xb0;
                 const float* xs = b1 ? xs1 : xs0;
                 const int Mr = MOE ? slot_ec[pp].y : p.M;
-                const bool has_row = gi < Mr;
                 const int grel0 = norm ? ss * p.Gs + gl : gl;  // group of the buffer at the segment start
                 float acc0[4] = {0.f, 0.f, 0.f, 0.f}, acc1[4] = {0.f, 0.f, 0.f, 0.f};
                 for (int g = 0; g < len; g += T, ++k) {
@@ -1098,7 +1096,7 @@ __global__ void __launch_bounds__(kThreads, 1) qproj_warp_kernel(const __grid_co
                     const uint8_t* sb = ring + s * slot_bytes;
                     for (int j = 0; j < cnt; ++j) {
                         uint4 xa, xbv;
-                        x_frag(xb, p.x_rs, gi, tq, grel0 + g + j, has_row, xa, xbv);
+                        x_frag(xb, p.x_rs, gi, tq, grel0 + g + j, Mr, xa, xbv);
                         const float2 xsv = *reinterpret_cast<const float2*>(
                             xs + (norm ? ss * p.Gs + gl + g + j : gl + g + j) * kMaxM + 2 * tq);
                         tile_mac<BITS>(sb + j * TILE, lane, xa, xbv, xsv, acc0);

@@ -33,6 +33,7 @@ TF_TUNE_STAGE_GROUPS = 2
 TF_TUNE_STAGES = 3
 TF_TUNE_WARPS = 4
 TF_TUNE_MODE = 5
+TF_TUNE_CHAIN = 6
 
 P = ctypes.c_void_p
 I64 = ctypes.c_int64

@@ -118,11 +118,29 @@ def _check_decoder(T, cfg, M, readout_rows=None):
     assert_close(lg, ref["logits"], tol_linear(ref["logits_abs"]), "logits")
 
 
+@pytest.mark.parametrize("per_projection", [False, True])
 @pytest.mark.parametrize("M", [1, 3, 8])
-def test_decoder_small(T, M):
+def test_decoder_small(T, M, per_projection):
+    # default: the whole step in one persistent kernel; per_projection: one kernel per projection
     cfg = synth.decoder(seed=30 + M, n_layers=3, d_model=256, d_ff=384, n_q_heads=4, n_kv_heads=2, head_dim=64,
                         vocab=1000, M=M)
-    _check_decoder(T, cfg, M)
+    T.tune_set(T.TF_TUNE_CHAIN, 1 if per_projection else -1)
+    try:
+        _check_decoder(T, cfg, M)
+    finally:
+        T.tune_set(T.TF_TUNE_CHAIN, -1)
+
+
+def test_decoder_step_leaves_workspace_clean_and_repeats_exactly(T):
+    cfg = synth.decoder(seed=39, n_layers=2, d_model=256, d_ff=384, n_q_heads=4, n_kv_heads=2, head_dim=64,
+                        vocab=1000, M=4)
+    dec = _pack_decoder(T, cfg)
+    x = dev_bf16(cfg["x"])
+    ws = T.workspace(T.tf_decode_step_workspace_bytes(dec, 4))
+    outs = [T.tf_decode_step_run(dec, x, ws=ws).clone() for _ in range(3)]
+    for o in outs[1:]:
+        assert torch.equal(o, outs[0])
+    assert T.tf_workspace_status(ws) == T.TF_OK
 
 
 @pytest.mark.parametrize("M", [1, 8])
