@@ -155,8 +155,13 @@ __device__ bool grid_wait(const ChainParams& p, int s, volatile int* flags)
             }
         }
     }
-    __threadfence();
-    return true;
+    return true;  // the acquire load orders every later read after the arrivals
+}
+
+// Thread 0, after the CTA's barrier: release the CTA's stores of stage s and arrive.
+__device__ __forceinline__ void grid_arrive(const ChainParams& p, int s)
+{
+    asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(p.bar + s) : "memory");
 }
 
 // Block rb's outputs from one lane's accumulator fragment (rows rb*16 + gi, + 8;
@@ -229,7 +234,8 @@ __global__ void __launch_bounds__(kChainThreads, 1) chain_kernel(const __grid_co
     if (warp == kChainWarps) {
         if (lane == 0) {
             const uint64_t pol = policy_evict_first();
-            int seq = 0;
+            int seq = 0, pslot = 0;
+            uint32_t pphase = 0;
             bool ok = true;
             for (int s = 0; s < S && ok; ++s) {
                 const StageDesc d = stage_desc(p, s);
@@ -238,8 +244,13 @@ __global__ void __launch_bounds__(kChainThreads, 1) chain_kernel(const __grid_co
                 for (int t = 0; t < rounds && ok; ++t) {
                     const int nv = min(d.R, nb - t * d.R);
                     for (int k = 0; k < steps; ++k, ++seq) {
-                        const int slot = seq % p.nst;
-                        if (!wait_or_abort(&empty[slot], ((seq / p.nst) & 1u) ^ 1u, flags, p.status, p.limit_ns)) {
+                        const int slot = pslot;
+                        const uint32_t ph = pphase;
+                        if (++pslot == p.nst) {
+                            pslot = 0;
+                            pphase ^= 1u;
+                        }
+                        if (!wait_or_abort(&empty[slot], ph ^ 1u, flags, p.status, p.limit_ns)) {
                             ok = false;
                             break;
                         }
@@ -266,7 +277,8 @@ __global__ void __launch_bounds__(kChainThreads, 1) chain_kernel(const __grid_co
 
     // ------------------------------------------------------------ consumers
     const int cw = warp, gi = lane >> 2, tq = lane & 3;
-    int seq = 0;
+    int slot = 0;
+    uint32_t phase = 0;
     bool alive = true;
     for (int s = 0; s < S; ++s) {
         const StageDesc d = stage_desc(p, s);
@@ -297,26 +309,53 @@ __global__ void __launch_bounds__(kChainThreads, 1) chain_kernel(const __grid_co
             const int kb = t * d.R + r_me;
             const bool valid = kb < nb;
             float acc0[4] = {0.f, 0.f, 0.f, 0.f}, acc1[4] = {0.f, 0.f, 0.f, 0.f};
-            for (int k = 0; k < steps; ++k, ++seq) {
-                const int slot = seq % p.nst;
-                const bool ok = alive && wait_or_abort(&full[slot], (seq / p.nst) & 1u, flags, p.status, p.limit_ns);
+            float bcc0[4] = {0.f, 0.f, 0.f, 0.f}, bcc1[4] = {0.f, 0.f, 0.f, 0.f};  // second chain
+            for (int k = 0; k < steps; ++k) {
+                const bool ok = alive && wait_or_abort(&full[slot], phase, flags, p.status, p.limit_ns);
                 alive = __all_sync(0xffffffffu, ok);
                 const int cnt = min(d.cg, d.groups - k * d.cg);
                 if (alive && valid) {
                     const uint8_t* sb = ring + slot * SLOT;
-                    for (int j = kp; j < cnt; j += KW) {
+                    const uint8_t* t0 = sb + (r_me * d.cg) * TILE;
+                    const uint8_t* t1 = sb + ((d.R + r_me) * d.cg) * TILE;
+                    int j = kp;
+                    // two tiles per iteration into separate accumulators: independent chains
+                    for (; j + KW < cnt; j += 2 * KW) {
+                        const int g = k * d.cg + j;
+                        uint4 xa, xb, ya, yb;
+                        x_frag(xraw, p.x_rs, gi, tq, g, p.M, xa, xb);
+                        x_frag(xraw, p.x_rs, gi, tq, g + KW, p.M, ya, yb);
+                        const float2 xs = *reinterpret_cast<const float2*>(xsum + g * kMaxM + 2 * tq);
+                        const float2 ys = *reinterpret_cast<const float2*>(xsum + (g + KW) * kMaxM + 2 * tq);
+                        tile_mac<BITS>(t0 + j * TILE, lane, xa, xb, xs, acc0);
+                        tile_mac<BITS>(t0 + (j + KW) * TILE, lane, ya, yb, ys, bcc0);
+                        if (d.mats == 2) {
+                            tile_mac<BITS>(t1 + j * TILE, lane, xa, xb, xs, acc1);
+                            tile_mac<BITS>(t1 + (j + KW) * TILE, lane, ya, yb, ys, bcc1);
+                        }
+                    }
+                    if (j < cnt) {
                         const int g = k * d.cg + j;
                         uint4 xa, xb;
                         x_frag(xraw, p.x_rs, gi, tq, g, p.M, xa, xb);
                         const float2 xs = *reinterpret_cast<const float2*>(xsum + g * kMaxM + 2 * tq);
-                        tile_mac<BITS>(sb + (r_me * d.cg + j) * TILE, lane, xa, xb, xs, acc0);
+                        tile_mac<BITS>(t0 + j * TILE, lane, xa, xb, xs, acc0);
                         if (d.mats == 2)
-                            tile_mac<BITS>(sb + ((d.R + r_me) * d.cg + j) * TILE, lane, xa, xb, xs, acc1);
+                            tile_mac<BITS>(t1 + j * TILE, lane, xa, xb, xs, acc1);
                     }
                 }
                 __syncwarp();
                 if (lane == 0)
                     mbar_arrive(&empty[slot]);
+                if (++slot == p.nst) {
+                    slot = 0;
+                    phase ^= 1u;
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                acc0[i] += bcc0[i];
+                acc1[i] += bcc1[i];
             }
             // sum the KW warps of the block (team barrier 1 + r_me)
             if (KW > 1) {
@@ -354,10 +393,8 @@ __global__ void __launch_bounds__(kChainThreads, 1) chain_kernel(const __grid_co
         // here, whatever its own waits returned)
         __syncwarp();
         named_bar_sync(kChainBarAll, kChainWarps * 32);
-        if (threadIdx.x == 0 && !flags[0]) {
-            __threadfence();
-            atomicAdd(p.bar + s, 1u);
-        }
+        if (threadIdx.x == 0 && !flags[0])
+            grid_arrive(p, s);
     }
     // the last CTA to finish resets every counter (nobody waits on them any more)
     if (threadIdx.x == 0 && !flags[0]) {
