@@ -28,7 +28,7 @@
 namespace tfq {
 namespace {
 
-constexpr int kChainWarps = 8;
+constexpr int kChainWarps = 16;
 constexpr int kChainThreads = (kChainWarps + 1) * 32;
 constexpr int kChainBarAll = 15;  // named barrier of the consumer warps; 1, 2 are team barriers
 
@@ -116,7 +116,7 @@ __device__ __forceinline__ StageDesc stage_desc(const ChainParams& p, int s)
     // blocks per CTA each warp owns whole blocks and no warp sums are needed
     const int per_cta = (d.n_rb + p.C - 1) / p.C;
     d.R = 1;
-    while (2 * d.R <= per_cta && 2 * d.R <= kChainWarps)
+    while (2 * d.R <= per_cta && 2 * d.R <= 8)
         d.R *= 2;
     d.cg = kChainSlotTiles / (d.mats * d.R);
     return d;
@@ -202,8 +202,9 @@ __device__ __forceinline__ void store_block(const StageDesc& d, int rb, int lane
     }
 }
 
+// 17 warps x 32 threads x 120 registers fit one SM's register file
 template <int BITS>
-__global__ void __launch_bounds__(kChainThreads, 1) chain_kernel(const __grid_constant__ ChainParams p)
+__global__ void __maxnreg__(120) chain_kernel(const __grid_constant__ ChainParams p)
 {
     constexpr int TILE = tile_bytes_for(BITS);
     constexpr int SLOT = kChainSlotTiles * TILE;
