@@ -7,14 +7,20 @@ whose total is more than four times the L2 cache, so every call streams its
 weights from HBM. Steps are captured once into a CUDA graph and replayed.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl tfq|reference]
-                  [--workload gateup|proj|wide|step|moe4|moe8|all]
+                  [--workload gateup|proj|wide|step|moe4|moe8]
+
+The other workloads: proj (one K=1024, N=3072 projection, M=1), wide (K=12800,
+N=2560, one M=1 and one M=8 call), step (the whole per-token weight stream of a
+28-layer dense decoder, one M=1 and one M=8 step), moe4 / moe8 (the MoE layer,
+M=8, one call).
 
 value      effective weight GB/s: algorithmic weight bytes (codes + scales +
            biases) of all calls / device time of the timed region.
 e2e        the same metric with the per-step activations copied in from pinned
            host memory and the outputs copied back inside the timed region.
-roofline   the dominant kernel's bytes per launch / its mean launch time against
-           the measured HBM copy bandwidth.
+roofline   bytes per call / mean call time of the timed region against the
+           measured HBM copy bandwidth; a call is one launch of the named kernel
+           (four launches for the MoE layer).
 cpu_baseline  the fp64 oracle on a bounded sample, on this host's cores.
 
 Under torchrun (N > 1) every rank runs an independent replica of the workload
@@ -166,23 +172,84 @@ def barrier(pg):
 # ----------------------------------------------------------------------------- workloads
 
 class Workload:
-    """A sequence of calls per step over rotating weight copies."""
+    """A sequence of calls per step (one per entry of `step_ms`) over rotating weight copies.
 
-    name = ""
-    kernel_key = ""
+    Subclasses set: name, kernel_key, kernel, desc, K, N, bits, per_call (weight bytes of
+    one call), n_copies, and implement call(copy, M, flags, x, out) plus the host sample of
+    the oracle."""
 
-    def __init__(self, T, torch, copies_bytes_min: int):
-        self.T = T
-        self.torch = torch
+    step_ms = (1, 8)
 
-    def weight_bytes_per_step(self) -> int:
-        raise NotImplementedError
+    def __init__(self, T, torch):
+        self.T, self.torch = T, torch
 
-    def step(self, i: int, flags: int):
-        raise NotImplementedError
+    # inputs per M: device tensors (used by the timed steps) and pinned host copies
+    def _io(self, x8_u16, out_cols):
+        torch = self.torch
+        self.x = {}
+        self.out = {}
+        self.x_h = {}
+        self.out_h = {}
+        for M in sorted(set(self.step_ms)):
+            self.x[M] = _dev_bf16(torch, x8_u16[:M])
+            self.out[M] = torch.empty((M, out_cols), dtype=torch.bfloat16, device="cuda")
+            self.x_h[M] = self.x[M].cpu().pin_memory()
+            self.out_h[M] = torch.empty_like(self.out[M], device="cpu").pin_memory()
 
-    def step_e2e(self, i: int, flags: int):
-        raise NotImplementedError
+    @property
+    def launches_per_step(self):
+        return len(self.step_ms) * self.launches_per_call
+
+    launches_per_call = 1
+
+    def weight_bytes_per_step(self):
+        return len(self.step_ms) * self.per_call
+
+    def step(self, i, flags):
+        for j, M in enumerate(self.step_ms):
+            self.call((len(self.step_ms) * i + j) % self.n_copies, M, flags, self.x[M], self.out[M])
+
+    def step_e2e(self, i, flags):
+        for j, M in enumerate(self.step_ms):
+            self.x[M].copy_(self.x_h[M], non_blocking=True)
+            self.call((len(self.step_ms) * i + j) % self.n_copies, M, 0, self.x[M], self.out[M])
+            self.out_h[M].copy_(self.out[M], non_blocking=True)
+
+    def io_bytes(self):
+        return (sum(self.x[M].numel() * 2 for M in self.step_ms),
+                sum(self.out[M].numel() * 2 for M in self.step_ms))
+
+    def per_m(self, flags, reps=100):
+        """Mean device time per call for each M (graph-replayed)."""
+        out = {}
+        for M in sorted(set(self.step_ms)):
+            def one(i, M=M):
+                self.call(i % self.n_copies, M, flags, self.x[M], self.out[M])
+            ms = time_graph(self.torch, one, reps)
+            out[M] = ms * 1e3 / reps
+        return out
+
+    def oracle_sample(self, seconds: float):
+        """The fp64 oracle on a row subset of one matrix of the workload, M as in a step,
+        for about `seconds`; returns (weight bytes covered, seconds, description)."""
+        import oracle
+        w, rows, what = self.sample_matrix()
+        sub = {"wq": w["wq"][:rows], "scales": w["scales"][:rows], "biases": w["biases"][:rows],
+               "N": rows, "K": w["K"], "bits": w["bits"]}
+        x = oracle.bf16_to_f64(self.sample_x)
+        per = rows * w["K"] * (w["bits"] / 8 + 4 / 64)
+        done, t0, reps = 0, time.perf_counter(), 0
+        while True:
+            for M in self.step_ms:
+                oracle.qlinear(x[:M], sub)
+                done += per
+            reps += 1
+            if time.perf_counter() - t0 >= seconds:
+                break
+        el = time.perf_counter() - t0
+        ms = " and ".join(f"M={M}" for M in self.step_ms)
+        return done, el, (f"{reps} x ({ms} calls of the projection oracle on the first {rows} rows of {what}, "
+                          f"K={w['K']}), single thread")
 
 
 def _dev_bf16(torch, u16):
@@ -200,76 +267,44 @@ def _clone_qweight(T, qw):
     return T.QWeight(buf, desc)
 
 
+def _pack(T, w):
+    return T.tf_qlinear_pack(w["wq"], w["scales"], w["biases"], w["bits"])
+
+
 class GateUp(Workload):
     """Fused RMSNorm + gate/up SwiGLU, K=1024, N=2x3072; one M=1 and one M=8 call per step."""
 
+    name = "gateup"
     kernel_key = "qproj_b4_dual_k1024_n3072"
+    kernel = "qproj_kernel<4, dual> (light team schedule)"
 
     def __init__(self, T, torch, l2_bytes, K=1024, N=3072):
+        super().__init__(T, torch)
         from skinny_gemm_bit_gb300 import synth
-        self.T, self.torch = T, torch
         cfg = synth.fused_gateup(seed=1, M=8, K=K, N=N)
-        self.K, self.N = K, N
-        g = T.tf_qlinear_pack(cfg["gate"]["wq"], cfg["gate"]["scales"], cfg["gate"]["biases"], 4)
-        u = T.tf_qlinear_pack(cfg["up"]["wq"], cfg["up"]["scales"], cfg["up"]["biases"], 4)
+        self.cfg = cfg
+        self.K, self.N, self.bits = K, N, 4
+        g, u = _pack(T, cfg["gate"]), _pack(T, cfg["up"])
         self.per_call = g.weight_bytes() + u.weight_bytes()
         n = _rotations(g.buf.numel() + u.buf.numel(), l2_bytes)
         self.copies = [(g, u)] + [(_clone_qweight(T, g), _clone_qweight(T, u)) for _ in range(n - 1)]
+        self.n_copies = n
         self.gamma = _dev_bf16(torch, cfg["gamma"])
         self.eps = cfg["eps"]
-        self.x8 = _dev_bf16(torch, cfg["x"])
-        self.x1 = self.x8[:1].clone()
-        self.h1 = torch.empty((1, N), dtype=torch.bfloat16, device="cuda")
-        self.h8 = torch.empty((8, N), dtype=torch.bfloat16, device="cuda")
+        self._io(cfg["x"], N)
         self.ws = T.workspace(T.tf_qmlp_gateup_workspace_bytes(g, u, 8))
-        # host side of the end-to-end variant
-        self.x1_h = self.x1.cpu().pin_memory()
-        self.x8_h = self.x8.cpu().pin_memory()
-        self.h1_h = torch.empty_like(self.h1, device="cpu").pin_memory()
-        self.h8_h = torch.empty_like(self.h8, device="cpu").pin_memory()
-        self.n_copies = n
-        self.launches_per_step = 2
+        self.sample_x = cfg["x"]
         self.desc = (f"fused RMSNorm + gate/up SwiGLU projection, 4-bit group-64, K={K}, N=2x{N}; "
                      f"one M=1 and one M=8 call per step")
 
-    def weight_bytes_per_step(self):
-        return 2 * self.per_call
-
-    def _calls(self, i, flags):
-        g, u = self.copies[(2 * i) % self.n_copies]
-        self.T.tf_qmlp_gateup_run(g, u, self.x1, self.gamma, self.eps, out=self.h1, ws=self.ws, flags=flags)
-        g, u = self.copies[(2 * i + 1) % self.n_copies]
-        self.T.tf_qmlp_gateup_run(g, u, self.x8, self.gamma, self.eps, out=self.h8, ws=self.ws, flags=flags)
-
-    def step(self, i, flags):
-        self._calls(i, flags)
-
-    def step_e2e(self, i, flags):
-        self.x1.copy_(self.x1_h, non_blocking=True)
-        self.x8.copy_(self.x8_h, non_blocking=True)
-        self._calls(i, 0)
-        self.h1_h.copy_(self.h1, non_blocking=True)
-        self.h8_h.copy_(self.h8, non_blocking=True)
-
-    def io_bytes(self):
-        return (self.x1.numel() + self.x8.numel()) * 2, (self.h1.numel() + self.h8.numel()) * 2
-
-    def per_m(self, flags, reps=200):
-        """Mean device time per call for M=1 and M=8 separately (graph-replayed)."""
-        out = {}
-        for M, x, h in ((1, self.x1, self.h1), (8, self.x8, self.h8)):
-            def one(i):
-                g, u = self.copies[i % self.n_copies]
-                self.T.tf_qmlp_gateup_run(g, u, x, self.gamma, self.eps, out=h, ws=self.ws, flags=flags)
-            ms = time_graph(self.torch, one, reps)
-            out[M] = ms * 1e3 / reps
-        return out
+    def call(self, i, M, flags, x, out):
+        g, u = self.copies[i]
+        self.T.tf_qmlp_gateup_run(g, u, x, self.gamma, self.eps, out=out, ws=self.ws, flags=flags)
 
     def oracle_sample(self, seconds: float):
-        """Run the fp64 oracle on gate/up rows for about `seconds`; returns (weight bytes, s, desc)."""
+        """The fused RMSNorm + gate/up oracle on the first 256 rows of each matrix."""
         import oracle
-        from skinny_gemm_bit_gb300 import synth
-        cfg = synth.fused_gateup(seed=1, M=8, K=self.K, N=self.N)
+        cfg = self.cfg
         rows = 256
         sub = lambda w: {"wq": w["wq"][:rows], "scales": w["scales"][:rows], "biases": w["biases"][:rows],  # noqa
                          "N": rows, "K": w["K"], "bits": w["bits"]}
@@ -287,6 +322,140 @@ class GateUp(Workload):
         el = time.perf_counter() - t0
         return done, el, (f"{reps} x (M=1 and M=8 calls of the fused RMSNorm + gate/up oracle on the first "
                           f"{rows} of {self.N} rows of each matrix, K={self.K}), single thread")
+
+
+class Proj(Workload):
+    """One 4-bit projection per step: K=1024, N=3072, M=1 (single projection), or
+    K=12800, N=2560 at M=1 and M=8 (wide verify projection)."""
+
+    def __init__(self, T, torch, l2_bytes, wide: bool):
+        super().__init__(T, torch)
+        from skinny_gemm_bit_gb300 import synth
+        if wide:
+            cfg = synth.wide_verify(seed=2, M=8)
+            self.name, self.step_ms = "wide", (1, 8)
+            self.kernel_key, self.kernel = "qproj_b4_k12800_n2560", "qproj_warp_kernel<4> (split K)"
+        else:
+            cfg = synth.single_projection(seed=0, M=1)
+            self.name, self.step_ms = "proj", (1,)
+            self.kernel_key, self.kernel = "qproj_b4_k1024_n3072", "qproj_kernel<4> (light team schedule)"
+        w0 = _pack(T, cfg["w"])
+        self.w = cfg["w"]
+        self.K, self.N, self.bits = w0.K, w0.N, 4
+        self.per_call = w0.weight_bytes()
+        n = _rotations(w0.buf.numel(), l2_bytes)
+        self.copies = [w0] + [_clone_qweight(T, w0) for _ in range(n - 1)]
+        self.n_copies = n
+        x8 = cfg["x"] if cfg["x"].shape[0] == 8 else np.repeat(cfg["x"], 8, axis=0)
+        self._io(x8, self.N)
+        self.ws = T.workspace(T.tf_qlinear_workspace_bytes(w0, 8))
+        self.sample_x = x8
+        ms = " and ".join(f"M={M}" for M in self.step_ms)
+        self.desc = (f"{'wide verify' if wide else 'single'} 4-bit group-64 projection, K={self.K}, N={self.N}; "
+                     f"one {ms} call per step")
+
+    def call(self, i, M, flags, x, out):
+        self.T.tf_qlinear_run(self.copies[i], x, out=out, ws=self.ws, flags=flags)
+
+    def sample_matrix(self):
+        return self.w, 256 if self.K <= 2048 else 32, "the weight matrix"
+
+
+class Step(Workload):
+    """The per-token weight stream of a 28-layer dense decoder (d_model 1024, d_ff 3072,
+    16 q / 8 kv heads of 128, tied readout 151,936), one M=1 and one M=8 step per bench step."""
+
+    name = "step"
+    kernel_key = "chain_b4_l28_d1024"
+    kernel = "chain_kernel<4> (whole step, one launch)"
+
+    def __init__(self, T, torch, l2_bytes):
+        super().__init__(T, torch)
+        from skinny_gemm_bit_gb300 import synth
+        cfg = synth.decoder(M=8)
+        self.cfg = cfg
+        d = cfg["dims"]
+        layers = []
+        for L in cfg["layers"]:
+            layers.append({k: (_pack(T, v) if k in ("qkv", "o", "gate", "up", "down") else _dev_bf16(torch, v))
+                           for k, v in L.items()})
+        self.dec = T.Decoder(layers, _dev_bf16(torch, cfg["final_norm"]), _pack(T, cfg["readout"]), d["d_model"],
+                             d["d_ff"], d["q_dim"], d["kv_dim"], cfg["eps"])
+        self.K, self.N, self.bits = d["d_model"], d["vocab"], 4
+        self.per_call = self.dec.weight_bytes()
+        self.copies = [self.dec]  # 335 MB per step: more than twice L2 already
+        self.n_copies = 1
+        self._io(cfg["x"], d["vocab"])
+        self.ws = T.workspace(T.tf_decode_step_workspace_bytes(self.dec, 8))
+        self.sample_x = cfg["x"]
+        self.desc = ("per-token weight stream of a 28-layer dense decoder, 4-bit group-64: norm+QKV, O, "
+                     "norm+gate/up+SwiGLU, down per layer, norm+tied readout 151936x1024; one M=1 and one M=8 step")
+
+    def call(self, i, M, flags, x, out):
+        self.T.tf_decode_step_run(self.dec, x, out=out, ws=self.ws, flags=flags)
+
+    def sample_matrix(self):
+        return self.cfg["layers"][0]["qkv"], 256, "layer 0's QKV matrix"
+
+
+class MoE(Workload):
+    """MoE expert projection: M=8 rows, 128 experts, top-8, hidden 2048, intermediate 768."""
+
+    step_ms = (8,)
+    launches_per_call = 4
+
+    def __init__(self, T, torch, l2_bytes, bits: int):
+        super().__init__(T, torch)
+        from skinny_gemm_bit_gb300 import synth
+        cfg = synth.moe_layer(bits=bits)
+        self.cfg = cfg
+        self.name = f"moe{bits}"
+        self.kernel_key = f"moe_b{bits}"
+        self.kernel = f"MoE layer ({bits}-bit): route, gate/up, down, combine"
+        g, u, dn = _pack(T, cfg["gate"]), _pack(T, cfg["up"]), _pack(T, cfg["down"])
+        self.logits = torch.from_numpy(cfg["logits"]).cuda()
+        self.K, self.N, self.bits = 2048, 768, bits
+        stack = g.buf.numel() + u.buf.numel() + dn.buf.numel()
+        n = max(2, int(np.ceil(2 * l2_bytes / stack)) + 1)
+        self.copies = [(g, u, dn)] + [tuple(_clone_qweight(T, w) for w in (g, u, dn)) for _ in range(n - 1)]
+        self.n_copies = n
+        self._io(cfg["x"], 2048)
+        self.ws = T.workspace(T.tf_qmoe_workspace_bytes(g, u, dn, 8, 8))
+        self.idx = torch.empty((8, 8), dtype=torch.int32, device="cuda")
+        self.wts = torch.empty((8, 8), dtype=torch.float32, device="cuda")
+        _, idx, _ = T.tf_qmoe_run(g, u, dn, self.logits, self.x[8], 8, ws=self.ws)
+        torch.cuda.synchronize()
+        distinct = len(np.unique(idx.cpu().numpy()))
+        self.per_call = distinct * (g.weight_bytes() + u.weight_bytes() + dn.weight_bytes()) // 128
+        self.sample_x = cfg["x"]
+        self.desc = (f"MoE expert projection, M=8, 128 experts, top-8, hidden 2048, intermediate 768, {bits}-bit "
+                     f"group-64 gate/up/down ({distinct} distinct experts read); one call per step")
+
+    def call(self, i, M, flags, x, out):
+        g, u, dn = self.copies[i]
+        self.T.tf_qmoe_run(g, u, dn, self.logits, x, 8, out=out, idx=self.idx, wts=self.wts, ws=self.ws,
+                           flags=flags)
+
+    def sample_matrix(self):
+        w = self.cfg["gate"]
+        e0 = {"wq": w["wq"][0], "scales": w["scales"][0], "biases": w["biases"][0], "N": w["N"], "K": w["K"],
+              "bits": w["bits"]}
+        return e0, 128, "expert 0's gate matrix"
+
+
+WORKLOADS = ("gateup", "proj", "wide", "step", "moe4", "moe8")
+
+
+def make_workload(name, T, torch, l2_bytes):
+    if name == "gateup":
+        return GateUp(T, torch, l2_bytes)
+    if name in ("proj", "wide"):
+        return Proj(T, torch, l2_bytes, wide=name == "wide")
+    if name == "step":
+        return Step(T, torch, l2_bytes)
+    if name in ("moe4", "moe8"):
+        return MoE(T, torch, l2_bytes, bits=int(name[3]))
+    raise ValueError(name)
 
 
 def time_graph(torch, fn, n):
@@ -325,7 +494,7 @@ def run_tfq(args):
 
     props = torch.cuda.get_device_properties(local)
     l2 = getattr(props, "L2_cache_size", 126 * 1024 * 1024) or 126 * 1024 * 1024
-    wl = GateUp(T, torch, l2)
+    wl = make_workload(args.workload, T, torch, l2)
     flags = T.TF_RUN_PDL
     K, W = args.steps, args.warmup
 
@@ -392,17 +561,20 @@ def run_tfq(args):
     bytes_step = wl.weight_bytes_per_step()
     value = world * bytes_step * K / (ms_max * 1e-3) / 1e9
     e2e_value = world * bytes_step * K / (ms_e2e * 1e-3) / 1e9
-    launch_us = ms_max * 1e3 / (K * wl.launches_per_step)
-    achieved = wl.per_call / (launch_us * 1e-6) / 1e9
+    call_us = ms_max * 1e3 / (K * len(wl.step_ms))
+    achieved = wl.per_call / (call_us * 1e-6) / 1e9
     cpu = cpu_baseline(wl, args.cpu_seconds)
     h2d, d2h = wl.io_bytes()
+    ms_list = sorted(set(wl.step_ms))
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": W,
         "ms_per_step": round(ms_max / K, 6), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16", "data": "synthetic (seeded random 4-bit weights and N(0,1) activations)",
-        "config": {"workload": wl.desc, "K": wl.K, "N": 2 * wl.N, "M": [1, 8], "bits": 4, "group": 64,
-                   "l2": f"weights rotate over {wl.n_copies} copies ({wl.n_copies * bytes_step / 2 / 1e6:.0f} MB, "
-                         f"> 4x L2), every call reads HBM", "graph": "CUDA graph, programmatic dependent launch",
+        "dtype": "bf16", "data": f"synthetic (seeded random {wl.bits}-bit weights and N(0,1) activations)",
+        "config": {"workload": wl.desc, "name": wl.name, "K": wl.K, "N": wl.N, "M": ms_list, "bits": wl.bits,
+                   "group": 64,
+                   "l2": (f"weights rotate over {wl.n_copies} copies, more than four times L2, every call reads HBM"
+                          if wl.n_copies > 1 else "every call streams more than twice L2 from HBM"),
+                   "graph": "CUDA graph" + (", programmatic dependent launch" if flags else ""),
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "pct_of_hbm_measured": round(100 * value / world / peak, 2),
         "pct_of_8tbs_nominal": round(100 * value / world / NOMINAL_HBM_GBS, 2),
@@ -410,11 +582,11 @@ def run_tfq(args):
                   for M, us in per_m.items()},
         "per_m_no_pdl": {str(M): {"us_per_call": round(us, 3), "gbs": round(wl.per_call / (us * 1e-6) / 1e9, 1)}
                          for M, us in per_m_nopdl.items()},
-        "m8_over_m1": round(per_m[8] / per_m[1], 3),
+        "m8_over_m1": round(per_m[8] / per_m[1], 3) if 1 in per_m and 8 in per_m else None,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": recorded_traffic(wl.kernel_key),
-                     "peak_source": peak_kind, "kernel": "qproj_kernel<4, dual>",
-                     "bytes_per_launch": wl.per_call, "launch_us": round(launch_us, 3)},
+                     "peak_source": peak_kind, "kernel": wl.kernel,
+                     "bytes_per_launch": wl.per_call, "launch_us": round(call_us, 3)},
         "cpu_baseline": cpu,
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": K * wl.launches_per_step,
@@ -430,6 +602,55 @@ def cpu_baseline(wl, seconds):
     return {"value": round(done / el / 1e9, 6), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": desc}
 
 
+class _HostOnly:
+    """The CPU side of a workload (its oracle sample), without packing anything on a GPU."""
+
+    def __init__(self, name):
+        from skinny_gemm_bit_gb300 import synth
+        self.name = name
+        if name == "gateup":
+            self.impl = GateUp.__new__(GateUp)
+            cfg = synth.fused_gateup(seed=1, M=8)
+            self.impl.cfg, self.impl.K, self.impl.N = cfg, 1024, 3072
+            self.desc = ("fused RMSNorm + gate/up SwiGLU projection, 4-bit group-64, K=1024, N=2x3072; "
+                         "one M=1 and one M=8 call per step")
+            self.K, self.N, self.ms, self.bits = 1024, 3072, [1, 8], 4
+        else:
+            self.impl = Workload.__new__(Workload)
+            if name in ("proj", "wide"):
+                cfg = synth.wide_verify(seed=2, M=8) if name == "wide" else synth.single_projection(seed=0, M=1)
+                w = cfg["w"]
+                x8 = cfg["x"] if cfg["x"].shape[0] == 8 else np.repeat(cfg["x"], 8, axis=0)
+                rows, what = (256, "the weight matrix") if w["K"] <= 2048 else (32, "the weight matrix")
+                self.impl.step_ms = (1, 8) if name == "wide" else (1,)
+                self.K, self.N, self.bits = w["K"], w["N"], 4
+                self.desc = f"{name} 4-bit group-64 projection, K={w['K']}, N={w['N']}"
+            elif name == "step":
+                cfg = synth.decoder(M=8, n_layers=1)  # layer 0 of the same seeded model
+                w, x8, rows, what = cfg["layers"][0]["qkv"], cfg["x"], 256, "layer 0's QKV matrix"
+                self.impl.step_ms = (1, 8)
+                self.K, self.N, self.bits = 1024, 151936, 4
+                self.desc = "per-token weight stream of a 28-layer dense decoder (sampled: layer 0 QKV rows)"
+            else:
+                bits = int(name[3])
+                cfg = synth.moe_layer(bits=bits)
+                g = cfg["gate"]
+                w = {"wq": g["wq"][0], "scales": g["scales"][0], "biases": g["biases"][0], "N": g["N"], "K": g["K"],
+                     "bits": g["bits"]}
+                x8, rows, what = cfg["x"], 128, "expert 0's gate matrix"
+                self.impl.step_ms = (8,)
+                self.K, self.N, self.bits = 2048, 768, bits
+                self.desc = f"MoE expert projection, M=8, 128 experts, top-8, {bits}-bit (sampled: expert 0 gate rows)"
+            self.impl.sample_x = x8
+            self.impl.sample_matrix = lambda w=w, rows=rows, what=what: (w, rows, what)
+            self.ms = sorted(set(self.impl.step_ms))
+
+    def oracle_sample(self, seconds):
+        if self.name == "gateup":
+            return GateUp.oracle_sample(self.impl, seconds)
+        return Workload.oracle_sample(self.impl, seconds)
+
+
 def run_reference(args):
     """The fp64 oracle as the reference arm, on this host's cores, rank 0 only."""
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -437,18 +658,12 @@ def run_reference(args):
     if rank != 0:
         return
     import oracle
-
-    class _Host:
-        pass
-
-    wl = GateUp.__new__(GateUp)
-    wl.K, wl.N = 1024, 3072
+    oracle.build()
+    host = _HostOnly(args.workload)
     desc = None
     steps_s = []
-    oracle.build()
     for i in range(args.warmup + args.steps):
-        t0 = time.perf_counter()
-        done, el, desc = wl.oracle_sample(args.ref_step_seconds)
+        done, el, desc = host.oracle_sample(args.ref_step_seconds)
         if i >= args.warmup:
             steps_s.append((done, el))
     total_b = sum(d for d, _ in steps_s)
@@ -458,10 +673,9 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * total_s / args.steps, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic (seeded random 4-bit weights and N(0,1) activations)",
-        "config": {"workload": "fused RMSNorm + gate/up SwiGLU projection, 4-bit group-64, K=1024, N=2x3072; "
-                               "one M=1 and one M=8 call per step", "K": 1024, "N": 6144, "M": [1, 8],
-                   "bits": 4, "group": 64},
+        "data": f"synthetic (seeded random {host.bits}-bit weights and N(0,1) activations)",
+        "config": {"workload": host.desc, "name": host.name, "K": host.K, "N": host.N, "M": host.ms,
+                   "bits": host.bits, "group": 64},
         "cpu_baseline": {"value": round(value, 6), "unit": "GB/s", "kind": "oracle", "cores": 1,
                          "sample": f"each step: {desc}"},
         "e2e": {"value": round(value, 6), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -477,6 +691,10 @@ def main():
     ap.add_argument("--impl", default="tfq", choices=["tfq", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--ref-step-seconds", type=float, default=0.2)
+    ap.add_argument("--workload", default="gateup", choices=WORKLOADS,
+                    help="gateup (default): fused RMSNorm + gate/up, K=1024, N=2x3072, M=1 and 8; proj: "
+                         "K=1024, N=3072, M=1; wide: K=12800, N=2560, M=1 and 8; step: 28-layer decoder weight "
+                         "stream, M=1 and 8; moe4 / moe8: MoE layer, M=8")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
