@@ -366,8 +366,9 @@ class Step(Workload):
     16 q / 8 kv heads of 128, tied readout 151,936), one M=1 and one M=8 step per bench step."""
 
     name = "step"
-    kernel_key = "chain_b4_l28_d1024"
-    kernel = "chain_kernel<4> (whole step, one launch)"
+    kernel_key = "step_b4_l28_d1024"
+    kernel = "qproj kernels, 4 per layer + readout, chained with programmatic dependent launch"
+    launches_per_call = 4 * 28 + 1
 
     def __init__(self, T, torch, l2_bytes):
         super().__init__(T, torch)

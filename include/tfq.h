@@ -255,7 +255,10 @@ typedef struct tf_decoder_desc {
  *   h1  = h + qkv[:, :q_dim] . Wo^T                  (q stands in for the attention output)
  *   a   = silu(rmsnorm(h1, mlp_norm) . Wg^T) * (rmsnorm(h1, mlp_norm) . Wu^T)
  *   h   = h1 + a . Wd^T
- * then logits = rmsnorm(h, final_norm) . Wreadout^T.
+ * then logits = rmsnorm(h, final_norm) . Wreadout^T. Each projection is one kernel,
+ * chained on `stream` with programmatic dependent launch (every kernel streams its
+ * weights while the previous one finishes); tf_tune_set(TF_TUNE_CHAIN, 2) runs the
+ * whole step as one persistent cooperative kernel instead.
  *   x        bf16 [M][d_model], the residual stream entering layer 0
  *   logits   bf16 [M][vocab]
  *   debug    NULL, or bf16 scratch of tf_decode_step_debug_elems(d, M) elements
@@ -296,8 +299,9 @@ int tf_selftest_wait_timeout(void* ws, uint64_t limit_ns, void* stream);
 #define TF_TUNE_WARPS 4       /* warp mode: consumer warps per CTA (1..16) */
 #define TF_TUNE_MODE 5        /* 1: lock-step teams, 2: warp workers, 3: light teams (one item per CTA),
                                  4: light teams with bulk-copied (not register-loaded) activations */
-#define TF_TUNE_CHAIN 6       /* tf_decode_step_run: 1 = one kernel per projection instead of the
-                                 single persistent kernel for the whole step */
+#define TF_TUNE_CHAIN 6       /* tf_decode_step_run: 2 = the whole step as one persistent kernel
+                                 (TF_E_UNSUPPORTED_SHAPE where it cannot run); otherwise one kernel
+                                 per projection, chained with programmatic dependent launch */
 int tf_tune_set(int key, int value);
 
 #ifdef __cplusplus

@@ -819,9 +819,11 @@ int tf_decode_step_run(const tf_decoder_desc* d, const uint16_t* x, int64_t M, u
 
     const size_t per_layer = (size_t)M * (QKV + D + F + D);
 
-    // ---- the whole step as one persistent kernel, when the shapes allow it
+    // ---- the whole step as one persistent kernel, on request (TF_TUNE_CHAIN = 2): on GB300
+    // its grid-wide stage barriers cost more than the kernel boundaries of the chain of
+    // projections with programmatic dependent launch, which is therefore the default
     int bits = d->readout.bits;
-    bool chain = g_tune[TF_TUNE_CHAIN] != 1 && d->n_layers <= kChainMaxLayers && D <= 1024 &&
+    bool chain = g_tune[TF_TUNE_CHAIN] == 2 && d->n_layers <= kChainMaxLayers && D <= 1024 &&
                  std::max<int64_t>(D, std::max<int64_t>(Q, F)) <= (int64_t)kChainMaxGroups * kGroup &&
                  d->vocab <= INT32_MAX;
     for (int l = 0; chain && l < d->n_layers; ++l) {
@@ -836,6 +838,9 @@ int tf_decode_step_run(const tf_decoder_desc* d, const uint16_t* x, int64_t M, u
                                       &cp.xsum_off, &cp.red_off, &cp.xraw_off, &cp.ring_off);
         chain = cp.nst >= 2 && chain_fits(bits, chain_smem_bytes);
     }
+    if (!chain && g_tune[TF_TUNE_CHAIN] == 2)
+        return fail(TF_E_UNSUPPORTED_SHAPE, "tf_decode_step_run: the single-kernel step cannot run for these shapes "
+                                            "on this device (and it was required)");
     if (chain) {
         cp.L = d->n_layers;
         cp.M = (int)M;

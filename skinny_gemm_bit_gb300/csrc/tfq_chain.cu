@@ -15,7 +15,8 @@
 // the previous stage (a per-stage arrival counter in global memory), load the
 // stage's activation rows from L2 straight into B-fragment order (normalising
 // them when the stage folds an RMSNorm in), run the rounds of the stage (R blocks
-// side by side, 8 / R warps on each, one slot per step), sum each block's warps,
+// side by side, the consumer warps split evenly over them, one slot per step),
+// sum each block's warps,
 // apply the epilogue and store, then arrive on the stage's counter.
 //
 // Every wait is bounded; a wait that gives up records TF_E_TIMEOUT in the status
@@ -28,7 +29,9 @@
 namespace tfq {
 namespace {
 
-constexpr int kChainWarps = 16;
+constexpr int kChainWarps = 12;
+constexpr int kChainMaxR = 4;  // blocks side by side in a round; divides kChainWarps
+static_assert(kChainWarps % kChainMaxR == 0, "every round's blocks get the same number of warps");
 constexpr int kChainThreads = (kChainWarps + 1) * 32;
 constexpr int kChainBarAll = 15;  // named barrier of the consumer warps; 1, 2 are team barriers
 
@@ -112,11 +115,10 @@ __device__ __forceinline__ StageDesc stage_desc(const ChainParams& p, int s)
     }
     d.n_rb = (d.N + kRowsPerBlock - 1) / kRowsPerBlock;
     d.groups = d.K / kGroup;
-    // up to 8 blocks side by side (as many as a CTA has, a power of two): with many
-    // blocks per CTA each warp owns whole blocks and no warp sums are needed
+    // up to kChainMaxR blocks side by side (as many as a CTA has, a power of two)
     const int per_cta = (d.n_rb + p.C - 1) / p.C;
     d.R = 1;
-    while (2 * d.R <= per_cta && 2 * d.R <= 8)
+    while (2 * d.R <= per_cta && 2 * d.R <= kChainMaxR)
         d.R *= 2;
     d.cg = kChainSlotTiles / (d.mats * d.R);
     return d;
@@ -202,9 +204,9 @@ __device__ __forceinline__ void store_block(const StageDesc& d, int rb, int lane
     }
 }
 
-// 17 warps x 32 threads x 120 registers fit one SM's register file
+// 13 warps: at most 4 per SM sub-partition, whose 16K registers hold 4 x 32 x 128
 template <int BITS>
-__global__ void __maxnreg__(120) chain_kernel(const __grid_constant__ ChainParams p)
+__global__ void __maxnreg__(128) chain_kernel(const __grid_constant__ ChainParams p)
 {
     constexpr int TILE = tile_bytes_for(BITS);
     constexpr int SLOT = kChainSlotTiles * TILE;

@@ -121,10 +121,11 @@ def _check_decoder(T, cfg, M, readout_rows=None):
 @pytest.mark.parametrize("per_projection", [False, True])
 @pytest.mark.parametrize("M", [1, 3, 8])
 def test_decoder_small(T, M, per_projection):
-    # default: the whole step in one persistent kernel; per_projection: one kernel per projection
+    # the whole step in one persistent kernel (required, so no silent fallback), or one
+    # kernel per projection
     cfg = synth.decoder(seed=30 + M, n_layers=3, d_model=256, d_ff=384, n_q_heads=4, n_kv_heads=2, head_dim=64,
                         vocab=1000, M=M)
-    T.tune_set(T.TF_TUNE_CHAIN, 1 if per_projection else -1)
+    T.tune_set(T.TF_TUNE_CHAIN, 1 if per_projection else 2)
     try:
         _check_decoder(T, cfg, M)
     finally:
@@ -145,8 +146,13 @@ def test_decoder_step_leaves_workspace_clean_and_repeats_exactly(T):
 
 @pytest.mark.parametrize("M", [1, 8])
 def test_decoder_full_size(T, M):
-    # 28 layers, model_dim 1024, hidden 3072, 16 q / 8 kv heads of 128, tied readout 151,936 x 1024
+    # 28 layers, model_dim 1024, hidden 3072, 16 q / 8 kv heads of 128, tied readout 151,936 x 1024,
+    # through the single-kernel step (required)
     cfg = synth.decoder(M=M)
     rows = np.sort(np.random.default_rng(9).choice(151936, size=512, replace=False))
     rows = np.concatenate([rows, [0, 151935]])
-    _check_decoder(T, cfg, M, readout_rows=np.unique(rows))
+    T.tune_set(T.TF_TUNE_CHAIN, 2)
+    try:
+        _check_decoder(T, cfg, M, readout_rows=np.unique(rows))
+    finally:
+        T.tune_set(T.TF_TUNE_CHAIN, -1)
