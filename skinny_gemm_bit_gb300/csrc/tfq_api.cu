@@ -147,9 +147,10 @@ Plan plan_qproj(int n_rb, int groups, int mats, int bits, int slots, int k_full,
     Plan pl{};
     pl.slots = slots;
 
-    // K splits: the split's activation slice (8 rows) must stay within 64 KB
+    // K splits: the split's activation slice for 8 rows must stay within 112 KB (the same
+    // split for every M, so a row gives the same bits alone or in a block of 8)
     int S = 1;
-    while (groups / S > 64 || groups % S != 0)
+    while ((int64_t)kMaxM * (groups / S) * kGroup * 2 > 112 * 1024 || groups % S != 0)
         ++S;
     if (g_tune[TF_TUNE_SPLITK] > 0 && groups % g_tune[TF_TUNE_SPLITK] == 0)
         S = g_tune[TF_TUNE_SPLITK];
@@ -184,9 +185,14 @@ Plan plan_qproj(int n_rb, int groups, int mats, int bits, int slots, int k_full,
         segs_per_cta = (double)U / C_units / pl.Gs + 1.0;
     }
 
+    // long rows (a plain problem with few, long segments per CTA and enough bytes to be
+    // bandwidth-bound): one segment at a time, all warps on it, stages of about 27 KB
+    const bool long_rows = slots == 1 && items <= 8LL * sms && (double)U * tile * mats > 8.0 * 1024 * 1024 &&
+                           pl.Gs >= 2 * kConsumerWarps;
+
     // teams: R segments side by side, KW warps per segment, at least two tiles a warp
     int R = 1;
-    while (R < kConsumerWarps && 2 * R <= segs_per_cta)
+    while (!long_rows && R < kConsumerWarps && 2 * R <= segs_per_cta)
         R *= 2;
     while (kConsumerWarps / R > std::max(1, pl.Gs / 2))
         R *= 2;
@@ -195,8 +201,8 @@ Plan plan_qproj(int n_rb, int groups, int mats, int bits, int slots, int k_full,
     pl.R = R;
     pl.KW = kConsumerWarps / R;
 
-    // stages of about 16 KB, a multiple of KW groups per segment
-    int cg = std::max(1, 16384 / (mats * pl.R * tile));
+    // stages of about 16 KB (27 KB for long rows), a multiple of KW groups per segment
+    int cg = std::max(1, (long_rows ? 27648 : 16384) / (mats * pl.R * tile));
     cg = (cg + pl.KW - 1) / pl.KW * pl.KW;
     if (g_tune[TF_TUNE_STAGE_GROUPS] > 0)
         cg = g_tune[TF_TUNE_STAGE_GROUPS];
@@ -266,9 +272,20 @@ Plan plan_qproj(int n_rb, int groups, int mats, int bits, int slots, int k_full,
     const int nw = g_tune[TF_TUNE_WARPS] > 0 ? std::min(g_tune[TF_TUNE_WARPS], kConsumerWarps) : kConsumerWarps;
     const int64_t W = (int64_t)sms * nw;
     const int64_t upc_max_all = (U + pl.C - 1) / pl.C;  // units per CTA with every slot active
-    bool warp_mode = U >= 4 * W && upc_max_all <= per_ps;
+    bool warp_mode = !long_rows && U >= 4 * W && upc_max_all <= per_ps;
     if (g_tune[TF_TUNE_MODE] > 0)
         warp_mode = g_tune[TF_TUNE_MODE] == 2 && upc_max_all <= per_ps;
+    if (warp_mode) {
+        // the activation buffers (two unless a single problem and split, or an RMSNorm)
+        // and two ring slots per worker must fit, else lock-step teams
+        const bool norm_rows = k_full > 0;
+        const int bufs = (!norm_rows && (int64_t)slots * S > 1) ? 2 : 1;
+        const int xcols = norm_rows ? k_full : pl.Gs * kGroup;
+        const int Tw = std::max(1, (mats == 2 ? 2304 : 4608) / tile);
+        const size_t need = 16384 + (size_t)bufs * rows * (xcols * 2 + 16) +
+                            (size_t)2 * nw * mats * std::min(Tw, pl.Gs) * tile;
+        warp_mode = need <= 227 * 1024;
+    }
     if (warp_mode) {
         pl.mode = 1;
         pl.nw = nw;
@@ -456,13 +473,24 @@ int tf_qweight_check(const tf_qweight* w, void* stream)
 
 // ------------------------------------------------------------------ projections
 
+// Split-K scratch of the plans for every activation row count up to 8 (the split count
+// depends on how many rows are staged), so one workspace serves any M.
+static size_t qlinear_scratch_all_m(const tf_qweight* w, const tf_qweight* w_up)
+{
+    size_t r = 0;
+    for (int rows = 1; rows <= kMaxM; ++rows) {
+        const Plan pl = plan_qproj((int)(w->n_pad / 16), (int)(w->K / kGroup), w_up ? 2 : 1, w->bits, 1, 0, rows);
+        r = std::max(r, plan_scratch(pl));
+    }
+    return r;
+}
+
 size_t tf_qlinear_workspace_bytes(const tf_qweight* w, int64_t M)
 {
     (void)M;
     if (check_desc(w, "tf_qlinear_workspace_bytes"))
         return 0;
-    const Plan pl = plan_qproj((int)(w->n_pad / 16), (int)(w->K / kGroup), 1, w->bits, 1, 0, kMaxM);
-    return kStatusBytes + plan_scratch(pl);
+    return kStatusBytes + qlinear_scratch_all_m(w, nullptr);
 }
 
 // `ws` holds the status word; `scratch` (scratch_bytes) the split-K counters and partials.
@@ -475,7 +503,9 @@ static int qlinear_impl(const tf_qweight* w, const tf_qweight* w_up, const uint1
     const Plan pl = plan_qproj((int)(w->n_pad / 16), (int)(w->K / kGroup), dual ? 2 : 1, w->bits, 1,
                                gamma != nullptr ? (int)w->K : 0, (int)M);
     if (pl.smem > 227 * 1024)
-        return fail(TF_E_UNSUPPORTED_SHAPE, "%s: K too large for the RMSNorm prologue (rows do not fit on chip)",
+        return fail(TF_E_UNSUPPORTED_SHAPE,
+                    gamma != nullptr ? "%s: K too large for the RMSNorm prologue (rows do not fit on chip)"
+                                     : "%s: the activation rows of a K split do not fit on chip",
                     name);
     if (scratch_bytes < plan_scratch(pl))
         return fail(TF_E_WORKSPACE_TOO_SMALL, "%s: workspace too small for the launch plan", name);
@@ -535,8 +565,7 @@ size_t tf_qmlp_gateup_workspace_bytes(const tf_qweight* gate, const tf_qweight* 
     (void)M;
     if (check_desc(gate, "gate") || check_desc(up, "up"))
         return 0;
-    const Plan pl = plan_qproj((int)(gate->n_pad / 16), (int)(gate->K / kGroup), 2, gate->bits, 1, 0, kMaxM);
-    return kStatusBytes + plan_scratch(pl);
+    return kStatusBytes + qlinear_scratch_all_m(gate, up);
 }
 
 int tf_qmlp_gateup_run(const tf_qweight* gate, const tf_qweight* up, const uint16_t* x, int64_t ldx, int64_t M,
@@ -758,9 +787,11 @@ StepLayout step_layout(const tf_decoder_desc* d, int64_t M)
     // qkv | h1 | a | h ping | h pong
     const size_t act_bytes = (L.qkv_e + L.h_e + L.a_e + 2 * L.h_e) * sizeof(uint16_t) + 5 * 256;
     L.red = align_up(L.act + act_bytes, 256);
-    size_t r = plan_scratch(L.p_ro);
+    size_t r = qlinear_scratch_all_m(&d->readout, nullptr);
     if (d->n_layers > 0) {
-        const size_t c[4] = {plan_scratch(L.p_qkv), plan_scratch(L.p_o), plan_scratch(L.p_gu), plan_scratch(L.p_dn)};
+        const tf_decoder_layer& l0 = d->layers[0];
+        const size_t c[4] = {qlinear_scratch_all_m(&l0.qkv, nullptr), qlinear_scratch_all_m(&l0.o, nullptr),
+                             qlinear_scratch_all_m(&l0.gate, &l0.up), qlinear_scratch_all_m(&l0.down, nullptr)};
         for (size_t v : c)
             r = v > r ? v : r;
     }

@@ -746,6 +746,7 @@ __global__ void __launch_bounds__((NWT + 1) * 32, NWT == 8 ? 2 : 1) qproj_kernel
         }
         const int xoff = norm ? first.y * p.Gs : 0;  // first group of the split inside the staged rows
         float acc0[4] = {0.f, 0.f, 0.f, 0.f}, acc1[4] = {0.f, 0.f, 0.f, 0.f};
+        float bcc0[4] = {0.f, 0.f, 0.f, 0.f}, bcc1[4] = {0.f, 0.f, 0.f, 0.f};  // second chain
         for (int g = 0; g < maxlen; g += p.cg, ++st_global) {
             const int s = st_global % p.nst;
             const uint32_t ph = (st_global / p.nst) & 1u;
@@ -753,20 +754,44 @@ __global__ void __launch_bounds__((NWT + 1) * 32, NWT == 8 ? 2 : 1) qproj_kernel
             alive = __all_sync(0xffffffffu, ok);
             const int cnt = alive ? min(p.cg, len - g) : 0;
             const uint8_t* sbase = stages + s * stage_bytes;
-            for (int j = kp; j < cnt; j += KW) {
+            const uint8_t* t0 = sbase + (r_me * p.cg) * TILE;
+            const uint8_t* t1 = sbase + ((R + r_me) * p.cg) * TILE;
+            int j = kp;
+            // a single matrix takes two tiles per iteration into separate accumulators (gate
+            // and up are two independent chains already)
+            for (; !DUAL && j + KW < cnt; j += 2 * KW) {
                 const int gl = gs + g + j;  // group within the split
+                uint4 xa, xb, ya, yb;
+                x_frag(xraw, p.x_rs, gi, tq, xoff + gl, Mrows, xa, xb);
+                x_frag(xraw, p.x_rs, gi, tq, xoff + gl + KW, Mrows, ya, yb);
+                const float2 xs = *reinterpret_cast<const float2*>(xsum + gl * kMaxM + 2 * tq);
+                const float2 ys = *reinterpret_cast<const float2*>(xsum + (gl + KW) * kMaxM + 2 * tq);
+                tile_mac<BITS>(t0 + j * TILE, lane, xa, xb, xs, acc0);
+                tile_mac<BITS>(t0 + (j + KW) * TILE, lane, ya, yb, ys, bcc0);
+                if constexpr (DUAL) {
+                    tile_mac<BITS>(t1 + j * TILE, lane, xa, xb, xs, acc1);
+                    tile_mac<BITS>(t1 + (j + KW) * TILE, lane, ya, yb, ys, bcc1);
+                }
+            }
+            for (; j < cnt; j += KW) {
+                const int gl = gs + g + j;
                 uint4 xa, xb;
                 x_frag(xraw, p.x_rs, gi, tq, xoff + gl, Mrows, xa, xb);
                 const float2 xs = *reinterpret_cast<const float2*>(xsum + gl * kMaxM + 2 * tq);
-                tile_mac<BITS>(sbase + (r_me * p.cg + j) * TILE, lane, xa, xb, xs, acc0);
+                tile_mac<BITS>(t0 + j * TILE, lane, xa, xb, xs, acc0);
                 if constexpr (DUAL)
-                    tile_mac<BITS>(sbase + ((R + r_me) * p.cg + j) * TILE, lane, xa, xb, xs, acc1);
+                    tile_mac<BITS>(t1 + j * TILE, lane, xa, xb, xs, acc1);
             }
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(&empty[s]);
         }
 
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            acc0[i] += bcc0[i];
+            acc1[i] += bcc1[i];
+        }
         // ---- sum the KW warps of the team (team barrier: ids 1..R)
         if constexpr (KW > 1) {
             named_bar_sync(1 + r_me, KW * 32);  // the previous round's reads of red are done
