@@ -269,7 +269,10 @@ Plan plan_qproj(int n_rb, int groups, int mats, int bits, int slots, int k_full,
     pl.nw = kConsumerWarps;
 
     // ---- bandwidth-bound calls: warp workers with private ring slots
-    const int nw = g_tune[TF_TUNE_WARPS] > 0 ? std::min(g_tune[TF_TUNE_WARPS], kConsumerWarps) : kConsumerWarps;
+    // MoE layers (many problems, each with its own activation rows): 8 workers a CTA
+    // measured fastest; otherwise all 16
+    const int nw_default = slots > 1 ? 8 : kConsumerWarps;
+    const int nw = g_tune[TF_TUNE_WARPS] > 0 ? std::min(g_tune[TF_TUNE_WARPS], kConsumerWarps) : nw_default;
     const int64_t W = (int64_t)sms * nw;
     const int64_t upc_max_all = (U + pl.C - 1) / pl.C;  // units per CTA with every slot active
     bool warp_mode = !long_rows && U >= 4 * W && upc_max_all <= per_ps;
@@ -281,7 +284,7 @@ Plan plan_qproj(int n_rb, int groups, int mats, int bits, int slots, int k_full,
         const bool norm_rows = k_full > 0;
         const int bufs = (!norm_rows && (int64_t)slots * S > 1) ? 2 : 1;
         const int xcols = norm_rows ? k_full : pl.Gs * kGroup;
-        const int Tw = std::max(1, (mats == 2 ? 2304 : 4608) / tile);
+        const int Tw = std::max(1, (mats == 2 && slots == 1 ? 2304 : 4608) / tile);
         const size_t need = 16384 + (size_t)bufs * rows * (xcols * 2 + 16) +
                             (size_t)2 * nw * mats * std::min(Tw, pl.Gs) * tile;
         warp_mode = need <= 227 * 1024;
@@ -304,9 +307,10 @@ Plan plan_qproj(int n_rb, int groups, int mats, int bits, int slots, int k_full,
             pl.kmax = upw_min >= 1 ? (int)std::min<int64_t>(pl.Gs, (pl.Gs - 1) / upw_min + 2) : pl.Gs;
             pl.pw = (int)(upw_max / pl.Gs + 4);
         }
-        // chunks of ~4.5 KB per matrix (one bulk copy each), two or more slots per worker
+        // chunks of ~4.5 KB per matrix (~2.3 KB for gate + up of one problem; one bulk copy
+        // each), two or more slots per worker
         int T = std::max(1, 4608 / tile);
-        if (mats == 2)
+        if (mats == 2 && slots == 1)
             T = std::max(1, T / 2);
         if (g_tune[TF_TUNE_STAGE_GROUPS] > 0)
             T = g_tune[TF_TUNE_STAGE_GROUPS];

@@ -3,7 +3,7 @@
 // Routing (uzu page, "Internals 1" table, mlp row: MixtureOfExperts with a
 // routing function; "radix top-k" is among its kernels): per row, the top_k
 // experts by fp32 logit, descending, equal logits to the lower index; weights
-// are the softmax of the selected logits (computed in double, stored fp32).
+// are the softmax of the selected logits (fp32 with a compensated sum).
 // The router then buckets the (row, slot) pairs by expert so that every
 // selected expert's weights are streamed once with all of its rows as MMA
 // columns, and writes the inverse map used by the deterministic combine.
@@ -13,39 +13,45 @@
 namespace tfq {
 namespace {
 
-constexpr int kRouteThreads = 1024;
+constexpr int kRouteThreads = 256;
 
+// One CTA. PER = logits per lane (E <= 32 PER), so a row's logits sit in registers.
+template <int PER>
 __global__ void __launch_bounds__(kRouteThreads) moe_route_kernel(const float* __restrict__ logits, int M, int E,
                                                                   int top_k, int32_t* __restrict__ idx_out,
                                                                   float* __restrict__ w_out, MoeMeta* meta)
 {
-    __shared__ int32_t sel[kMaxM * 8];
-    __shared__ int32_t cnt[1024];
-    __shared__ int32_t warp_tot[32];
+    __shared__ int32_t sel[kMaxM * 8];  // (row, j) -> expert, -1 when unused
+    __shared__ uint8_t act[1024];       // expert selected by some row
+    __shared__ int32_t warp_tot[kRouteThreads / 32];
 
     pdl_wait();
     pdl_launch_dependents();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int i = threadIdx.x; i < 1024; i += kRouteThreads)
+        act[i] = 0;
+    if (threadIdx.x < kMaxM * 8)
+        sel[threadIdx.x] = -1;
+    __syncthreads();
 
-    // ---- top-k per row: k rounds of a warp arg-max over the not-yet-taken experts
-    if (warp < M) {
-        const float* l = logits + (int64_t)warp * E;
-        uint32_t taken = 0;  // bit i: expert lane + 32 i taken (E <= 1024)
-        float vals[32];
-        const int per = (E + 31) / 32;
-        for (int i = 0; i < per; ++i) {
+    // ---- top-k per row (warp m): k rounds of a warp arg-max over the experts not yet taken
+    for (int m = warp; m < M; m += kRouteThreads / 32) {
+        const float* l = logits + (int64_t)m * E;
+        float vals[PER];
+#pragma unroll
+        for (int i = 0; i < PER; ++i) {
             const int e = lane + 32 * i;
             vals[i] = e < E ? __ldcg(l + e) : 0.f;
         }
+        uint32_t taken = 0;  // bit i: expert lane + 32 i taken
         float top = 0.f, mine = 0.f;  // the largest selected logit; lane j: the j-th one
         for (int j = 0; j < top_k; ++j) {
             float bv = 0.f;
             int be = -1;
-            for (int i = 0; i < per; ++i) {
+#pragma unroll
+            for (int i = 0; i < PER; ++i) {
                 const int e = lane + 32 * i;
-                if (e >= E || ((taken >> i) & 1u))
-                    continue;
-                if (be < 0 || vals[i] > bv) {  // ascending e: strict '>' keeps the lower index
+                if (e < E && !((taken >> i) & 1u) && (be < 0 || vals[i] > bv)) {  // ascending e keeps the lower
                     bv = vals[i];
                     be = e;
                 }
@@ -64,8 +70,10 @@ __global__ void __launch_bounds__(kRouteThreads) moe_route_kernel(const float* _
                 top = bv;
             if (lane == j)
                 mine = bv;
-            if (lane == 0)
-                sel[warp * 8 + j] = be;
+            if (lane == 0) {
+                sel[m * 8 + j] = be;
+                act[be] = 1;
+            }
         }
         // softmax over the selected logits: lane j takes exp(l_j - l_0) <= 1 (the k
         // exponentials run side by side; 2 ulp each), every lane adds them in ascending j
@@ -84,50 +92,51 @@ __global__ void __launch_bounds__(kRouteThreads) moe_route_kernel(const float* _
         if (lane < top_k) {
             const float q = ex / s_hi;
             const float w = fmaf(-q, s_lo / s_hi, q);
-            idx_out[warp * top_k + lane] = sel[warp * 8 + lane];
-            w_out[warp * top_k + lane] = w;
-            meta->w[warp * 8 + lane] = w;
+            idx_out[m * top_k + lane] = sel[m * 8 + lane];
+            w_out[m * top_k + lane] = w;
+            meta->w[m * 8 + lane] = w;
         }
     }
     __syncthreads();
 
-    // ---- bucket (row, slot) pairs by expert; active experts get slots in ascending expert order
-    for (int e = threadIdx.x; e < 1024; e += blockDim.x) {
-        int c = 0;
-        if (e < E)
-            for (int q = 0; q < M * 8; ++q)
-                c += ((q & 7) < top_k && (q >> 3) < M && sel[q] == e) ? 1 : 0;
-        cnt[e] = c;
+    // ---- active experts get slots in ascending expert order: thread t owns experts
+    // 4t .. 4t + 3; exclusive prefix of their counts over the CTA
+    const int e0 = threadIdx.x * 4;
+    int cnt = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        cnt += act[e0 + i];
+    int incl = cnt;
+    for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o)
+            incl += v;
     }
+    if (lane == 31)
+        warp_tot[warp] = incl;
     __syncthreads();
-    // exclusive prefix count of active experts: one ballot per warp of 32 experts
-    const int e = threadIdx.x;  // blockDim == 1024 covers every expert index
-    const bool act = cnt[e] > 0;
-    const uint32_t bal = __ballot_sync(0xffffffffu, act);
-    if (lane == 0)
-        warp_tot[warp] = __popc(bal);
-    __syncthreads();
-    int before = __popc(bal & ((1u << lane) - 1u));
+    int before = incl - cnt;
     for (int w = 0; w < warp; ++w)
         before += warp_tot[w];
-    if (threadIdx.x == 1023) {
-        int tot = 0;
-        for (int w = 0; w < 32; ++w)
-            tot += warp_tot[w];
-        meta->n_active = tot;
-    }
-    if (act) {
-        MoeSlot& s = meta->slot[before];
+    if (threadIdx.x == kRouteThreads - 1)
+        meta->n_active = before + cnt;
+    // ---- each active expert's rows, in ascending (row, slot j) order
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int e = e0 + i;
+        if (!act[e])
+            continue;
+        const int slot = before++;
+        MoeSlot& s = meta->slot[slot];
         s.expert = e;
         int c = 0;
-        for (int m = 0; m < M; ++m)
-            for (int j = 0; j < top_k; ++j)
-                if (sel[m * 8 + j] == e) {
-                    s.rows[c] = m;
-                    s.js[c] = j;
-                    meta->inv[m * 8 + j] = before * 8 + c;
-                    ++c;
-                }
+        for (int q = 0; q < M * 8; ++q)
+            if (sel[q] == e) {
+                s.rows[c] = q >> 3;
+                s.js[c] = q & 7;
+                meta->inv[q] = slot * 8 + c;
+                ++c;
+            }
         for (int c2 = c; c2 < kMaxM; ++c2) {
             s.rows[c2] = 0;
             s.js[c2] = 0;
@@ -191,7 +200,13 @@ cudaError_t launch_moe_route(const float* logits, int M, int E, int top_k, int32
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, moe_route_kernel, logits, M, E, top_k, idx, w, meta);
+    if (E <= 32)
+        return cudaLaunchKernelEx(&cfg, moe_route_kernel<1>, logits, M, E, top_k, idx, w, meta);
+    if (E <= 128)
+        return cudaLaunchKernelEx(&cfg, moe_route_kernel<4>, logits, M, E, top_k, idx, w, meta);
+    if (E <= 256)
+        return cudaLaunchKernelEx(&cfg, moe_route_kernel<8>, logits, M, E, top_k, idx, w, meta);
+    return cudaLaunchKernelEx(&cfg, moe_route_kernel<32>, logits, M, E, top_k, idx, w, meta);
 }
 
 cudaError_t launch_moe_combine(const MoeMeta* meta, const float* o, int M, int top_k, int H, uint16_t* y,
