@@ -363,7 +363,8 @@ __global__ void __maxnreg__(128) chain_kernel(const __grid_constant__ ChainParam
             // sum the KW warps of the block (team barrier 1 + r_me)
             if (KW > 1) {
                 float4* red4 = reinterpret_cast<float4*>(red);
-                named_bar_sync(1 + r_me, KW * 32);  // the previous round's reads are done
+                if (t > 0)
+                    named_bar_sync(1 + r_me, KW * 32);  // the previous round's reads are done
                 red4[cw * 32 + lane] = make_float4(acc0[0], acc0[1], acc0[2], acc0[3]);
                 red4[kChainWarps * 32 + cw * 32 + lane] = make_float4(acc1[0], acc1[1], acc1[2], acc1[3]);
                 named_bar_sync(1 + r_me, KW * 32);

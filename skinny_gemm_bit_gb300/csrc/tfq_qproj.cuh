@@ -269,8 +269,9 @@ __device__ __forceinline__ void x_direct_raw(const uint16_t* x, int64_t ldx, int
             xs[i] = 0.f;
     if (gamma != nullptr) {
         // WPR warps per row (the largest power of two with WPR * Mrows <= nwarps), each
-        // on a run of cpw chunks (a multiple of 8, at most 4 per lane since K <= 1024);
-        // the row's sum of squares is the WPR warp sums added in warp order
+        // normalising a run of cpw chunks (a multiple of 8; at most 4 a lane since K <=
+        // 1024). With one warp a row, the warp's own sum of squares is the row's; with
+        // several, the WPR warp sums are added in warp order after a CTA barrier.
         int WPR = 1;
         while (2 * WPR * Mrows <= nwarps)
             WPR *= 2;
@@ -299,13 +300,17 @@ __device__ __forceinline__ void x_direct_raw(const uint16_t* x, int64_t ldx, int
             }
         }
         const float wsum = warp_sum((sq[0] + sq[1]) + (sq[2] + sq[3]));
-        if (row_warp && lane == 0)
-            ss_part[cw] = wsum;
-        named_bar_sync(bar_id, nwarps * 32);
+        float ss = wsum;
+        if (WPR > 1) {  // uniform
+            if (row_warp && lane == 0)
+                ss_part[cw] = wsum;
+            named_bar_sync(bar_id, nwarps * 32);
+            ss = 0.f;
+            if (row_warp)
+                for (int w = 0; w < WPR; ++w)
+                    ss += ss_part[m * WPR + w];
+        }
         if (row_warp) {
-            float ss = 0.f;
-            for (int w = 0; w < WPR; ++w)
-                ss += ss_part[m * WPR + w];
             const float inv = rsqrtf(ss / (float)K + eps);
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
@@ -794,7 +799,8 @@ __global__ void __launch_bounds__((NWT + 1) * 32, NWT == 8 ? 2 : 1) qproj_kernel
         }
         // ---- sum the KW warps of the team (team barrier: ids 1..R)
         if constexpr (KW > 1) {
-            named_bar_sync(1 + r_me, KW * 32);  // the previous round's reads of red are done
+            if (t > 0)
+                named_bar_sync(1 + r_me, KW * 32);  // the previous round's reads of red are done
             // one float4 per lane and matrix, the lanes of a warp side by side (no bank conflicts)
             float4* red4 = reinterpret_cast<float4*>(red);
             red4[cw * 32 + lane] = make_float4(acc0[0], acc0[1], acc0[2], acc0[3]);
