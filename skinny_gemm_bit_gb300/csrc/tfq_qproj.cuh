@@ -1130,11 +1130,23 @@ __global__ void __launch_bounds__(kThreads, 1) qproj_warp_kernel(const __grid_co
                         break;
                     }
                     const uint8_t* sb = ring + s * slot_bytes;
-                    for (int j = 0; j < cnt; ++j) {
+                    const int xs0 = norm ? ss * p.Gs + gl + g : gl + g;  // group sums of the chunk start
+                    int j = 0;
+                    // a single matrix takes two tiles per iteration into separate accumulators
+                    // (gate and up are two independent chains already)
+                    for (; !DUAL && j + 1 < cnt; j += 2) {
+                        uint4 xa, xbv, ya, ybv;
+                        x_frag(xb, p.x_rs, gi, tq, grel0 + g + j, Mr, xa, xbv);
+                        x_frag(xb, p.x_rs, gi, tq, grel0 + g + j + 1, Mr, ya, ybv);
+                        const float2 xsv = *reinterpret_cast<const float2*>(xs + (xs0 + j) * kMaxM + 2 * tq);
+                        const float2 ysv = *reinterpret_cast<const float2*>(xs + (xs0 + j + 1) * kMaxM + 2 * tq);
+                        tile_mac<BITS>(sb + j * TILE, lane, xa, xbv, xsv, acc0);
+                        tile_mac<BITS>(sb + (j + 1) * TILE, lane, ya, ybv, ysv, acc1);
+                    }
+                    for (; j < cnt; ++j) {
                         uint4 xa, xbv;
                         x_frag(xb, p.x_rs, gi, tq, grel0 + g + j, Mr, xa, xbv);
-                        const float2 xsv = *reinterpret_cast<const float2*>(
-                            xs + (norm ? ss * p.Gs + gl + g + j : gl + g + j) * kMaxM + 2 * tq);
+                        const float2 xsv = *reinterpret_cast<const float2*>(xs + (xs0 + j) * kMaxM + 2 * tq);
                         tile_mac<BITS>(sb + j * TILE, lane, xa, xbv, xsv, acc0);
                         if constexpr (DUAL)
                             tile_mac<BITS>(sb + (T + j) * TILE, lane, xa, xbv, xsv, acc1);
@@ -1145,6 +1157,13 @@ __global__ void __launch_bounds__(kThreads, 1) qproj_warp_kernel(const __grid_co
                 }
                 if (!alive)
                     break;
+                if constexpr (!DUAL) {  // the second chain of a single matrix
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        acc0[i] += acc1[i];
+                        acc1[i] = 0.f;
+                    }
+                }
                 if (S == 1 && len == p.groups) {
                     store_outputs<DUAL, MOE>(p, pp, Mr, rb * kRowsPerBlock, lane, acc0, acc1);
                 } else if (np < p.pw) {
