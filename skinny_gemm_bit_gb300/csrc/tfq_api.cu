@@ -293,7 +293,11 @@ Plan plan_qproj(int n_rb, int groups, int mats, int bits, int slots, int k_full,
         pl.mode = 1;
         pl.nw = nw;
         const int64_t W_items = std::min<int64_t>(W, std::max<int64_t>(items, 1));
-        const int64_t W_units = std::min<int64_t>(W, std::max<int64_t>(U, 1));
+        // stream-K workers (as the kernel counts them): at least Gs / 2 units each
+        auto workers_for = [&](int64_t units) {
+            return std::min<int64_t>(W, std::max<int64_t>(units / std::max(1, pl.Gs / 2), 1));
+        };
+        const int64_t W_units = workers_for(U);
         const double per_w = (double)items / W_items;
         const double imb = (double)((items + W_items - 1) / W_items) / per_w;
         pl.aligned = imb <= 1.10 ? 1 : 0;
@@ -302,8 +306,8 @@ Plan plan_qproj(int n_rb, int groups, int mats, int bits, int slots, int k_full,
             pl.kmax = 1;
             pl.pw = S > 1 ? (int)((items + W_items - 1) / W_items) + 1 : 1;
         } else {
-            const int64_t upw_min = U_min / std::min<int64_t>(W, U_min);
-            const int64_t upw_max = (U + W_units - 1) / W_units;
+            const int64_t upw_min = U_min / workers_for(U_min);
+            const int64_t upw_max = std::max<int64_t>((U + W_units - 1) / W_units, pl.Gs);
             pl.kmax = upw_min >= 1 ? (int)std::min<int64_t>(pl.Gs, (pl.Gs - 1) / upw_min + 2) : pl.Gs;
             pl.pw = (int)(upw_max / pl.Gs + 4);
         }

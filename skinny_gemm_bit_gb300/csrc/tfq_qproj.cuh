@@ -985,7 +985,10 @@ __global__ void __launch_bounds__(kThreads, 1) qproj_warp_kernel(const __grid_co
     pt.items = (int64_t)P * p.S * p.n_rb;
     pt.U = pt.items * p.Gs;
     pt.inv_U = 1.f / (float)max(pt.U, (int64_t)1);
-    const int W = (int)min((int64_t)p.C * NW, max(pt.aligned ? pt.items : pt.U, (int64_t)1));
+    // stream-K workers take at least half a row block's units each (fewer workers for
+    // small problems), which bounds the contributors of a row block
+    const int64_t wcap = pt.aligned ? pt.items : pt.U / max(1, p.Gs / 2);
+    const int W = (int)min((int64_t)p.C * NW, max(wcap, (int64_t)1));
     pt.C = W;  // the partition is over workers
     auto wrange = [&](int v, int64_t& a, int64_t& b) {
         if (v < W) {
