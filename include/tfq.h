@@ -296,9 +296,10 @@ int tf_selftest_wait_timeout(void* ws, uint64_t limit_ns, void* stream);
 #define TF_TUNE_SPLITK 1      /* K splits (must divide K / 64) */
 #define TF_TUNE_STAGE_GROUPS 2 /* 64-column groups per pipeline stage */
 #define TF_TUNE_STAGES 3      /* pipeline depth (ring slots per worker in warp mode) */
-#define TF_TUNE_WARPS 4       /* warp mode: consumer warps per CTA (1..16) */
+#define TF_TUNE_WARPS 4       /* warp mode: consumer warps per CTA (1..16); streaming: 8 or 16 */
 #define TF_TUNE_MODE 5        /* 1: lock-step teams, 2: warp workers, 3: light teams (one item per CTA),
-                                 4: light teams with bulk-copied (not register-loaded) activations */
+                                 4: light teams with bulk-copied (not register-loaded) activations,
+                                 5: streaming CTAs (one matrix; RMSNorm only for K <= 1024) */
 #define TF_TUNE_CHAIN 6       /* tf_decode_step_run: 2 = the whole step as one persistent kernel
                                  (TF_E_UNSUPPORTED_SHAPE where it cannot run); otherwise one kernel
                                  per projection, chained with programmatic dependent launch */

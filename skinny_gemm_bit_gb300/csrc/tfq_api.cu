@@ -132,6 +132,69 @@ int device_sms()
     return g_sms_cache[dev];
 }
 
+// Streaming plan (tfq_stream.cuh) for one matrix of one problem: false when the call
+// does not suit it (an RMSNorm over K > 1024, or more K splits than SMs).
+bool plan_stream(int n_rb, int groups, int bits, int k_full, int sms, Plan& pl)
+{
+    const int tile = tile_bytes_for(bits);
+    if (k_full > 1024)  // the normalised rows are staged by warps holding at most 4 chunks a lane
+        return false;
+    // 8 compute warps and at most 110 KB: the next kernel's CTA fits beside this one's,
+    // so its weight copies start while this kernel finishes; 16 warps take a whole SM
+    const int W = g_tune[TF_TUNE_WARPS] == 16 ? 16 : 8;
+    const size_t budget = W == 8 ? 110 * 1024 : 227 * 1024;
+    // K splits: 8 rows of a split's slice within 28 KB (the same split for every M)
+    int S = 1;
+    if (k_full == 0) {
+        while (S < groups && (groups % S != 0 || (int64_t)kMaxM * ((groups / S) * kGroup * 2 + 16) > 28 * 1024))
+            ++S;
+        if (g_tune[TF_TUNE_SPLITK] > 0 && groups % g_tune[TF_TUNE_SPLITK] == 0)
+            S = g_tune[TF_TUNE_SPLITK];
+    }
+    if (S > sms)
+        return false;
+    const int Gs = groups / S;
+    pl = Plan{};
+    pl.mode = 2;
+    pl.slots = 1;
+    pl.S = S;
+    pl.Gs = Gs;
+    pl.nw = W;
+    pl.KW = 1;
+    pl.R = 1;
+    const int64_t Us = (int64_t)n_rb * Gs;
+    // S groups of C / S CTAs, one split each, every CTA with at least one unit
+    pl.C = S * (int)std::min<int64_t>(sms / S, Us);
+    const int64_t upc_min = Us / (pl.C / S);
+    pl.kmax = upc_min >= 1 ? (int)std::min<int64_t>(Gs, (Gs - 1) / upc_min + 2) : Gs;
+    pl.aligned = 0;
+    // chunks of 32 tiles (a multiple of 2 W: a warp's two tiles share a chunk)
+    int CH = g_tune[TF_TUNE_STAGE_GROUPS] > 0 ? g_tune[TF_TUNE_STAGE_GROUPS] : 32;
+    CH = std::max(2 * W, (CH + 2 * W - 1) / (2 * W) * (2 * W));
+    pl.cg = CH;
+    pl.pw = 4;  // hand-off slots of the reducer
+    const int xg = k_full > 0 ? groups : Gs;  // groups staged
+    pl.xraw_off = (int)align_up(384 + (size_t)xg * kMaxM * 4, 128);
+    pl.x_rs = xg * kGroup * 2 + 16;
+    pl.red_off = (int)align_up(pl.xraw_off + (size_t)kMaxM * pl.x_rs, 128);  // all 8 rows (zero past M)
+    const int64_t upc_max = (Us + pl.C / S - 1) / (pl.C / S);
+    pl.segmax = (int)(upc_max / Gs + 2);  // row blocks a CTA touches
+    pl.last_off = (int)align_up(pl.red_off + (size_t)pl.pw * W * 32 * 16, 128);
+    pl.stage_off = (int)align_up(pl.last_off + (size_t)pl.segmax * 4, 128);
+    const size_t slot = (size_t)CH * tile;
+    int NS = pl.stage_off + 2 * slot <= budget ? (int)((budget - pl.stage_off) / slot) : 0;
+    NS = std::min(NS, 8);
+    if (g_tune[TF_TUNE_STAGES] > 0)
+        NS = std::min(NS, g_tune[TF_TUNE_STAGES]);
+    if (NS < 2)
+        return false;
+    pl.nst = NS;
+    pl.smem = pl.stage_off + (size_t)NS * slot;
+    pl.ws_counters = align_up((size_t)n_rb * sizeof(int), 256);
+    pl.ws_partials = align_up((size_t)S * n_rb * pl.kmax * 32 * 4 * sizeof(float), 256);
+    return true;
+}
+
 // Plan of one projection launch (persistent grid, at most one CTA per SM).
 //   n_rb, groups  16-row blocks and 64-column groups of one matrix
 //   mats          2 for gate + up, else 1
@@ -265,6 +328,14 @@ Plan plan_qproj(int n_rb, int groups, int mats, int bits, int slots, int k_full,
         // row must fit four 8-column chunks per lane (K <= 1024)
         pl.x_direct = slots == 1 && (k_full == 0 || k_full <= 1024) && g_tune[TF_TUNE_MODE] != 4 ? 1 : 0;
         return pl;
+    }
+    // ---- one large matrix: streaming CTAs (selected with TF_TUNE_MODE 5; on GB300 it
+    // measured no faster than the long-row teams and warp workers below: every schedule
+    // is bound by the instructions per tile, ~90-110, not by the memory system)
+    if (slots == 1 && mats == 1 && g_tune[TF_TUNE_MODE] == 5) {
+        Plan sp;
+        if (plan_stream(n_rb, groups, bits, k_full, sms, sp))
+            return sp;
     }
     pl.nw = kConsumerWarps;
 
@@ -481,15 +552,17 @@ int tf_qweight_check(const tf_qweight* w, void* stream)
 
 // ------------------------------------------------------------------ projections
 
-// Split-K scratch of the plans for every activation row count up to 8 (the split count
-// depends on how many rows are staged), so one workspace serves any M.
+// Split-K scratch of the plans for every activation row count up to 8, with and without
+// an RMSNorm prologue, so one workspace serves any call of these weights.
 static size_t qlinear_scratch_all_m(const tf_qweight* w, const tf_qweight* w_up)
 {
     size_t r = 0;
-    for (int rows = 1; rows <= kMaxM; ++rows) {
-        const Plan pl = plan_qproj((int)(w->n_pad / 16), (int)(w->K / kGroup), w_up ? 2 : 1, w->bits, 1, 0, rows);
-        r = std::max(r, plan_scratch(pl));
-    }
+    for (int rows = 1; rows <= kMaxM; ++rows)
+        for (int k_full : {0, (int)w->K}) {  // with and without an RMSNorm prologue
+            const Plan pl =
+                plan_qproj((int)(w->n_pad / 16), (int)(w->K / kGroup), w_up ? 2 : 1, w->bits, 1, k_full, rows);
+            r = std::max(r, plan_scratch(pl));
+        }
     return r;
 }
 

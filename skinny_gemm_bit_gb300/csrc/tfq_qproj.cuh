@@ -457,14 +457,13 @@ struct Part {
 
 // Sum of the fp32 partial slots of row block rb of problem prob, in (split,
 // contributor) order, zeroing every slot read (the workspace is left as it was
-// found). Loads are issued several slots at a time before any is used, so the L2
-// round trips overlap.
-template <bool DUAL>
+// found). Loads are issued B slots at a time before any is used, so the L2 round
+// trips overlap.
+template <bool DUAL, int B = 4>
 __device__ __forceinline__ void sum_partials(const QProjParams& p, const Part& pt, int prob, int rb, int lane,
                                              float (&t0)[4], float (&t1)[4])
 {
     constexpr int VALS = DUAL ? 8 : 4;
-    constexpr int B = 4;
     auto kc_of = [&](int s2) {
         return pt.aligned ? 1
                           : min(pt.contributors((int64_t)prob * pt.per_p + (int64_t)s2 * pt.per_ps + (int64_t)rb * p.Gs),

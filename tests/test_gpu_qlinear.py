@@ -324,3 +324,44 @@ def test_both_schedules_match(T, mode, M, K, N, bits, dual):
     else:
         y_ref, ad = oracle.qlinear(oracle.bf16_to_f64(x), w)
         assert_close(host_f64(y), y_ref, tol_linear(ad), f"mode {mode}")
+
+
+@pytest.mark.parametrize("warps,chunk", [(8, 32), (16, 32), (8, 16), (8, 64)])
+@pytest.mark.parametrize("M,K,N,bits,norm", [
+    (8, 12800, 2560, 4, False),  # 8 K splits of 25 groups, stream-K cuts inside row blocks
+    (1, 12800, 2560, 4, False),
+    (3, 2048, 1000, 8, False),   # ragged N, 8-bit codes
+    (8, 1024, 4100, 4, True),    # RMSNorm over whole staged rows, ragged last row block
+    (1, 1024, 30000, 4, True),   # many whole row blocks per CTA, stored without partials
+    (5, 640, 333, 4, False),     # fewer units than CTAs: CTAs capped at one unit each
+    (2, 64, 48, 4, True),        # one group a row block
+])
+def test_streaming_schedule_matches_oracle(T, warps, chunk, M, K, N, bits, norm):
+    # the streaming schedule forced on every shape (it is the default only above 8 MB of
+    # weights), with a residual and an fp32 output; the workspace is left all-zero
+    rng = np.random.default_rng(M * 131 + N + K + warps + chunk)
+    x = synth.activations(rng, M, K)
+    w = synth.quant_weights(rng, N, K, bits)
+    gamma_h = synth.gamma(rng, K) if norm else None
+    res_h = synth.activations(rng, M, N)
+    qw = pack(T, w)
+    T.tune_set(T.TF_TUNE_MODE, 5)
+    T.tune_set(T.TF_TUNE_WARPS, warps)
+    T.tune_set(T.TF_TUNE_STAGE_GROUPS, chunk)
+    try:
+        ws = T.workspace(T.tf_qlinear_workspace_bytes(qw, 8))  # sized for the tuned plan
+        y = T.tf_qlinear_run(qw, dev_bf16(x), gamma=dev_bf16(gamma_h) if norm else None, eps=1e-6,
+                             residual=dev_bf16(res_h), ws=ws, out_dtype=torch.float32)
+        torch.cuda.synchronize()
+    finally:
+        for key in (T.TF_TUNE_MODE, T.TF_TUNE_WARPS, T.TF_TUNE_STAGE_GROUPS):
+            T.tune_set(key, -1)
+    assert T.tf_workspace_status(ws) == T.TF_OK
+    assert int(ws.count_nonzero()) == 0
+    xd = oracle.bf16_to_f64(x)
+    if norm:
+        xd = oracle.rmsnorm(xd, oracle.bf16_to_f64(gamma_h), 1e-6)
+    y_ref, ad = oracle.qlinear(xd, w)
+    y_ref = y_ref + oracle.bf16_to_f64(res_h)
+    tol = tol_linear(ad) + (2.0 ** -8 * np.abs(y_ref) if norm else 0.0)
+    assert_close(host_f64(y), y_ref, tol, f"streaming W={warps} CH={chunk}")
