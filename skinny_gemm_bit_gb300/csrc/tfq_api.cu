@@ -356,7 +356,7 @@ Plan plan_qproj(int n_rb, int groups, int mats, int bits, int slots, int k_full,
         const int bufs = (!norm_rows && (int64_t)slots * S > 1) ? 2 : 1;
         const int xcols = norm_rows ? k_full : pl.Gs * kGroup;
         const int Tw = std::max(1, (mats == 2 && slots == 1 ? 2304 : 4608) / tile);
-        const size_t need = 16384 + (size_t)bufs * rows * (xcols * 2 + 16) +
+        const size_t need = 16384 + (size_t)bufs * kMaxM * (xcols * 2 + 16) +
                             (size_t)2 * nw * mats * std::min(Tw, pl.Gs) * tile;
         warp_mode = need <= 227 * 1024;
     }
@@ -404,8 +404,9 @@ Plan plan_qproj(int n_rb, int groups, int mats, int bits, int slots, int k_full,
         pl.xraw_off = (int)align_up(pl.gamma_off + (size_t)std::max(k_full, 0) * 2, 128);
         const int xcols = norm ? k_full : pl.Gs * kGroup;
         pl.x_rs = xcols * 2 + 16;
-        pl.xraw1_off = (int)align_up(pl.xraw_off + (size_t)rows * pl.x_rs, 128);
-        pl.stage_off = (int)align_up(pl.xraw1_off + (two_bufs ? (size_t)rows * pl.x_rs : 0), 128);
+        // all 8 rows of each buffer (the rows past M are zero-filled)
+        pl.xraw1_off = (int)align_up(pl.xraw_off + (size_t)kMaxM * pl.x_rs, 128);
+        pl.stage_off = (int)align_up(pl.xraw1_off + (two_bufs ? (size_t)kMaxM * pl.x_rs : 0), 128);
         const size_t budget = 227 * 1024;
         int SW = budget > pl.stage_off + 2 * nw * slot ? (int)((budget - pl.stage_off) / (nw * slot)) : 1;
         SW = std::min(SW, kMaxStages);

@@ -140,6 +140,35 @@ __device__ __forceinline__ void tile_mac(const uint8_t* tile, int lane, const ui
     }
 }
 
+// tile_mac with one accumulation chain for 4-bit codes (the caller keeps two tiles
+// in flight, which hides the MMA latency); 8-bit codes as tile_mac.
+template <int BITS>
+__device__ __forceinline__ void tile_mac_chain(const uint8_t* tile, int lane, const uint4& xa, const uint4& xb,
+                                               const float2& xs, float (&acc)[4])
+{
+    if constexpr (BITS == 4) {
+        const uint2 sb = *reinterpret_cast<const uint2*>(tile + tile_q_bytes_for(4) + (lane >> 2) * 8);
+        const uint4 wv = *reinterpret_cast<const uint4*>(tile + lane * 16);
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
+        mma_bf16_16816(d, nib2_bf16(wv.x), nib2_bf16(wv.x >> 4), nib2_bf16(wv.x >> 8), nib2_bf16(wv.x >> 12),
+                       xa.x, xa.y);
+        mma_bf16_16816(d, nib2_bf16(wv.y), nib2_bf16(wv.y >> 4), nib2_bf16(wv.y >> 8), nib2_bf16(wv.y >> 12),
+                       xa.z, xa.w);
+        mma_bf16_16816(d, nib2_bf16(wv.z), nib2_bf16(wv.z >> 4), nib2_bf16(wv.z >> 8), nib2_bf16(wv.z >> 12),
+                       xb.x, xb.y);
+        mma_bf16_16816(d, nib2_bf16(wv.w), nib2_bf16(wv.w >> 4), nib2_bf16(wv.w >> 8), nib2_bf16(wv.w >> 12),
+                       xb.z, xb.w);
+        const float s_lo = bf16lo_f32(sb.x), s_hi = bf16hi_f32(sb.x);
+        const float c_lo = fmaf(-128.f, s_lo, bf16lo_f32(sb.y)), c_hi = fmaf(-128.f, s_hi, bf16hi_f32(sb.y));
+        acc[0] = fmaf(s_lo, d[0], fmaf(c_lo, xs.x, acc[0]));
+        acc[1] = fmaf(s_lo, d[1], fmaf(c_lo, xs.y, acc[1]));
+        acc[2] = fmaf(s_hi, d[2], fmaf(c_hi, xs.x, acc[2]));
+        acc[3] = fmaf(s_hi, d[3], fmaf(c_hi, xs.y, acc[3]));
+    } else {
+        tile_mac<BITS>(tile, lane, xa, xb, xs, acc);
+    }
+}
+
 // ---------------------------------------------------------------- activation staging
 //
 // A staged activation buffer holds rows rows[0..Mrows) of x, columns
@@ -384,6 +413,19 @@ __device__ __forceinline__ void x_frag(const uint8_t* buf, int x_rs, int gi, int
         xa = make_uint4(0u, 0u, 0u, 0u);
         xb = xa;
     }
+}
+
+// B fragments of group g_rel of a buffer whose 8 rows are all staged (rows >= M
+// zero-filled): the same two ldmatrix as x_frag, without the row clamp.
+__device__ __forceinline__ void x_frag8(const uint8_t* buf, int x_rs, int lane, int g_rel, uint4& xa, uint4& xb)
+{
+    const uint32_t a = smem_u32(buf + (lane & 7) * x_rs + g_rel * 128 + (lane >> 3) * 16);
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(xa.x), "=r"(xa.y), "=r"(xa.z), "=r"(xa.w)
+                 : "r"(a));
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(xb.x), "=r"(xb.y), "=r"(xb.z), "=r"(xb.w)
+                 : "r"(a + 64));
 }
 
 // Final values of one lane's accumulator fragment (rows row0 + gi, row0 + gi + 8;
@@ -1086,6 +1128,14 @@ __global__ void __launch_bounds__(kThreads, 1) qproj_warp_kernel(const __grid_co
     const int xg0_0 = norm ? 0 : (run0 % S) * p.Gs, xg0_1 = (run1 % S) * p.Gs;
     const int xgc = norm ? p.groups : p.Gs;
     bool alive = ca < cb && !flags[0];
+    // rows M..7 of each activation buffer read as zero (no per-tile row clamp); the
+    // bulk copies write only rows below M, and x_prepare's closing barrier orders
+    // these stores before any fragment load
+    for (int i = (cw * 32 + lane) * 16 + M0 * p.x_rs; i < kMaxM * p.x_rs; i += kConsumerWarps * 32 * 16)
+        *reinterpret_cast<uint4*>(xb0 + i) = make_uint4(0u, 0u, 0u, 0u);
+    if (two)
+        for (int i = (cw * 32 + lane) * 16 + M1 * p.x_rs; i < kMaxM * p.x_rs; i += kConsumerWarps * 32 * 16)
+            *reinterpret_cast<uint4*>(xb1 + i) = make_uint4(0u, 0u, 0u, 0u);
     if (cw == 0) {
         __syncwarp();
         if (lane == 0 && alive) {
@@ -1138,20 +1188,20 @@ __global__ void __launch_bounds__(kThreads, 1) qproj_warp_kernel(const __grid_co
                     // (gate and up are two independent chains already)
                     for (; !DUAL && j + 1 < cnt; j += 2) {
                         uint4 xa, xbv, ya, ybv;
-                        x_frag(xb, p.x_rs, gi, tq, grel0 + g + j, Mr, xa, xbv);
-                        x_frag(xb, p.x_rs, gi, tq, grel0 + g + j + 1, Mr, ya, ybv);
+                        x_frag8(xb, p.x_rs, lane, grel0 + g + j, xa, xbv);
+                        x_frag8(xb, p.x_rs, lane, grel0 + g + j + 1, ya, ybv);
                         const float2 xsv = *reinterpret_cast<const float2*>(xs + (xs0 + j) * kMaxM + 2 * tq);
                         const float2 ysv = *reinterpret_cast<const float2*>(xs + (xs0 + j + 1) * kMaxM + 2 * tq);
-                        tile_mac<BITS>(sb + j * TILE, lane, xa, xbv, xsv, acc0);
-                        tile_mac<BITS>(sb + (j + 1) * TILE, lane, ya, ybv, ysv, acc1);
+                        tile_mac_chain<BITS>(sb + j * TILE, lane, xa, xbv, xsv, acc0);
+                        tile_mac_chain<BITS>(sb + (j + 1) * TILE, lane, ya, ybv, ysv, acc1);
                     }
                     for (; j < cnt; ++j) {
                         uint4 xa, xbv;
-                        x_frag(xb, p.x_rs, gi, tq, grel0 + g + j, Mr, xa, xbv);
+                        x_frag8(xb, p.x_rs, lane, grel0 + g + j, xa, xbv);
                         const float2 xsv = *reinterpret_cast<const float2*>(xs + (xs0 + j) * kMaxM + 2 * tq);
-                        tile_mac<BITS>(sb + j * TILE, lane, xa, xbv, xsv, acc0);
+                        tile_mac_chain<BITS>(sb + j * TILE, lane, xa, xbv, xsv, acc0);
                         if constexpr (DUAL)
-                            tile_mac<BITS>(sb + (T + j) * TILE, lane, xa, xbv, xsv, acc1);
+                            tile_mac_chain<BITS>(sb + (T + j) * TILE, lane, xa, xbv, xsv, acc1);
                     }
                     __syncwarp();
                     if (lane == 0)
