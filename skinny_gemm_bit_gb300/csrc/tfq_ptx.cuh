@@ -148,6 +148,16 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint3
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// The same with fp16 inputs.
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                              uint32_t b0, uint32_t b1)
+{
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
 // (a & b) | c in one LOP3.
 __device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t b, uint32_t c)
 {
@@ -164,6 +174,12 @@ __device__ __forceinline__ uint32_t nib2_bf16(uint32_t w)
     return lop3_and_or(w, 0x000F000Fu, 0x43004300u);
 }
 
+// fp16 has 10 mantissa bits and 0x64 is the exponent of 1024 (unit in the last place
+// 1): the codes in bits 0-3 / 16-19 become the pair (1024 + lo, 1024 + hi) and those in
+// bits 4-7 / 20-23 the pair (1024 + 16 lo, 1024 + 16 hi), one LOP3 each, no shift.
+__device__ __forceinline__ uint32_t nib2_f16(uint32_t w) { return lop3_and_or(w, 0x000F000Fu, 0x64006400u); }
+__device__ __forceinline__ uint32_t nib2_f16_x16(uint32_t w) { return lop3_and_or(w, 0x00F000F0u, 0x64006400u); }
+
 __device__ __forceinline__ float bf16lo_f32(uint32_t pair) { return __uint_as_float(pair << 16); }
 __device__ __forceinline__ float bf16hi_f32(uint32_t pair) { return __uint_as_float(pair & 0xFFFF0000u); }
 
@@ -171,6 +187,14 @@ __device__ __forceinline__ uint32_t f32x2_to_bf16x2(float lo, float hi)
 {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// A bf16 pair as an fp16 pair (exact for |v| < 65536, apart from fp16 subnormals).
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t pair)
+{
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(bf16hi_f32(pair)), "f"(bf16lo_f32(pair)));
+    return r;
 }
 
 }  // namespace tfq

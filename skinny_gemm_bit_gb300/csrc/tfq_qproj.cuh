@@ -169,6 +169,63 @@ __device__ __forceinline__ void tile_mac_chain(const uint8_t* tile, int lane, co
     }
 }
 
+// The tile math on fp16 activations (B fragments converted from bf16 after staging).
+//   4-bit: A registers 0 and 2 (rows gi) hold 1024 + q and registers 1 and 3 (rows
+//   gi + 8) hold 1024 + 16 q (one LOP3 each, no shift), so
+//      sum_k x (s q + b) = s D + (b - 1024 s) sum x          (rows gi)
+//                        = (s / 16) D + (b - 64 s) sum x     (rows gi + 8)
+//   8-bit: q = 16 hi + lo, and the low- and high-nibble MMAs of a k block share one
+//   accumulator: D = sum x (1024 + lo) + sum x (1024 + 16 hi) = sum x q + 2048 sum x.
+template <int BITS>
+__device__ __forceinline__ void tile_mac_f16(const uint8_t* tile, int lane, const uint4& xa, const uint4& xb,
+                                             const float2& xs, float (&acc)[4])
+{
+    constexpr int QB = tile_q_bytes_for(BITS);
+    const uint2 sb = *reinterpret_cast<const uint2*>(tile + QB + (lane >> 2) * 8);
+    float d[4] = {0.f, 0.f, 0.f, 0.f};
+    if constexpr (BITS == 4) {
+        const uint4 wv = *reinterpret_cast<const uint4*>(tile + lane * 16);
+        mma_f16_16816(d, nib2_f16(wv.x), nib2_f16_x16(wv.x), nib2_f16(wv.x >> 8), nib2_f16_x16(wv.x >> 8), xa.x, xa.y);
+        mma_f16_16816(d, nib2_f16(wv.y), nib2_f16_x16(wv.y), nib2_f16(wv.y >> 8), nib2_f16_x16(wv.y >> 8), xa.z, xa.w);
+        mma_f16_16816(d, nib2_f16(wv.z), nib2_f16_x16(wv.z), nib2_f16(wv.z >> 8), nib2_f16_x16(wv.z >> 8), xb.x, xb.y);
+        mma_f16_16816(d, nib2_f16(wv.w), nib2_f16_x16(wv.w), nib2_f16(wv.w >> 8), nib2_f16_x16(wv.w >> 8), xb.z, xb.w);
+        const float s_lo = bf16lo_f32(sb.x), s_hi = bf16hi_f32(sb.x);
+        const float c_lo = fmaf(-1024.f, s_lo, bf16lo_f32(sb.y)), c_hi = fmaf(-64.f, s_hi, bf16hi_f32(sb.y));
+        const float s_hi16 = s_hi * 0.0625f;
+        acc[0] = fmaf(s_lo, d[0], fmaf(c_lo, xs.x, acc[0]));
+        acc[1] = fmaf(s_lo, d[1], fmaf(c_lo, xs.y, acc[1]));
+        acc[2] = fmaf(s_hi16, d[2], fmaf(c_hi, xs.x, acc[2]));
+        acc[3] = fmaf(s_hi16, d[3], fmaf(c_hi, xs.y, acc[3]));
+    } else {
+        const uint4 w01 = *reinterpret_cast<const uint4*>(tile + lane * 32);
+        const uint4 w23 = *reinterpret_cast<const uint4*>(tile + lane * 32 + 16);
+#define TFQ_KB8H(w0, w1, b0, b1)                                                                               \
+    mma_f16_16816(d, nib2_f16(w0), nib2_f16((w0) >> 8), nib2_f16(w1), nib2_f16((w1) >> 8), b0, b1);            \
+    mma_f16_16816(d, nib2_f16_x16(w0), nib2_f16_x16((w0) >> 8), nib2_f16_x16(w1), nib2_f16_x16((w1) >> 8), b0, b1);
+        TFQ_KB8H(w01.x, w01.y, xa.x, xa.y)
+        TFQ_KB8H(w01.z, w01.w, xa.z, xa.w)
+        TFQ_KB8H(w23.x, w23.y, xb.x, xb.y)
+        TFQ_KB8H(w23.z, w23.w, xb.z, xb.w)
+#undef TFQ_KB8H
+        const float s_lo = bf16lo_f32(sb.x), s_hi = bf16hi_f32(sb.x);
+        const float c_lo = fmaf(-2048.f, s_lo, bf16lo_f32(sb.y)), c_hi = fmaf(-2048.f, s_hi, bf16hi_f32(sb.y));
+        acc[0] = fmaf(s_lo, d[0], fmaf(c_lo, xs.x, acc[0]));
+        acc[1] = fmaf(s_lo, d[1], fmaf(c_lo, xs.y, acc[1]));
+        acc[2] = fmaf(s_hi, d[2], fmaf(c_hi, xs.x, acc[2]));
+        acc[3] = fmaf(s_hi, d[3], fmaf(c_hi, xs.y, acc[3]));
+    }
+}
+
+template <int BITS, bool F16>
+__device__ __forceinline__ void tile_mac_x(const uint8_t* tile, int lane, const uint4& xa, const uint4& xb,
+                                           const float2& xs, float (&acc)[4])
+{
+    if constexpr (F16)
+        tile_mac_f16<BITS>(tile, lane, xa, xb, xs, acc);
+    else
+        tile_mac_chain<BITS>(tile, lane, xa, xb, xs, acc);
+}
+
 // ---------------------------------------------------------------- activation staging
 //
 // A staged activation buffer holds rows rows[0..Mrows) of x, columns
@@ -426,6 +483,39 @@ __device__ __forceinline__ void x_frag8(const uint8_t* buf, int x_rs, int lane, 
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
                  : "=r"(xb.x), "=r"(xb.y), "=r"(xb.z), "=r"(xb.w)
                  : "r"(a + 64));
+}
+
+// True when some bf16 value in rows [0, rows) of a staged buffer (cols columns) has
+// |v| >= 2^e_lim or is not finite. 2^16: an fp16 copy would not hold it exactly; 2^12
+// for 4-bit codes, whose fp16 offset of 1024 code units (against 128 in bf16) would
+// otherwise cost more in the cancellation s D - 1024 s sum x than the bf16 path.
+template <int e_lim>
+__device__ __forceinline__ bool x_beyond_f16(const uint8_t* buf, int x_rs, int rows, int cols, int t, int nt)
+{
+    constexpr uint32_t kLim = (127u + e_lim) << 7;  // bf16 exponent field of 2^e_lim
+    const int per_row = cols / 8;  // 16-byte chunks
+    bool big = false;
+    for (int i = t; i < rows * per_row; i += nt) {
+        const int m = i / per_row, c = i - m * per_row;
+        const uint4 v = *reinterpret_cast<const uint4*>(buf + m * x_rs + c * 16);
+        const uint32_t vv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            big |= (vv[q] & 0x7F80u) >= kLim || ((vv[q] >> 16) & 0x7F80u) >= kLim;
+    }
+    return big;
+}
+
+// Rows [0, rows) of a staged buffer from bf16 to fp16 in place.
+__device__ __forceinline__ void x_to_f16(uint8_t* buf, int x_rs, int rows, int cols, int t, int nt)
+{
+    const int per_row = cols / 8;
+    for (int i = t; i < rows * per_row; i += nt) {
+        const int m = i / per_row, c = i - m * per_row;
+        uint4* ptr = reinterpret_cast<uint4*>(buf + m * x_rs + c * 16);
+        const uint4 v = *ptr;
+        *ptr = make_uint4(bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y), bf16x2_to_f16x2(v.z), bf16x2_to_f16x2(v.w));
+    }
 }
 
 // Final values of one lane's accumulator fragment (rows row0 + gi, row0 + gi + 8;
@@ -945,6 +1035,35 @@ __global__ void __launch_bounds__((NWT + 1) * 32, NWT == 8 ? 2 : 1) qproj_kernel
     }
 }
 
+// One chunk of a warp worker: cnt tiles of one row block (and, for gate + up, the
+// matching tiles of the second matrix T tiles further), groups g0.. of the staged
+// buffer, group sums from xs0; a single matrix takes two tiles per iteration into
+// separate accumulators (gate and up are two independent chains already).
+template <int BITS, bool DUAL, bool F16>
+__device__ __forceinline__ void warp_chunk(const uint8_t* sb, const uint8_t* xb, const float* xs, int x_rs, int lane,
+                                           int tq, int g0, int xs0, int cnt, int T, float (&acc0)[4], float (&acc1)[4])
+{
+    constexpr int TILE = tile_bytes_for(BITS);
+    int j = 0;
+    for (; !DUAL && j + 1 < cnt; j += 2) {
+        uint4 xa, xbv, ya, ybv;
+        x_frag8(xb, x_rs, lane, g0 + j, xa, xbv);
+        x_frag8(xb, x_rs, lane, g0 + j + 1, ya, ybv);
+        const float2 xsv = *reinterpret_cast<const float2*>(xs + (xs0 + j) * kMaxM + 2 * tq);
+        const float2 ysv = *reinterpret_cast<const float2*>(xs + (xs0 + j + 1) * kMaxM + 2 * tq);
+        tile_mac_x<BITS, F16>(sb + j * TILE, lane, xa, xbv, xsv, acc0);
+        tile_mac_x<BITS, F16>(sb + (j + 1) * TILE, lane, ya, ybv, ysv, acc1);
+    }
+    for (; j < cnt; ++j) {
+        uint4 xa, xbv;
+        x_frag8(xb, x_rs, lane, g0 + j, xa, xbv);
+        const float2 xsv = *reinterpret_cast<const float2*>(xs + (xs0 + j) * kMaxM + 2 * tq);
+        tile_mac_x<BITS, F16>(sb + j * TILE, lane, xa, xbv, xsv, acc0);
+        if constexpr (DUAL)
+            tile_mac_x<BITS, F16>(sb + (T + j) * TILE, lane, xa, xbv, xsv, acc1);
+    }
+}
+
 // ---------------------------------------------------------------- warp mode
 //
 // For bandwidth-bound calls. The C x nw consumer warps of the grid are "workers";
@@ -1000,6 +1119,7 @@ __global__ void __launch_bounds__(kThreads, 1) qproj_warp_kernel(const __grid_co
         mbar_init(&xbar[0], 1);
         mbar_init(&xbar[1], 1);
         flags[0] = 0;
+        flags[2] = 0;  // a staged value has no exact fp16 copy
         fence_mbar_init();
     }
     if (threadIdx.x < 16)
@@ -1156,6 +1276,27 @@ __global__ void __launch_bounds__(kThreads, 1) qproj_warp_kernel(const __grid_co
               kConsumerWarps, kBarConsumers);
     if (two)
         x_prepare(p, xb1, nullptr, M1, xg0_1, xg0_1, p.Gs, xs1, inv1, cw, lane, kConsumerWarps, kBarConsumers);
+    // fp16 activations when every staged value converts exactly and, for 4-bit codes,
+    // |x| < 4096 (the group sums above are of the same values): the codes then unpack
+    // with fewer instructions. The decision is the CTA's, from one snapshot.
+    {
+        constexpr int kLimExp = BITS == 4 ? 12 : 16;
+        const int t = cw * 32 + lane, nt = kConsumerWarps * 32;
+        bool big = x_beyond_f16<kLimExp>(xb0, p.x_rs, M0, xgc * kGroup, t, nt);
+        if (two)
+            big |= x_beyond_f16<kLimExp>(xb1, p.x_rs, M1, xgc * kGroup, t, nt);
+        if (big)
+            flags[2] = 1;
+        named_bar_sync(kBarConsumers, kConsumerWarps * 32);
+    }
+    const bool f16 = flags[2] == 0;
+    if (f16) {
+        const int t = cw * 32 + lane, nt = kConsumerWarps * 32;
+        x_to_f16(xb0, p.x_rs, M0, xgc * kGroup, t, nt);
+        if (two)
+            x_to_f16(xb1, p.x_rs, M1, xgc * kGroup, t, nt);
+        named_bar_sync(kBarConsumers, kConsumerWarps * 32);
+    }
 
     if (cw < NW && alive) {
         int64_t u, u1;
@@ -1183,26 +1324,10 @@ __global__ void __launch_bounds__(kThreads, 1) qproj_warp_kernel(const __grid_co
                     }
                     const uint8_t* sb = ring + s * slot_bytes;
                     const int xs0 = norm ? ss * p.Gs + gl + g : gl + g;  // group sums of the chunk start
-                    int j = 0;
-                    // a single matrix takes two tiles per iteration into separate accumulators
-                    // (gate and up are two independent chains already)
-                    for (; !DUAL && j + 1 < cnt; j += 2) {
-                        uint4 xa, xbv, ya, ybv;
-                        x_frag8(xb, p.x_rs, lane, grel0 + g + j, xa, xbv);
-                        x_frag8(xb, p.x_rs, lane, grel0 + g + j + 1, ya, ybv);
-                        const float2 xsv = *reinterpret_cast<const float2*>(xs + (xs0 + j) * kMaxM + 2 * tq);
-                        const float2 ysv = *reinterpret_cast<const float2*>(xs + (xs0 + j + 1) * kMaxM + 2 * tq);
-                        tile_mac_chain<BITS>(sb + j * TILE, lane, xa, xbv, xsv, acc0);
-                        tile_mac_chain<BITS>(sb + (j + 1) * TILE, lane, ya, ybv, ysv, acc1);
-                    }
-                    for (; j < cnt; ++j) {
-                        uint4 xa, xbv;
-                        x_frag8(xb, p.x_rs, lane, grel0 + g + j, xa, xbv);
-                        const float2 xsv = *reinterpret_cast<const float2*>(xs + (xs0 + j) * kMaxM + 2 * tq);
-                        tile_mac_chain<BITS>(sb + j * TILE, lane, xa, xbv, xsv, acc0);
-                        if constexpr (DUAL)
-                            tile_mac_chain<BITS>(sb + (T + j) * TILE, lane, xa, xbv, xsv, acc1);
-                    }
+                    if (f16)
+                        warp_chunk<BITS, DUAL, true>(sb, xb, xs, p.x_rs, lane, tq, grel0 + g, xs0, cnt, T, acc0, acc1);
+                    else
+                        warp_chunk<BITS, DUAL, false>(sb, xb, xs, p.x_rs, lane, tq, grel0 + g, xs0, cnt, T, acc0, acc1);
                     __syncwarp();
                     if (lane == 0)
                         mbar_arrive(&empty[s]);

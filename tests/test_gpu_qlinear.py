@@ -326,6 +326,34 @@ def test_both_schedules_match(T, mode, M, K, N, bits, dual):
         assert_close(host_f64(y), y_ref, tol_linear(ad), f"mode {mode}")
 
 
+@pytest.mark.parametrize("bits", [4, 8])
+@pytest.mark.parametrize("case", ["below_4096", "near_65536", "beyond_65536", "tiny"])
+def test_warp_workers_fp16_activation_edges(T, bits, case):
+    # the warp workers convert staged activations to fp16 when every value converts
+    # exactly (|x| < 65536, finite; for 4-bit codes |x| < 4096) and keep bf16
+    # otherwise; fp16 subnormals round
+    rng = np.random.default_rng(["below_4096", "near_65536", "beyond_65536", "tiny"].index(case) * 10 + bits)
+    M, K, N = 3, 1024, 4096
+    xf = rng.standard_normal((M, K)).astype(np.float32)
+    if case == "below_4096":
+        xf[0, 5], xf[2, 700] = 4080.0, -3968.0  # fp16 path for both code widths
+    elif case == "near_65536":
+        xf[0, 5], xf[2, 700] = 65280.0, -61440.0  # largest bf16 values below 65536
+    elif case == "beyond_65536":
+        xf[1, 17] = 131072.0  # the bf16 path for the CTAs staging row 1
+    else:
+        xf *= 1e-6  # fp16 subnormal range
+    x = synth.f32_to_bf16_bits(xf)
+    w = synth.quant_weights(rng, N, K, bits)
+    T.tune_set(T.TF_TUNE_MODE, 2)
+    try:
+        y = T.tf_qlinear_run(pack(T, w), dev_bf16(x), out_dtype=torch.float32)
+    finally:
+        T.tune_set(T.TF_TUNE_MODE, -1)
+    y_ref, ad = oracle.qlinear(oracle.bf16_to_f64(x), w)
+    assert_close(host_f64(y), y_ref, tol_linear(ad), f"warp workers, {case}, {bits}-bit")
+
+
 @pytest.mark.parametrize("warps,chunk", [(8, 32), (16, 32), (8, 16), (8, 64)])
 @pytest.mark.parametrize("M,K,N,bits,norm", [
     (8, 12800, 2560, 4, False),  # 8 K splits of 25 groups, stream-K cuts inside row blocks
