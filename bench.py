@@ -7,12 +7,13 @@ whose total is more than four times the L2 cache, so every call streams its
 weights from HBM. Steps are captured once into a CUDA graph and replayed.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl tfq|reference]
-                  [--workload gateup|proj|wide|step|moe4|moe8]
+                  [--workload gateup|proj|wide|readout|step|moe4|moe8]
 
 The other workloads: proj (one K=1024, N=3072 projection, M=1), wide (K=12800,
-N=2560, one M=1 and one M=8 call), step (the whole per-token weight stream of a
-28-layer dense decoder, one M=1 and one M=8 step), moe4 / moe8 (the MoE layer,
-M=8, one call).
+N=2560, one M=1 and one M=8 call), readout (the decoder's RMSNorm + tied readout,
+K=1024, N=151936, one M=1 and one M=8 call), step (the whole per-token weight
+stream of a 28-layer dense decoder, one M=1 and one M=8 step), moe4 / moe8 (the
+MoE layer, M=8, one call).
 
 value      effective weight GB/s: algorithmic weight bytes (codes + scales +
            biases) of all calls / device time of the timed region.
@@ -325,20 +326,28 @@ class GateUp(Workload):
 
 
 class Proj(Workload):
-    """One 4-bit projection per step: K=1024, N=3072, M=1 (single projection), or
-    K=12800, N=2560 at M=1 and M=8 (wide verify projection)."""
+    """One 4-bit projection per step: K=1024, N=3072, M=1 (single projection); K=12800,
+    N=2560 at M=1 and M=8 (wide verify projection); or the decoder's tied readout with
+    its RMSNorm, K=1024, N=151936, at M=1 and M=8."""
 
-    def __init__(self, T, torch, l2_bytes, wide: bool):
+    def __init__(self, T, torch, l2_bytes, kind: str):
         super().__init__(T, torch)
         from skinny_gemm_bit_gb300 import synth
-        if wide:
+        self.gamma, self.eps = None, 1e-6
+        if kind == "wide":
             cfg = synth.wide_verify(seed=2, M=8)
             self.name, self.step_ms = "wide", (1, 8)
-            self.kernel_key, self.kernel = "qproj_b4_k12800_n2560", "qproj_warp_kernel<4> (split K)"
+            self.kernel_key, self.kernel = "qproj_b4_k12800_n2560", "qproj_kernel<4> (long-row team schedule, K split)"
+        elif kind == "readout":
+            cfg = synth.single_projection(seed=3, M=8, K=1024, N=151936)
+            self.name, self.step_ms = "readout", (1, 8)
+            self.kernel_key, self.kernel = "qproj_b4_k1024_n151936_norm", "qproj_warp_kernel<4> (warp workers)"
+            self.gamma = _dev_bf16(torch, synth.gamma(np.random.default_rng(5), 1024))
         else:
             cfg = synth.single_projection(seed=0, M=1)
             self.name, self.step_ms = "proj", (1,)
             self.kernel_key, self.kernel = "qproj_b4_k1024_n3072", "qproj_kernel<4> (light team schedule)"
+        wide = kind == "wide"
         w0 = _pack(T, cfg["w"])
         self.w = cfg["w"]
         self.K, self.N, self.bits = w0.K, w0.N, 4
@@ -351,11 +360,11 @@ class Proj(Workload):
         self.ws = T.workspace(T.tf_qlinear_workspace_bytes(w0, 8))
         self.sample_x = x8
         ms = " and ".join(f"M={M}" for M in self.step_ms)
-        self.desc = (f"{'wide verify' if wide else 'single'} 4-bit group-64 projection, K={self.K}, N={self.N}; "
-                     f"one {ms} call per step")
+        what = {"wide": "wide verify", "readout": "RMSNorm + tied readout", "proj": "single"}[kind]
+        self.desc = f"{what} 4-bit group-64 projection, K={self.K}, N={self.N}; one {ms} call per step"
 
     def call(self, i, M, flags, x, out):
-        self.T.tf_qlinear_run(self.copies[i], x, out=out, ws=self.ws, flags=flags)
+        self.T.tf_qlinear_run(self.copies[i], x, gamma=self.gamma, eps=self.eps, out=out, ws=self.ws, flags=flags)
 
     def sample_matrix(self):
         return self.w, 256 if self.K <= 2048 else 32, "the weight matrix"
@@ -444,14 +453,14 @@ class MoE(Workload):
         return e0, 128, "expert 0's gate matrix"
 
 
-WORKLOADS = ("gateup", "proj", "wide", "step", "moe4", "moe8")
+WORKLOADS = ("gateup", "proj", "wide", "readout", "step", "moe4", "moe8")
 
 
 def make_workload(name, T, torch, l2_bytes):
     if name == "gateup":
         return GateUp(T, torch, l2_bytes)
-    if name in ("proj", "wide"):
-        return Proj(T, torch, l2_bytes, wide=name == "wide")
+    if name in ("proj", "wide", "readout"):
+        return Proj(T, torch, l2_bytes, kind=name)
     if name == "step":
         return Step(T, torch, l2_bytes)
     if name in ("moe4", "moe8"):
@@ -618,12 +627,14 @@ class _HostOnly:
             self.K, self.N, self.ms, self.bits = 1024, 3072, [1, 8], 4
         else:
             self.impl = Workload.__new__(Workload)
-            if name in ("proj", "wide"):
-                cfg = synth.wide_verify(seed=2, M=8) if name == "wide" else synth.single_projection(seed=0, M=1)
+            if name in ("proj", "wide", "readout"):
+                cfg = {"wide": lambda: synth.wide_verify(seed=2, M=8),
+                       "readout": lambda: synth.single_projection(seed=3, M=8, K=1024, N=151936),
+                       "proj": lambda: synth.single_projection(seed=0, M=1)}[name]()
                 w = cfg["w"]
                 x8 = cfg["x"] if cfg["x"].shape[0] == 8 else np.repeat(cfg["x"], 8, axis=0)
                 rows, what = (256, "the weight matrix") if w["K"] <= 2048 else (32, "the weight matrix")
-                self.impl.step_ms = (1, 8) if name == "wide" else (1,)
+                self.impl.step_ms = (1,) if name == "proj" else (1, 8)
                 self.K, self.N, self.bits = w["K"], w["N"], 4
                 self.desc = f"{name} 4-bit group-64 projection, K={w['K']}, N={w['N']}"
             elif name == "step":
@@ -694,8 +705,9 @@ def main():
     ap.add_argument("--ref-step-seconds", type=float, default=0.2)
     ap.add_argument("--workload", default="gateup", choices=WORKLOADS,
                     help="gateup (default): fused RMSNorm + gate/up, K=1024, N=2x3072, M=1 and 8; proj: "
-                         "K=1024, N=3072, M=1; wide: K=12800, N=2560, M=1 and 8; step: 28-layer decoder weight "
-                         "stream, M=1 and 8; moe4 / moe8: MoE layer, M=8")
+                         "K=1024, N=3072, M=1; wide: K=12800, N=2560, M=1 and 8; readout: RMSNorm + tied "
+                         "readout, K=1024, N=151936, M=1 and 8; step: 28-layer decoder weight stream, M=1 and 8; "
+                         "moe4 / moe8: MoE layer, M=8")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
