@@ -212,8 +212,16 @@ Plan plan_qproj(int n_rb, int groups, int mats, int bits, int slots, int k_full,
 
     // K splits: the split's activation slice for 8 rows must stay within 112 KB (the same
     // split for every M, so a row gives the same bits alone or in a block of 8)
+    // long rows of one plain matrix (few row blocks, many groups, bandwidth-bound):
+    // warp workers over K splits of at most 40 groups, 8 workers a CTA (on GB300 this
+    // measured 12.8 / 14.8 us at M = 1 / 8 for K = 12800, N = 2560, against 14.6 / 17.0
+    // for lock-step teams over two splits)
+    const bool long_plain = slots == 1 && mats == 1 && k_full == 0 && groups >= 64 && n_rb <= 2 * sms &&
+                            (double)n_rb * groups * tile > 8.0 * 1024 * 1024 && g_tune[TF_TUNE_MODE] <= 0;
     int S = 1;
     while ((int64_t)kMaxM * (groups / S) * kGroup * 2 > 112 * 1024 || groups % S != 0)
+        ++S;
+    while (long_plain && (groups / S > 40 || groups % S != 0))
         ++S;
     if (g_tune[TF_TUNE_SPLITK] > 0 && groups % g_tune[TF_TUNE_SPLITK] == 0)
         S = g_tune[TF_TUNE_SPLITK];
@@ -250,8 +258,8 @@ Plan plan_qproj(int n_rb, int groups, int mats, int bits, int slots, int k_full,
 
     // long rows (a plain problem with few, long segments per CTA and enough bytes to be
     // bandwidth-bound): one segment at a time, all warps on it, stages of about 27 KB
-    const bool long_rows = slots == 1 && items <= 8LL * sms && (double)U * tile * mats > 8.0 * 1024 * 1024 &&
-                           pl.Gs >= 2 * kConsumerWarps;
+    const bool long_rows = !long_plain && slots == 1 && items <= 8LL * sms &&
+                           (double)U * tile * mats > 8.0 * 1024 * 1024 && pl.Gs >= 2 * kConsumerWarps;
 
     // teams: R segments side by side, KW warps per segment, at least two tiles a warp
     int R = 1;
@@ -342,11 +350,11 @@ Plan plan_qproj(int n_rb, int groups, int mats, int bits, int slots, int k_full,
     // ---- bandwidth-bound calls: warp workers with private ring slots
     // MoE layers (many problems, each with its own activation rows): 8 workers a CTA
     // measured fastest; otherwise all 16
-    const int nw_default = slots > 1 ? 8 : kConsumerWarps;
+    const int nw_default = slots > 1 || long_plain ? 8 : kConsumerWarps;
     const int nw = g_tune[TF_TUNE_WARPS] > 0 ? std::min(g_tune[TF_TUNE_WARPS], kConsumerWarps) : nw_default;
     const int64_t W = (int64_t)sms * nw;
     const int64_t upc_max_all = (U + pl.C - 1) / pl.C;  // units per CTA with every slot active
-    bool warp_mode = !long_rows && U >= 4 * W && upc_max_all <= per_ps;
+    bool warp_mode = (long_plain || (!long_rows && U >= 4 * W)) && upc_max_all <= per_ps;
     if (g_tune[TF_TUNE_MODE] > 0)
         warp_mode = g_tune[TF_TUNE_MODE] == 2 && upc_max_all <= per_ps;
     if (warp_mode) {
