@@ -15,6 +15,18 @@ namespace {
 
 constexpr int kRouteThreads = 256;
 
+// Order-preserving unsigned key of an fp32 logit (-0 as +0): a > b iff key(a) > key(b).
+__device__ __forceinline__ uint32_t order_key(float f)
+{
+    const uint32_t b = __float_as_uint(f == 0.f ? 0.f : f);
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+__device__ __forceinline__ float key_value(uint32_t k)
+{
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
 // One CTA. PER = logits per lane (E <= 32 PER), so a row's logits sit in registers.
 template <int PER>
 __global__ void __launch_bounds__(kRouteThreads) moe_route_kernel(const float* __restrict__ logits, int M, int E,
@@ -23,6 +35,7 @@ __global__ void __launch_bounds__(kRouteThreads) moe_route_kernel(const float* _
 {
     __shared__ int32_t sel[kMaxM * 8];  // (row, j) -> expert, -1 when unused
     __shared__ uint8_t act[1024];       // expert selected by some row
+    __shared__ int32_t slot_of[1024];   // active expert -> its slot
     __shared__ int32_t warp_tot[kRouteThreads / 32];
 
     pdl_wait();
@@ -34,44 +47,42 @@ __global__ void __launch_bounds__(kRouteThreads) moe_route_kernel(const float* _
         sel[threadIdx.x] = -1;
     __syncthreads();
 
-    // ---- top-k per row (warp m): k rounds of a warp arg-max over the experts not yet taken
+    // ---- top-k per row (warp m): k rounds of a warp arg-max over the experts not yet
+    // taken: each lane proposes its largest logit (lowest expert on ties), one warp max
+    // of the order keys finds the value, one warp min the lowest expert holding it
     for (int m = warp; m < M; m += kRouteThreads / 32) {
         const float* l = logits + (int64_t)m * E;
-        float vals[PER];
+        uint32_t keys[PER];
 #pragma unroll
         for (int i = 0; i < PER; ++i) {
             const int e = lane + 32 * i;
-            vals[i] = e < E ? __ldcg(l + e) : 0.f;
+            keys[i] = e < E ? order_key(__ldcg(l + e)) : 0u;
         }
         uint32_t taken = 0;  // bit i: expert lane + 32 i taken
         float top = 0.f, mine = 0.f;  // the largest selected logit; lane j: the j-th one
         for (int j = 0; j < top_k; ++j) {
-            float bv = 0.f;
-            int be = -1;
+            uint32_t bk = 0;
+            int bi = -1;
 #pragma unroll
             for (int i = 0; i < PER; ++i) {
                 const int e = lane + 32 * i;
-                if (e < E && !((taken >> i) & 1u) && (be < 0 || vals[i] > bv)) {  // ascending e keeps the lower
-                    bv = vals[i];
-                    be = e;
+                if (e < E && !((taken >> i) & 1u) && (bi < 0 || keys[i] > bk)) {  // ascending i keeps the lower
+                    bk = keys[i];
+                    bi = i;
                 }
             }
-            for (int o = 16; o > 0; o >>= 1) {
-                const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-                const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-                if (oe >= 0 && (be < 0 || ov > bv || (ov == bv && oe < be))) {
-                    bv = ov;
-                    be = oe;
-                }
-            }
-            if ((be & 31) == lane)
+            const uint32_t kmax = __reduce_max_sync(0xffffffffu, bk);
+            const uint32_t be = __reduce_min_sync(0xffffffffu, bi >= 0 && bk == kmax ? (uint32_t)(lane + 32 * bi)
+                                                                                       : 0xffffffffu);
+            if ((int)(be & 31u) == lane)
                 taken |= 1u << (be >> 5);
+            const float v = key_value(kmax);
             if (j == 0)
-                top = bv;
+                top = v;
             if (lane == j)
-                mine = bv;
+                mine = v;
             if (lane == 0) {
-                sel[m * 8 + j] = be;
+                sel[m * 8 + j] = (int)be;
                 act[be] = 1;
             }
         }
@@ -120,28 +131,38 @@ __global__ void __launch_bounds__(kRouteThreads) moe_route_kernel(const float* _
         before += warp_tot[w];
     if (threadIdx.x == kRouteThreads - 1)
         meta->n_active = before + cnt;
-    // ---- each active expert's rows, in ascending (row, slot j) order
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int e = e0 + i;
-        if (!act[e])
-            continue;
-        const int slot = before++;
-        MoeSlot& s = meta->slot[slot];
-        s.expert = e;
-        int c = 0;
-        for (int q = 0; q < M * 8; ++q)
-            if (sel[q] == e) {
-                s.rows[c] = q >> 3;
-                s.js[c] = q & 7;
-                meta->inv[q] = slot * 8 + c;
-                ++c;
-            }
-        for (int c2 = c; c2 < kMaxM; ++c2) {
-            s.rows[c2] = 0;
-            s.js[c2] = 0;
+    for (int i = 0; i < 4; ++i)
+        if (act[e0 + i])
+            slot_of[e0 + i] = before++;
+    __syncthreads();
+
+    // ---- one thread per (row, j) pair: its rank among the earlier pairs of the same
+    // expert is its column in the expert's slot, so each slot lists its rows in
+    // ascending (row, j) order; the first pair of an expert fills the slot's header
+    const int q = threadIdx.x;
+    if (q < M * 8 && sel[q] >= 0) {
+        const int e = sel[q];
+        int c = 0, total = 0;
+        for (int q2 = 0; q2 < M * 8; ++q2) {
+            const int same = sel[q2] == e;
+            total += same;
+            if (q2 < q)
+                c += same;
         }
-        s.count = c;
+        const int slot = slot_of[e];
+        MoeSlot& s = meta->slot[slot];
+        s.rows[c] = q >> 3;
+        s.js[c] = q & 7;
+        meta->inv[q] = slot * 8 + c;
+        if (c == 0) {
+            s.expert = e;
+            s.count = total;
+            for (int c2 = total; c2 < kMaxM; ++c2) {
+                s.rows[c2] = 0;
+                s.js[c2] = 0;
+            }
+        }
     }
 }
 
