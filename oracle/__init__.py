@@ -73,6 +73,8 @@ def _load():
     lib.oracle_swiglu.restype = None
     lib.oracle_topk_softmax.argtypes = [P, I64, I64, I64, P, P]
     lib.oracle_topk_softmax.restype = I
+    lib.oracle_rht.argtypes = [P, I64, I64, P, I64, P]
+    lib.oracle_rht.restype = I
     _lib = lib
     return lib
 
@@ -143,6 +145,22 @@ def rmsnorm(x, gamma, eps: float) -> np.ndarray:
     M, K = x.shape
     out = np.empty_like(x)
     _load().oracle_rmsnorm(_ptr(x), M, K, _ptr(gamma), float(eps), _ptr(out))
+    return out
+
+
+def rht(x, signs, block: int = 64) -> np.ndarray:
+    """Input randomized Hadamard transform, float64: per block of `block` columns,
+    H (d * x) / sqrt(block), H Sylvester-ordered, d[k] = -1 where bit k of the
+    LSB-first bit vector `signs` (uint8 [K / 8]) is set (uzu page, "Internals 1"
+    table, linear row: input RHT)."""
+    x = _c(np.atleast_2d(x), np.float64)
+    M, K = x.shape
+    signs = _c(signs, np.uint8)
+    if signs.size * 8 < K:
+        raise ValueError("signs must hold K bits")
+    out = np.empty_like(x)
+    if _load().oracle_rht(_ptr(x), M, K, _ptr(signs), block, _ptr(out)):
+        raise ValueError(f"block {block} must be a power of two dividing K={K}")
     return out
 
 

@@ -27,6 +27,12 @@
  *   - MoE routing (uzu page, same table, mlp row: MixtureOfExperts with a
  *     routing function): top-k of the router logits, descending, ties to the
  *     lower expert index, softmax over the k selected logits.
+ *   - input randomized Hadamard transform (uzu page, same table, linear row:
+ *     an input-side RHT block that spreads quantisation error): the pages give
+ *     no block size or layout; the reading used is, per block of `block`
+ *     consecutive columns (64 = one quantisation group), xr = H (d .* x) /
+ *     sqrt(block) with H the Sylvester-ordered Walsh-Hadamard matrix and d a
+ *     +-1 vector stored as bits, least-significant first, bit set = -1.
  *
  * Parity pins for every function live in tests/test_oracle_pins.py.
  */
@@ -200,5 +206,38 @@ int oracle_topk_softmax(const float *logits, int64_t M, int64_t E, int64_t top_k
             w[m * top_k + j] = exp((double)l[idx[m * top_k + j]] - lmax) / denom;
     }
     free(taken);
+    return 0;
+}
+
+/* Input randomized Hadamard transform, row by row and block by block:
+ * out[m][b*block + i] = sum_j H[i][j] * d[b*block + j] * x[m][b*block + j] / sqrt(block),
+ * H[i][j] = (-1)^popcount(i & j), computed with the textbook in-place butterflies
+ * (stride 1, 2, 4, ...: (a, b) -> (a + b, a - b)), which give exactly that order.
+ * signs: bit k % 8 of byte k / 8 set means d[k] = -1. block: a power of two
+ * dividing K. Returns nonzero on a bad block size. */
+int oracle_rht(const double *x, int64_t M, int64_t K, const uint8_t *signs, int64_t block, double *out)
+{
+    if (block < 1 || (block & (block - 1)) != 0 || K % block != 0)
+        return 1;
+    const double scale = 1.0 / sqrt((double)block);
+    for (int64_t m = 0; m < M; ++m) {
+        for (int64_t k0 = 0; k0 < K; k0 += block) {
+            double *v = out + m * K + k0;
+            for (int64_t j = 0; j < block; ++j) {
+                const int64_t k = k0 + j;
+                const int neg = (signs[k / 8] >> (k % 8)) & 1;
+                v[j] = neg ? -x[m * K + k] : x[m * K + k];
+            }
+            for (int64_t h = 1; h < block; h *= 2)
+                for (int64_t i = 0; i < block; i += 2 * h)
+                    for (int64_t j = i; j < i + h; ++j) {
+                        const double a = v[j], b = v[j + h];
+                        v[j] = a + b;
+                        v[j + h] = a - b;
+                    }
+            for (int64_t j = 0; j < block; ++j)
+                v[j] *= scale;
+        }
+    }
     return 0;
 }

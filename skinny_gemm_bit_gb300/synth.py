@@ -64,6 +64,12 @@ def gamma(rng, K: int) -> np.ndarray:
     return f32_to_bf16_bits(1.0 + 0.1 * rng.standard_normal(K, dtype=np.float32))
 
 
+def rht_signs(rng, K: int) -> np.ndarray:
+    """Random +-1 signs of an input Hadamard transform as K bits (uint8 [K / 8],
+    least-significant bit first, bit set = -1), uniform and independent."""
+    return rng.integers(0, 256, size=(K + 7) // 8, dtype=np.uint8)
+
+
 def router_logits(rng, M: int, E: int) -> np.ndarray:
     """Router logits ~ N(0, 1), fp32 [M, E]."""
     return rng.standard_normal((M, E), dtype=np.float32)

@@ -307,3 +307,61 @@ def test_decode_step_ignores_k_and_v_rows():
     b = oracle.decode_step(x, _oracle_layers(cfg), fn, cfg["readout"], q_dim)
     assert np.array_equal(a["logits"], b["logits"])
     assert not np.array_equal(a["stages"][0]["qkv"][:, q_dim:], b["stages"][0]["qkv"][:, q_dim:])
+
+
+# ------------------------------------------------------------------ input Hadamard transform
+
+def _signs_to_pm1(signs, K):
+    bits = np.unpackbits(np.asarray(signs, np.uint8), bitorder="little")[:K]
+    return 1.0 - 2.0 * bits.astype(np.float64)
+
+
+@pytest.mark.parametrize("block", [64, 16, 256])
+def test_rht_matches_the_library_hadamard_matrix(block):
+    # scipy's Sylvester Hadamard matrix, the sign vector unpacked with numpy: the
+    # oracle's butterflies must give exactly H (d * x) / sqrt(block) per block
+    from scipy.linalg import hadamard
+    rng = np.random.default_rng(500 + block)
+    M, K = 3, 512
+    x = rng.standard_normal((M, K))
+    signs = synth.rht_signs(rng, K)
+    d = _signs_to_pm1(signs, K)
+    H = hadamard(block).astype(np.float64) / math.sqrt(block)
+    expect = np.concatenate([(H @ (d[k0:k0 + block] * x[:, k0:k0 + block]).T).T for k0 in range(0, K, block)], axis=1)
+    np.testing.assert_allclose(oracle.rht(x, signs, block), expect, rtol=0, atol=1e-12)
+
+
+def test_rht_is_orthonormal_and_undone_by_its_transpose():
+    rng = np.random.default_rng(510)
+    M, K = 4, 1024
+    x = rng.standard_normal((M, K))
+    signs = synth.rht_signs(rng, K)
+    xr = oracle.rht(x, signs)
+    np.testing.assert_allclose(np.linalg.norm(xr, axis=1), np.linalg.norm(x, axis=1), rtol=1e-13)
+    # H is symmetric and orthonormal: applying it again without signs, then the signs, gives x back
+    back = oracle.rht(xr, np.zeros_like(signs)) * _signs_to_pm1(signs, K)
+    np.testing.assert_allclose(back, x, rtol=0, atol=1e-12)
+
+
+def test_rht_with_rotated_weights_leaves_the_projection():
+    # weights quantised in the rotated basis: W_r = W (D H / 8) per group; then
+    # W_r . rht(x) = W . x (the rotation the transform exists to apply)
+    rng = np.random.default_rng(520)
+    M, K, N = 2, 256, 40
+    x = rng.standard_normal((M, K))
+    W = rng.standard_normal((N, K))
+    signs = synth.rht_signs(rng, K)
+    W_r = oracle.rht(W, signs)  # each row of W rotated the same way
+    np.testing.assert_allclose(W_r @ oracle.rht(x, signs).T, W @ x.T, rtol=1e-12, atol=1e-10)
+
+
+def test_rht_single_column_block_flips_signs_only():
+    rng = np.random.default_rng(530)
+    x = rng.standard_normal((2, 64))
+    signs = synth.rht_signs(rng, 64)
+    np.testing.assert_array_equal(oracle.rht(x, signs, block=1), x * _signs_to_pm1(signs, 64))
+
+
+def test_rht_rejects_a_block_that_is_not_a_power_of_two():
+    with pytest.raises(ValueError):
+        oracle.rht(np.zeros((1, 96)), np.zeros(12, np.uint8), block=48)
