@@ -156,6 +156,25 @@ int tf_qlinear_run(const tf_qweight* w, const uint16_t* x, int64_t ldx, int64_t 
                    void* y, int y_dtype, void* ws, size_t ws_bytes, unsigned flags, void* stream);
 
 /*
+ * tf_qlinear_run with an input randomized Hadamard transform folded into the
+ * activation staging (uzu page, "Internals 1: models are assembled from
+ * configuration", linear row of the table: an input-side RHT block that spreads
+ * quantisation error). The pages give no block size or layout; here
+ *   xr[m][64 g + i] = (1/8) sum_j H[i][j] d[64 g + j] xn[m][64 g + j],
+ *   H[i][j] = (-1)^popcount(i & j)   (the Sylvester-ordered 64-point
+ *                                     Walsh-Hadamard matrix, one per group)
+ * and y[m][n] = residual[m][n] + sum_k xr[m][k] * w[n][k]: w holds weights
+ * quantised in the rotated basis, xn is x or its RMSNorm as in tf_qlinear_run
+ * (normalisation first), and xr is rounded to bf16 once.
+ *   rht_signs  device uint8 [K / 8]: bit (k % 8) of byte k / 8 set means d[k] = -1
+ *              (must not be NULL; read during the call only)
+ *   Other arguments, the workspace query and the errors: as tf_qlinear_run.
+ */
+int tf_qlinear_run_rht(const tf_qweight* w, const uint16_t* x, int64_t ldx, int64_t M, const uint8_t* rht_signs,
+                       const uint16_t* rms_gamma, float rms_eps, const uint16_t* residual, void* y, int y_dtype,
+                       void* ws, size_t ws_bytes, unsigned flags, void* stream);
+
+/*
  * tf_qlinear_run without a workspace argument: the same projection, the same
  * kernels and the same results, with the split-K scratch (status word, arrival
  * counters, fp32 partial slots) taken from one fixed 4 MiB device array inside

@@ -587,7 +587,7 @@ size_t tf_qlinear_workspace_bytes(const tf_qweight* w, int64_t M)
 static int qlinear_impl(const tf_qweight* w, const tf_qweight* w_up, const uint16_t* x, int64_t ldx, int64_t M,
                         const uint16_t* gamma, float eps, const uint16_t* residual, void* y, int64_t ldy, int y_dtype,
                         void* ws, uint8_t* scratch, size_t scratch_bytes, bool pdl, cudaStream_t stream,
-                        const char* name)
+                        const char* name, const uint8_t* rht = nullptr)
 {
     const bool dual = w_up != nullptr;
     const Plan pl = plan_qproj((int)(w->n_pad / 16), (int)(w->K / kGroup), dual ? 2 : 1, w->bits, 1,
@@ -618,15 +618,37 @@ static int qlinear_impl(const tf_qweight* w, const tf_qweight* w_up, const uint1
     p.ldy = ldy;
     p.y_f32 = y_dtype == TF_DTYPE_F32;
     fill_common(p, pl, ws, scratch);
+    p.rht = rht;
     cudaError_t e = launch_qproj(w->bits, dual, false, pl, p, stream, pdl);
     if (e != cudaSuccess)
         return cuda_fail(e, name);
     return TF_OK;
 }
 
+static int qlinear_entry(const tf_qweight* w, const uint16_t* x, int64_t ldx, int64_t M, const uint8_t* rht,
+                         const uint16_t* rms_gamma, float rms_eps, const uint16_t* residual, void* y, int y_dtype,
+                         void* ws, size_t ws_bytes, unsigned flags, void* stream);
+
 int tf_qlinear_run(const tf_qweight* w, const uint16_t* x, int64_t ldx, int64_t M, const uint16_t* rms_gamma,
                    float rms_eps, const uint16_t* residual, void* y, int y_dtype, void* ws, size_t ws_bytes,
                    unsigned flags, void* stream)
+{
+    return qlinear_entry(w, x, ldx, M, nullptr, rms_gamma, rms_eps, residual, y, y_dtype, ws, ws_bytes, flags, stream);
+}
+
+int tf_qlinear_run_rht(const tf_qweight* w, const uint16_t* x, int64_t ldx, int64_t M, const uint8_t* rht_signs,
+                       const uint16_t* rms_gamma, float rms_eps, const uint16_t* residual, void* y, int y_dtype,
+                       void* ws, size_t ws_bytes, unsigned flags, void* stream)
+{
+    if (rht_signs == nullptr)
+        return fail(TF_E_INVALID_ARG, "tf_qlinear_run_rht: rht_signs is NULL");
+    return qlinear_entry(w, x, ldx, M, rht_signs, rms_gamma, rms_eps, residual, y, y_dtype, ws, ws_bytes, flags,
+                         stream);
+}
+
+static int qlinear_entry(const tf_qweight* w, const uint16_t* x, int64_t ldx, int64_t M, const uint8_t* rht,
+                         const uint16_t* rms_gamma, float rms_eps, const uint16_t* residual, void* y, int y_dtype,
+                         void* ws, size_t ws_bytes, unsigned flags, void* stream)
 {
     int rc = check_desc(w, "tf_qlinear_run");
     if (rc)
@@ -647,7 +669,7 @@ int tf_qlinear_run(const tf_qweight* w, const uint16_t* x, int64_t ldx, int64_t 
         return fail(TF_E_WORKSPACE_TOO_SMALL, "%s: workspace too small", "tf_qlinear_run");
     return qlinear_impl(w, nullptr, x, ldx, M, rms_gamma, rms_eps, residual, y, w->N, y_dtype, ws,
                         static_cast<uint8_t*>(ws) + kStatusBytes, ws_bytes - kStatusBytes, (flags & TF_RUN_PDL) != 0,
-                        static_cast<cudaStream_t>(stream), "tf_qlinear_run");
+                        static_cast<cudaStream_t>(stream), rht ? "tf_qlinear_run_rht" : "tf_qlinear_run", rht);
 }
 
 size_t tf_qmlp_gateup_workspace_bytes(const tf_qweight* gate, const tf_qweight* up, int64_t M)

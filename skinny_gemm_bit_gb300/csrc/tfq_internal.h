@@ -86,6 +86,7 @@ struct QProjParams {
     int nw, pw, xsum1_off, xraw1_off;
     int gamma_off;  // staged RMSNorm weight (K bf16)
     int x_direct;   // activations loaded straight into registers (unsplit calls), not by bulk copy
+    const uint8_t* rht;  // input Hadamard transform signs (K bits, LSB first, set = -1) or nullptr
 };
 
 struct Plan {

@@ -234,6 +234,57 @@ __device__ __forceinline__ void tile_mac_x(const uint8_t* tile, int lane, const 
 // then fall in 8 different bank groups, so the ldmatrix that builds the MMA's B
 // fragments (8 rows x 16 bytes per matrix) is conflict-free.
 
+// Input randomized Hadamard transform of one 64-column group held by 8 lanes (lane &
+// 7 = chunk cc, columns 8 cc .. 8 cc + 7; every lane of the warp must call it): the
+// signs byte's bit i negates column 8 cc + i, then the Sylvester-ordered 64-point
+// Walsh-Hadamard transform as H8 over the columns inside a lane (three butterfly
+// stages) and H8 over the chunks across the 8 lanes (three shuffle stages), scaled by
+// 1/8: H64[8 c + i][8 c' + i'] = (-1)^(popcount(c & c') + popcount(i & i')).
+__device__ __forceinline__ void rht_group(float (&v)[8], uint32_t sign_bits, int lane)
+{
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        if ((sign_bits >> i) & 1u)
+            v[i] = -v[i];
+#pragma unroll
+    for (int h = 1; h < 8; h <<= 1)
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            if (!(i & h)) {
+                const float a = v[i], b = v[i + h];
+                v[i] = a + b;
+                v[i + h] = a - b;
+            }
+    const int cc = lane & 7;
+#pragma unroll
+    for (int h = 1; h < 8; h <<= 1)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float o = __shfl_xor_sync(0xffffffffu, v[i], h);
+            v[i] = (cc & h) ? o - v[i] : v[i] + o;
+        }
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        v[i] *= 0.125f;
+}
+
+// bf16 pairs <-> 8 floats
+__device__ __forceinline__ void unpack8(const uint32_t (&vv)[4], float (&v)[8])
+{
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        v[2 * q] = bf16lo_f32(vv[q]);
+        v[2 * q + 1] = bf16hi_f32(vv[q]);
+    }
+}
+
+__device__ __forceinline__ void pack8(const float (&v)[8], uint32_t (&vv)[4])
+{
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+        vv[q] = f32x2_to_bf16x2(v[2 * q], v[2 * q + 1]);
+}
+
 // One thread: copy the rows into the buffer (and, with an RMSNorm, gamma into
 // gbuf); completion on `bar`.
 __device__ __forceinline__ void x_issue(const QProjParams& p, uint8_t* buf, uint8_t* gbuf, const int* rows, int Mrows,
@@ -288,20 +339,35 @@ __device__ __forceinline__ void x_prepare(const QProjParams& p, uint8_t* buf, co
         const int gl = pi / Mrows, m = pi - gl * Mrows;
         const bool valid = pi < ng * Mrows;
         float part = 0.f;
+        uint4* chunk = reinterpret_cast<uint4*>(buf + (valid ? m : 0) * p.x_rs + (valid ? g_lo - xg0 + gl : 0) * 128) + cc;
+        uint32_t vv[4] = {0u, 0u, 0u, 0u};
         if (valid) {
-            uint4* chunk = reinterpret_cast<uint4*>(buf + m * p.x_rs + (g_lo - xg0 + gl) * 128) + cc;
-            uint4 v = *chunk;
-            uint32_t vv[4] = {v.x, v.y, v.z, v.w};
-            if (norm) {
+            const uint4 v = *chunk;
+            vv[0] = v.x;
+            vv[1] = v.y;
+            vv[2] = v.z;
+            vv[3] = v.w;
+        }
+        if (norm || p.rht != nullptr) {  // warp-uniform
+            float f[8];
+            unpack8(vv, f);
+            if (norm && valid) {
                 const uint4 gv = *reinterpret_cast<const uint4*>(gbuf + ((g_lo + gl) * kGroup + cc * 8) * 2);
                 const uint32_t gg[4] = {gv.x, gv.y, gv.z, gv.w};
+                float gf[8];
+                unpack8(gg, gf);
                 const float inv = inv_rms[m];
 #pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    vv[q] = f32x2_to_bf16x2(bf16lo_f32(vv[q]) * inv * bf16lo_f32(gg[q]),
-                                            bf16hi_f32(vv[q]) * inv * bf16hi_f32(gg[q]));
-                *chunk = make_uint4(vv[0], vv[1], vv[2], vv[3]);
+                for (int i = 0; i < 8; ++i)
+                    f[i] = f[i] * inv * gf[i];
             }
+            if (p.rht != nullptr)  // the group's 8 lanes hold one (group, row)
+                rht_group(f, valid ? __ldg(p.rht + (g_lo + gl) * 8 + cc) : 0u, lane);
+            pack8(f, vv);
+            if (valid)
+                *chunk = make_uint4(vv[0], vv[1], vv[2], vv[3]);
+        }
+        if (valid) {
 #pragma unroll
             for (int q = 0; q < 4; ++q)
                 part += bf16lo_f32(vv[q]) + bf16hi_f32(vv[q]);
@@ -346,7 +412,7 @@ __device__ __forceinline__ void x_put_chunk(uint8_t* buf, int x_rs, float* xs, i
 template <int NB = 4>
 __device__ __forceinline__ void x_direct_raw(const uint16_t* x, int64_t ldx, int K, const uint16_t* gamma, float eps,
                                              int x_rs, uint8_t* buf, int Mrows, float* xs, float* ss_part, int cw,
-                                             int lane, int nwarps, int bar_id)
+                                             int lane, int nwarps, int bar_id, const uint8_t* rht = nullptr)
 {
     const int groups = K / kGroup;
     const int nch = groups * 8;  // 8-column chunks per row
@@ -405,11 +471,16 @@ __device__ __forceinline__ void x_direct_raw(const uint16_t* x, int64_t ldx, int
                 const int c = c0 + j * 32 + lane;
                 const uint32_t xv[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
                 const uint32_t gg[4] = {gv[j].x, gv[j].y, gv[j].z, gv[j].w};
-                uint32_t vv[4];
+                float f[8], gf[8];
+                unpack8(xv, f);
+                unpack8(gg, gf);
 #pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    vv[q] = f32x2_to_bf16x2(bf16lo_f32(xv[q]) * inv * bf16lo_f32(gg[q]),
-                                            bf16hi_f32(xv[q]) * inv * bf16hi_f32(gg[q]));
+                for (int i = 0; i < 8; ++i)
+                    f[i] = f[i] * inv * gf[i];
+                if (rht != nullptr)  // lanes 8k .. 8k + 7 hold one group
+                    rht_group(f, c < c1 ? __ldg(rht + c) : 0u, lane);
+                uint32_t vv[4];
+                pack8(f, vv);
                 x_put_chunk(buf, x_rs, xs, m, c, c < c1, vv);
             }
         }
@@ -433,7 +504,13 @@ __device__ __forceinline__ void x_direct_raw(const uint16_t* x, int64_t ldx, int
                 for (int m = 0; m < kMaxM; ++m) {
                     if (m >= Mrows)  // uniform
                         break;
-                    const uint32_t vv[4] = {v[m].x, v[m].y, v[m].z, v[m].w};
+                    uint32_t vv[4] = {v[m].x, v[m].y, v[m].z, v[m].w};
+                    if (rht != nullptr) {  // lanes 8k .. 8k + 7 hold one group
+                        float f[8];
+                        unpack8(vv, f);
+                        rht_group(f, c < nch ? __ldg(rht + c) : 0u, lane);
+                        pack8(f, vv);
+                    }
                     x_put_chunk(buf, x_rs, xs, m, c, c < nch, vv);
                 }
             }
@@ -445,7 +522,7 @@ __device__ __forceinline__ void x_direct_raw(const uint16_t* x, int64_t ldx, int
 __device__ __forceinline__ void x_direct(const QProjParams& p, uint8_t* buf, int Mrows, float* xs, float* ss_part,
                                          int cw, int lane, int nwarps, int bar_id)
 {
-    x_direct_raw<4>(p.x, p.ldx, p.K, p.gamma, p.eps, p.x_rs, buf, Mrows, xs, ss_part, cw, lane, nwarps, bar_id);
+    x_direct_raw<4>(p.x, p.ldx, p.K, p.gamma, p.eps, p.x_rs, buf, Mrows, xs, ss_part, cw, lane, nwarps, bar_id, p.rht);
 }
 
 // The B fragments (xa: k blocks 0, 1; xb: k blocks 2, 3) of group g_rel of a buffer,

@@ -79,6 +79,8 @@ _SIGS = {
     "tf_qlinear_workspace_bytes": (SZ, [ctypes.POINTER(tf_qweight), I64]),
     "tf_qlinear_run": (ctypes.c_int, [ctypes.POINTER(tf_qweight), P, I64, I64, P, ctypes.c_float, P, P,
                                       ctypes.c_int, P, SZ, ctypes.c_uint, P]),
+    "tf_qlinear_run_rht": (ctypes.c_int, [ctypes.POINTER(tf_qweight), P, I64, I64, P, P, ctypes.c_float, P, P,
+                                          ctypes.c_int, P, ctypes.c_size_t, ctypes.c_uint, P]),
     "tf_qlinear_run_noalloc": (ctypes.c_int, [ctypes.POINTER(tf_qweight), P, I64, I64, P, ctypes.c_float, P, P,
                                               ctypes.c_int, ctypes.c_uint, P]),
     "tf_qmlp_gateup_workspace_bytes": (SZ, [ctypes.POINTER(tf_qweight), ctypes.POINTER(tf_qweight), I64]),
@@ -271,6 +273,23 @@ def tf_qlinear_run(w: QWeight, x: torch.Tensor, gamma=None, eps: float = 1e-6, r
         ws = workspace(tf_qlinear_workspace_bytes(w, M), x.device)
     _check(lib().tf_qlinear_run(ctypes.byref(w.desc), _ptr(x), ldx, M, _ptr(gamma), eps, _ptr(residual), _ptr(out),
                                 ydt, _ptr(ws), ws.numel(), flags, _stream(stream)))
+    return out
+
+
+def tf_qlinear_run_rht(w: QWeight, x: torch.Tensor, signs: torch.Tensor, gamma=None, eps: float = 1e-6,
+                       residual=None, out=None, out_dtype=torch.bfloat16, ws=None, flags: int = 0,
+                       stream=None) -> torch.Tensor:
+    """tf_qlinear_run with the input Hadamard transform: signs is a device uint8 [K / 8] bit vector."""
+    M, ldx = _rows(x)
+    if signs.dtype != torch.uint8 or not signs.is_cuda or signs.numel() * 8 < w.K:
+        raise ValueError("signs must be a device uint8 tensor of K / 8 bytes")
+    if out is None:
+        out = torch.empty((M, w.N), dtype=out_dtype, device=x.device)
+    ydt = TF_DTYPE_F32 if out.dtype == torch.float32 else TF_DTYPE_BF16
+    if ws is None:
+        ws = workspace(tf_qlinear_workspace_bytes(w, M), x.device)
+    _check(lib().tf_qlinear_run_rht(ctypes.byref(w.desc), _ptr(x), ldx, M, _ptr(signs), _ptr(gamma), eps,
+                                    _ptr(residual), _ptr(out), ydt, _ptr(ws), ws.numel(), flags, _stream(stream)))
     return out
 
 

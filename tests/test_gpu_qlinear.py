@@ -393,3 +393,58 @@ def test_streaming_schedule_matches_oracle(T, warps, chunk, M, K, N, bits, norm)
     y_ref = y_ref + oracle.bf16_to_f64(res_h)
     tol = tol_linear(ad) + (2.0 ** -8 * np.abs(y_ref) if norm else 0.0)
     assert_close(host_f64(y), y_ref, tol, f"streaming W={warps} CH={chunk}")
+
+
+@pytest.mark.parametrize("mode", [-1, 1, 2, 3, 4, 5])
+@pytest.mark.parametrize("M,K,N,bits,norm", [
+    (1, 1024, 3072, 4, False),
+    (8, 1024, 3072, 4, True),
+    (3, 2048, 1000, 8, False),
+    (8, 12800, 2560, 4, False),  # K split: every split rotates its own groups
+    (2, 1024, 18992, 4, True),
+])
+def test_rht_projection_matches_oracle(T, mode, M, K, N, bits, norm):
+    # tf_qlinear_run_rht: the input Hadamard transform folded into every staging path
+    # (planner's choice, lock-step teams, warp workers, light teams with register-loaded
+    # and with bulk-copied activations, streaming), after the RMSNorm when there is one
+    rng = np.random.default_rng(600 + M + K + N + bits + mode)
+    x = synth.activations(rng, M, K)
+    w = synth.quant_weights(rng, N, K, bits)
+    signs = synth.rht_signs(rng, K)
+    gamma_h = synth.gamma(rng, K) if norm else None
+    res_h = synth.activations(rng, M, N)
+    qw = pack(T, w)
+    T.tune_set(T.TF_TUNE_MODE, mode)
+    try:
+        ws = T.workspace(T.tf_qlinear_workspace_bytes(qw, 8))
+        y = T.tf_qlinear_run_rht(qw, dev_bf16(x), torch.from_numpy(signs).cuda(),
+                                 gamma=dev_bf16(gamma_h) if norm else None, eps=1e-6, residual=dev_bf16(res_h),
+                                 ws=ws, out_dtype=torch.float32)
+        torch.cuda.synchronize()
+    finally:
+        T.tune_set(T.TF_TUNE_MODE, -1)
+    assert T.tf_workspace_status(ws) == T.TF_OK
+    xd = oracle.bf16_to_f64(x)
+    if norm:
+        xd = oracle.rmsnorm(xd, oracle.bf16_to_f64(gamma_h), 1e-6)
+    y_ref, ad = oracle.qlinear(oracle.rht(xd, signs), w)
+    y_ref = y_ref + oracle.bf16_to_f64(res_h)
+    assert_close(host_f64(y), y_ref, tol_linear(ad), f"rht, mode {mode}")
+
+
+def test_rht_with_zero_signs_is_not_the_plain_projection(T):
+    # control: with the transform the result differs from the plain call on the same
+    # inputs (the rotation is applied), and equals it after rotating x on the host
+    rng = np.random.default_rng(650)
+    M, K, N = 2, 1024, 512
+    x = synth.activations(rng, M, K)
+    w = synth.quant_weights(rng, N, K, 4)
+    signs = np.zeros(K // 8, np.uint8)
+    qw = pack(T, w)
+    y_rht = host_f64(T.tf_qlinear_run_rht(qw, dev_bf16(x), torch.from_numpy(signs).cuda(), out_dtype=torch.float32))
+    y_plain = host_f64(T.tf_qlinear_run(qw, dev_bf16(x), out_dtype=torch.float32))
+    assert np.abs(y_rht - y_plain).max() > 1.0
+    xr = synth.f32_to_bf16_bits(oracle.rht(oracle.bf16_to_f64(x), signs).astype(np.float32))
+    y_host = host_f64(T.tf_qlinear_run(qw, dev_bf16(xr), out_dtype=torch.float32))
+    _, ad = oracle.qlinear(oracle.rht(oracle.bf16_to_f64(x), signs), w)
+    assert_close(y_rht, y_host, tol_linear(ad), "rht on device vs on host")
