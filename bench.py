@@ -7,10 +7,11 @@ whose total is more than four times the L2 cache, so every call streams its
 weights from HBM. Steps are captured once into a CUDA graph and replayed.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl tfq|reference]
-                  [--workload gateup|proj|wide|readout|step|moe4|moe8]
+                  [--workload gateup|proj|wide|wide_rht|readout|step|moe4|moe8]
 
 The other workloads: proj (one K=1024, N=3072 projection, M=1), wide (K=12800,
-N=2560, one M=1 and one M=8 call), readout (the decoder's RMSNorm + tied readout,
+N=2560, one M=1 and one M=8 call), wide_rht (the same with the input Hadamard
+transform folded into the activation staging), readout (the decoder's RMSNorm + tied readout,
 K=1024, N=151936, one M=1 and one M=8 call), step (the whole per-token weight
 stream of a 28-layer dense decoder, one M=1 and one M=8 step), moe4 / moe8 (the
 MoE layer, M=8, one call).
@@ -238,18 +239,20 @@ class Workload:
         sub = {"wq": w["wq"][:rows], "scales": w["scales"][:rows], "biases": w["biases"][:rows],
                "N": rows, "K": w["K"], "bits": w["bits"]}
         x = oracle.bf16_to_f64(self.sample_x)
+        signs = getattr(self, "host_signs", None)  # input Hadamard transform, when the workload has one
         per = rows * w["K"] * (w["bits"] / 8 + 4 / 64)
         done, t0, reps = 0, time.perf_counter(), 0
         while True:
             for M in self.step_ms:
-                oracle.qlinear(x[:M], sub)
+                oracle.qlinear(x[:M] if signs is None else oracle.rht(x[:M], signs), sub)
                 done += per
             reps += 1
             if time.perf_counter() - t0 >= seconds:
                 break
         el = time.perf_counter() - t0
         ms = " and ".join(f"M={M}" for M in self.step_ms)
-        return done, el, (f"{reps} x ({ms} calls of the projection oracle on the first {rows} rows of {what}, "
+        what_oracle = "projection" if signs is None else "input Hadamard transform + projection"
+        return done, el, (f"{reps} x ({ms} calls of the {what_oracle} oracle on the first {rows} rows of {what}, "
                           f"K={w['K']}), single thread")
 
 
@@ -333,8 +336,15 @@ class Proj(Workload):
     def __init__(self, T, torch, l2_bytes, kind: str):
         super().__init__(T, torch)
         from skinny_gemm_bit_gb300 import synth
-        self.gamma, self.eps = None, 1e-6
-        if kind == "wide":
+        self.gamma, self.eps, self.signs = None, 1e-6, None
+        if kind == "wide_rht":
+            cfg = synth.wide_verify(seed=2, M=8)
+            self.name, self.step_ms = "wide_rht", (1, 8)
+            self.kernel_key = "qproj_b4_k12800_n2560_rht"
+            self.kernel = "qproj_warp_kernel<4> (warp workers, K split, input Hadamard transform at staging)"
+            self.host_signs = synth.rht_signs(np.random.default_rng(2), 12800)
+            self.signs = torch.from_numpy(self.host_signs).cuda()
+        elif kind == "wide":
             cfg = synth.wide_verify(seed=2, M=8)
             self.name, self.step_ms = "wide", (1, 8)
             self.kernel_key, self.kernel = "qproj_b4_k12800_n2560", "qproj_kernel<4> (long-row team schedule, K split)"
@@ -347,7 +357,7 @@ class Proj(Workload):
             cfg = synth.single_projection(seed=0, M=1)
             self.name, self.step_ms = "proj", (1,)
             self.kernel_key, self.kernel = "qproj_b4_k1024_n3072", "qproj_kernel<4> (light team schedule)"
-        wide = kind == "wide"
+        wide = kind in ("wide", "wide_rht")
         w0 = _pack(T, cfg["w"])
         self.w = cfg["w"]
         self.K, self.N, self.bits = w0.K, w0.N, 4
@@ -360,11 +370,15 @@ class Proj(Workload):
         self.ws = T.workspace(T.tf_qlinear_workspace_bytes(w0, 8))
         self.sample_x = x8
         ms = " and ".join(f"M={M}" for M in self.step_ms)
-        what = {"wide": "wide verify", "readout": "RMSNorm + tied readout", "proj": "single"}[kind]
+        what = {"wide": "wide verify", "wide_rht": "input Hadamard transform + wide verify",
+                "readout": "RMSNorm + tied readout", "proj": "single"}[kind]
         self.desc = f"{what} 4-bit group-64 projection, K={self.K}, N={self.N}; one {ms} call per step"
 
     def call(self, i, M, flags, x, out):
-        self.T.tf_qlinear_run(self.copies[i], x, gamma=self.gamma, eps=self.eps, out=out, ws=self.ws, flags=flags)
+        if self.signs is not None:
+            self.T.tf_qlinear_run_rht(self.copies[i], x, self.signs, out=out, ws=self.ws, flags=flags)
+        else:
+            self.T.tf_qlinear_run(self.copies[i], x, gamma=self.gamma, eps=self.eps, out=out, ws=self.ws, flags=flags)
 
     def sample_matrix(self):
         return self.w, 256 if self.K <= 2048 else 32, "the weight matrix"
@@ -453,13 +467,13 @@ class MoE(Workload):
         return e0, 128, "expert 0's gate matrix"
 
 
-WORKLOADS = ("gateup", "proj", "wide", "readout", "step", "moe4", "moe8")
+WORKLOADS = ("gateup", "proj", "wide", "wide_rht", "readout", "step", "moe4", "moe8")
 
 
 def make_workload(name, T, torch, l2_bytes):
     if name == "gateup":
         return GateUp(T, torch, l2_bytes)
-    if name in ("proj", "wide", "readout"):
+    if name in ("proj", "wide", "wide_rht", "readout"):
         return Proj(T, torch, l2_bytes, kind=name)
     if name == "step":
         return Step(T, torch, l2_bytes)
@@ -627,14 +641,17 @@ class _HostOnly:
             self.K, self.N, self.ms, self.bits = 1024, 3072, [1, 8], 4
         else:
             self.impl = Workload.__new__(Workload)
-            if name in ("proj", "wide", "readout"):
+            if name in ("proj", "wide", "wide_rht", "readout"):
                 cfg = {"wide": lambda: synth.wide_verify(seed=2, M=8),
+                       "wide_rht": lambda: synth.wide_verify(seed=2, M=8),
                        "readout": lambda: synth.single_projection(seed=3, M=8, K=1024, N=151936),
                        "proj": lambda: synth.single_projection(seed=0, M=1)}[name]()
                 w = cfg["w"]
                 x8 = cfg["x"] if cfg["x"].shape[0] == 8 else np.repeat(cfg["x"], 8, axis=0)
                 rows, what = (256, "the weight matrix") if w["K"] <= 2048 else (32, "the weight matrix")
                 self.impl.step_ms = (1,) if name == "proj" else (1, 8)
+                if name == "wide_rht":
+                    self.impl.host_signs = synth.rht_signs(np.random.default_rng(2), 12800)
                 self.K, self.N, self.bits = w["K"], w["N"], 4
                 self.desc = f"{name} 4-bit group-64 projection, K={w['K']}, N={w['N']}"
             elif name == "step":
@@ -705,7 +722,8 @@ def main():
     ap.add_argument("--ref-step-seconds", type=float, default=0.2)
     ap.add_argument("--workload", default="gateup", choices=WORKLOADS,
                     help="gateup (default): fused RMSNorm + gate/up, K=1024, N=2x3072, M=1 and 8; proj: "
-                         "K=1024, N=3072, M=1; wide: K=12800, N=2560, M=1 and 8; readout: RMSNorm + tied "
+                         "K=1024, N=3072, M=1; wide: K=12800, N=2560, M=1 and 8; wide_rht: the same with the "
+                         "input Hadamard transform; readout: RMSNorm + tied "
                          "readout, K=1024, N=151936, M=1 and 8; step: 28-layer decoder weight stream, M=1 and 8; "
                          "moe4 / moe8: MoE layer, M=8")
     args = ap.parse_args()
