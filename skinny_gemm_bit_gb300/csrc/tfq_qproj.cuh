@@ -339,35 +339,20 @@ __device__ __forceinline__ void x_prepare(const QProjParams& p, uint8_t* buf, co
         const int gl = pi / Mrows, m = pi - gl * Mrows;
         const bool valid = pi < ng * Mrows;
         float part = 0.f;
-        uint4* chunk = reinterpret_cast<uint4*>(buf + (valid ? m : 0) * p.x_rs + (valid ? g_lo - xg0 + gl : 0) * 128) + cc;
-        uint32_t vv[4] = {0u, 0u, 0u, 0u};
         if (valid) {
-            const uint4 v = *chunk;
-            vv[0] = v.x;
-            vv[1] = v.y;
-            vv[2] = v.z;
-            vv[3] = v.w;
-        }
-        if (norm || p.rht != nullptr) {  // warp-uniform
-            float f[8];
-            unpack8(vv, f);
-            if (norm && valid) {
+            uint4* chunk = reinterpret_cast<uint4*>(buf + m * p.x_rs + (g_lo - xg0 + gl) * 128) + cc;
+            uint4 v = *chunk;
+            uint32_t vv[4] = {v.x, v.y, v.z, v.w};
+            if (norm) {
                 const uint4 gv = *reinterpret_cast<const uint4*>(gbuf + ((g_lo + gl) * kGroup + cc * 8) * 2);
                 const uint32_t gg[4] = {gv.x, gv.y, gv.z, gv.w};
-                float gf[8];
-                unpack8(gg, gf);
                 const float inv = inv_rms[m];
 #pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    f[i] = f[i] * inv * gf[i];
-            }
-            if (p.rht != nullptr)  // the group's 8 lanes hold one (group, row)
-                rht_group(f, valid ? __ldg(p.rht + (g_lo + gl) * 8 + cc) : 0u, lane);
-            pack8(f, vv);
-            if (valid)
+                for (int q = 0; q < 4; ++q)
+                    vv[q] = f32x2_to_bf16x2(bf16lo_f32(vv[q]) * inv * bf16lo_f32(gg[q]),
+                                            bf16hi_f32(vv[q]) * inv * bf16hi_f32(gg[q]));
                 *chunk = make_uint4(vv[0], vv[1], vv[2], vv[3]);
-        }
-        if (valid) {
+            }
 #pragma unroll
             for (int q = 0; q < 4; ++q)
                 part += bf16lo_f32(vv[q]) + bf16hi_f32(vv[q]);
@@ -412,7 +397,7 @@ __device__ __forceinline__ void x_put_chunk(uint8_t* buf, int x_rs, float* xs, i
 template <int NB = 4>
 __device__ __forceinline__ void x_direct_raw(const uint16_t* x, int64_t ldx, int K, const uint16_t* gamma, float eps,
                                              int x_rs, uint8_t* buf, int Mrows, float* xs, float* ss_part, int cw,
-                                             int lane, int nwarps, int bar_id, const uint8_t* rht = nullptr)
+                                             int lane, int nwarps, int bar_id)
 {
     const int groups = K / kGroup;
     const int nch = groups * 8;  // 8-column chunks per row
@@ -420,68 +405,45 @@ __device__ __forceinline__ void x_direct_raw(const uint16_t* x, int64_t ldx, int
         if ((i & 7) >= Mrows)
             xs[i] = 0.f;
     if (gamma != nullptr) {
-        // WPR warps per row (the largest power of two with WPR * Mrows <= nwarps), each
-        // normalising a run of cpw chunks (a multiple of 8; at most 4 a lane since K <=
-        // 1024). With one warp a row, the warp's own sum of squares is the row's; with
-        // several, the WPR warp sums are added in warp order after a CTA barrier.
-        int WPR = 1;
-        while (2 * WPR * Mrows <= nwarps)
-            WPR *= 2;
-        const int m = cw / WPR, sub = cw - m * WPR;
-        const int cpw = ((nch + WPR - 1) / WPR + 7) / 8 * 8;
-        const bool row_warp = m < Mrows;  // warp-uniform
-        const int c0 = sub * cpw, c1 = min(nch, c0 + cpw);
+        // one warp a row, four chunks a lane (K <= 1024): the row's sum of squares is a
+        // warp reduction in an order that does not depend on how many rows are staged,
+        // so a row normalises to the same bits alone or in a block of eight
+        const int nch_row = nch;
         const uint4* g4 = reinterpret_cast<const uint4*>(gamma);
-        const uint4* x4 = reinterpret_cast<const uint4*>(x + (int64_t)(row_warp ? m : 0) * ldx);
-        uint4 v[4], gv[4];
-        float sq[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int c = c0 + j * 32 + lane;
-            const bool ok = row_warp && c < c1;
-            v[j] = ok ? __ldcg(x4 + c) : make_uint4(0u, 0u, 0u, 0u);
-            gv[j] = ok ? __ldg(g4 + c) : make_uint4(0u, 0u, 0u, 0u);
-        }
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const uint32_t vv[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const float a = bf16lo_f32(vv[q]), b = bf16hi_f32(vv[q]);
-                sq[q] = fmaf(b, b, fmaf(a, a, sq[q]));
-            }
-        }
-        const float wsum = warp_sum((sq[0] + sq[1]) + (sq[2] + sq[3]));
-        float ss = wsum;
-        if (WPR > 1) {  // uniform
-            if (row_warp && lane == 0)
-                ss_part[cw] = wsum;
-            named_bar_sync(bar_id, nwarps * 32);
-            ss = 0.f;
-            if (row_warp)
-                for (int w = 0; w < WPR; ++w)
-                    ss += ss_part[m * WPR + w];
-        }
-        if (row_warp) {
-            const float inv = rsqrtf(ss / (float)K + eps);
+        for (int m = cw; m < Mrows; m += nwarps) {
+            const uint4* x4 = reinterpret_cast<const uint4*>(x + (int64_t)m * ldx);
+            uint4 v[4], gv[4];
+            float sq[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                if (c0 + j * 32 >= c1)  // warp-uniform
+                const int c = j * 32 + lane;
+                const bool ok = c < nch_row;
+                v[j] = ok ? __ldcg(x4 + c) : make_uint4(0u, 0u, 0u, 0u);
+                gv[j] = ok ? __ldg(g4 + c) : make_uint4(0u, 0u, 0u, 0u);
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const uint32_t vv[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const float a = bf16lo_f32(vv[q]), b = bf16hi_f32(vv[q]);
+                    sq[q] = fmaf(b, b, fmaf(a, a, sq[q]));
+                }
+            }
+            const float inv = rsqrtf(warp_sum((sq[0] + sq[1]) + (sq[2] + sq[3])) / (float)K + eps);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                if (j * 32 >= nch_row)  // warp-uniform
                     break;
-                const int c = c0 + j * 32 + lane;
+                const int c = j * 32 + lane;
                 const uint32_t xv[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
                 const uint32_t gg[4] = {gv[j].x, gv[j].y, gv[j].z, gv[j].w};
-                float f[8], gf[8];
-                unpack8(xv, f);
-                unpack8(gg, gf);
-#pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    f[i] = f[i] * inv * gf[i];
-                if (rht != nullptr)  // lanes 8k .. 8k + 7 hold one group
-                    rht_group(f, c < c1 ? __ldg(rht + c) : 0u, lane);
                 uint32_t vv[4];
-                pack8(f, vv);
-                x_put_chunk(buf, x_rs, xs, m, c, c < c1, vv);
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    vv[q] = f32x2_to_bf16x2(bf16lo_f32(xv[q]) * inv * bf16lo_f32(gg[q]),
+                                            bf16hi_f32(xv[q]) * inv * bf16hi_f32(gg[q]));
+                x_put_chunk(buf, x_rs, xs, m, c, c < nch_row, vv);
             }
         }
     } else {
@@ -504,13 +466,7 @@ __device__ __forceinline__ void x_direct_raw(const uint16_t* x, int64_t ldx, int
                 for (int m = 0; m < kMaxM; ++m) {
                     if (m >= Mrows)  // uniform
                         break;
-                    uint32_t vv[4] = {v[m].x, v[m].y, v[m].z, v[m].w};
-                    if (rht != nullptr) {  // lanes 8k .. 8k + 7 hold one group
-                        float f[8];
-                        unpack8(vv, f);
-                        rht_group(f, c < nch ? __ldg(rht + c) : 0u, lane);
-                        pack8(f, vv);
-                    }
+                    const uint32_t vv[4] = {v[m].x, v[m].y, v[m].z, v[m].w};
                     x_put_chunk(buf, x_rs, xs, m, c, c < nch, vv);
                 }
             }
@@ -522,7 +478,48 @@ __device__ __forceinline__ void x_direct_raw(const uint16_t* x, int64_t ldx, int
 __device__ __forceinline__ void x_direct(const QProjParams& p, uint8_t* buf, int Mrows, float* xs, float* ss_part,
                                          int cw, int lane, int nwarps, int bar_id)
 {
-    x_direct_raw<4>(p.x, p.ldx, p.K, p.gamma, p.eps, p.x_rs, buf, Mrows, xs, ss_part, cw, lane, nwarps, bar_id, p.rht);
+    x_direct_raw<4>(p.x, p.ldx, p.K, p.gamma, p.eps, p.x_rs, buf, Mrows, xs, ss_part, cw, lane, nwarps, bar_id);
+}
+
+// Input Hadamard transform of a staged buffer, in place: groups [0, ng) of rows
+// [0, Mrows) (the buffer's group gl is group g_abs0 + gl of K), then their group sums
+// again; 8 lanes a (group, row), four a warp at a time. Runs between the staging and
+// the tile loop, so the staging code carries none of it; ends with a barrier.
+__device__ __forceinline__ void x_rht(uint8_t* buf, int x_rs, float* xs, int Mrows, int g_abs0, int ng,
+                                     const uint8_t* rht, int cw, int lane, int nwarps, int bar_id)
+{
+    const int cc = lane & 7;
+    for (int base = cw * 4; base < ng * Mrows; base += nwarps * 4) {
+        const int pi = base + (lane >> 3);
+        const bool valid = pi < ng * Mrows;
+        const int gl = valid ? pi / Mrows : 0, m = valid ? pi - gl * Mrows : 0;
+        uint4* chunk = reinterpret_cast<uint4*>(buf + m * x_rs + gl * 128) + cc;
+        uint32_t vv[4] = {0u, 0u, 0u, 0u};
+        if (valid) {
+            const uint4 v = *chunk;
+            vv[0] = v.x;
+            vv[1] = v.y;
+            vv[2] = v.z;
+            vv[3] = v.w;
+        }
+        float f[8];
+        unpack8(vv, f);
+        rht_group(f, valid ? __ldg(rht + (g_abs0 + gl) * 8 + cc) : 0u, lane);
+        pack8(f, vv);
+        float part = 0.f;
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            part += bf16lo_f32(vv[q]) + bf16hi_f32(vv[q]);
+        part += __shfl_xor_sync(0xffffffffu, part, 4);
+        part += __shfl_xor_sync(0xffffffffu, part, 2);
+        part += __shfl_xor_sync(0xffffffffu, part, 1);
+        if (valid) {
+            *chunk = make_uint4(vv[0], vv[1], vv[2], vv[3]);
+            if (cc == 0)
+                xs[gl * kMaxM + m] = part;
+        }
+    }
+    named_bar_sync(bar_id, nwarps * 32);
 }
 
 // The B fragments (xa: k blocks 0, 1; xb: k blocks 2, 3) of group g_rel of a buffer,
@@ -927,6 +924,8 @@ __global__ void __launch_bounds__((NWT + 1) * 32, NWT == 8 ? 2 : 1) qproj_kernel
                 Mrows = slot_ec[first.x].y;
             if (!MOE && p.x_direct) {  // unsplit plain rows: no bulk copy, no wait
                 x_direct(p, xraw, Mrows, xsum, red, cw, lane, NWT, kBarConsumers);
+                if (!MOE && p.rht != nullptr)
+                    x_rht(xraw, p.x_rs, xsum, Mrows, 0, p.groups, p.rht, cw, lane, NWT, kBarConsumers);
             } else {
                 if (threadIdx.x < kMaxM)
                     rowsel[threadIdx.x] = MOE ? slot_rows[first.x * kMaxM + threadIdx.x] : (int)threadIdx.x;
@@ -944,6 +943,9 @@ __global__ void __launch_bounds__((NWT + 1) * 32, NWT == 8 ? 2 : 1) qproj_kernel
                 alive = __all_sync(0xffffffffu, ok);
                 x_prepare(p, xraw, smem + p.gamma_off, Mrows, xg0, first.y * p.Gs, p.Gs, xsum, inv_rms, cw, lane, NWT,
                           kBarConsumers);
+                if (!MOE && p.rht != nullptr)  // the split's groups, where the buffer holds them
+                    x_rht(xraw + (first.y * p.Gs - xg0) * 128, p.x_rs, xsum, Mrows, first.y * p.Gs, p.Gs, p.rht, cw,
+                          lane, NWT, kBarConsumers);
             }
             cur_p = first.x;
             cur_s = first.y;
@@ -1353,6 +1355,12 @@ __global__ void __launch_bounds__(kThreads, 1) qproj_warp_kernel(const __grid_co
               kConsumerWarps, kBarConsumers);
     if (two)
         x_prepare(p, xb1, nullptr, M1, xg0_1, xg0_1, p.Gs, xs1, inv1, cw, lane, kConsumerWarps, kBarConsumers);
+    if (!MOE && p.rht != nullptr) {  // input Hadamard transform of the staged rows
+        x_rht(xb0, p.x_rs, xs0, M0, norm ? 0 : xg0_0, norm ? p.groups : p.Gs, p.rht, cw, lane, kConsumerWarps,
+              kBarConsumers);
+        if (two)
+            x_rht(xb1, p.x_rs, xs1, M1, xg0_1, p.Gs, p.rht, cw, lane, kConsumerWarps, kBarConsumers);
+    }
     // fp16 activations when every staged value converts exactly and, for 4-bit codes,
     // |x| < 4096 (the group sums above are of the same values): the codes then unpack
     // with fewer instructions. The decision is the CTA's, from one snapshot.

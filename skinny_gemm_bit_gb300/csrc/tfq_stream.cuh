@@ -201,8 +201,9 @@ __global__ void __launch_bounds__((W + 2) * 32, W <= 8 ? 2 : 1) qstream_kernel(c
     for (int i = (w * 32 + lane) * 16 + p.M * p.x_rs; i < kMaxM * p.x_rs; i += W * 32 * 16)
         *reinterpret_cast<uint4*>(xbuf + i) = make_uint4(0u, 0u, 0u, 0u);
     x_direct_raw<4>(p.x + (norm ? 0 : (int64_t)s * p.Gs * kGroup), p.ldx, norm ? p.K : p.Gs * kGroup, p.gamma, p.eps,
-                    p.x_rs, xbuf, p.M, xs, ss_part, w, lane, W, kStreamBarX,
-                    p.rht == nullptr ? nullptr : p.rht + (norm ? 0 : s * p.Gs * (kGroup / 8)));
+                    p.x_rs, xbuf, p.M, xs, ss_part, w, lane, W, kStreamBarX);
+    if (p.rht != nullptr)  // input Hadamard transform of the staged slice
+        x_rht(xbuf, p.x_rs, xs, p.M, norm ? 0 : s * p.Gs, norm ? p.groups : p.Gs, p.rht, w, lane, W, kStreamBarX);
 
     bool alive = true;
     int cur = 0;  // row block (relative to rb0) the accumulators belong to

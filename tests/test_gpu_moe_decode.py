@@ -132,6 +132,24 @@ def test_decoder_small(T, M, per_projection):
         T.tune_set(T.TF_TUNE_CHAIN, -1)
 
 
+@pytest.mark.parametrize("per_projection", [False, True])
+def test_decoder_step_rows_are_independent_bit_exact(T, per_projection):
+    # a row's logits are the same bits whether it runs alone or in a block of 8 (the
+    # property a greedy verify block needs: its predictions equal one-row decoding)
+    cfg = synth.decoder(seed=37, n_layers=2, d_model=1024, d_ff=1024, n_q_heads=4, n_kv_heads=2, head_dim=128,
+                        vocab=4096, M=8)
+    dec = _pack_decoder(T, cfg)
+    x = dev_bf16(cfg["x"])
+    T.tune_set(T.TF_TUNE_CHAIN, 1 if per_projection else 2)
+    try:
+        y8 = T.tf_decode_step_run(dec, x)
+        for m in range(8):
+            y1 = T.tf_decode_step_run(dec, x[m:m + 1])
+            assert torch.equal(y1[0], y8[m]), m
+    finally:
+        T.tune_set(T.TF_TUNE_CHAIN, -1)
+
+
 def test_decoder_step_leaves_workspace_clean_and_repeats_exactly(T):
     cfg = synth.decoder(seed=39, n_layers=2, d_model=256, d_ff=384, n_q_heads=4, n_kv_heads=2, head_dim=64,
                         vocab=1000, M=4)
