@@ -7,14 +7,16 @@ whose total is more than four times the L2 cache, so every call streams its
 weights from HBM. Steps are captured once into a CUDA graph and replayed.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl tfq|reference]
-                  [--workload gateup|proj|wide|wide_rht|readout|step|moe4|moe8]
+                  [--workload gateup|proj|wide|wide_rht|readout|step|moe4|moe8|verify]
 
 The other workloads: proj (one K=1024, N=3072 projection, M=1), wide (K=12800,
 N=2560, one M=1 and one M=8 call), wide_rht (the same with the input Hadamard
 transform folded into the activation staging), readout (the decoder's RMSNorm + tied readout,
 K=1024, N=151936, one M=1 and one M=8 call), step (the whole per-token weight
 stream of a 28-layer dense decoder, one M=1 and one M=8 step), moe4 / moe8 (the
-MoE layer, M=8, one call).
+MoE layer, M=8, one call), verify (greedy generation of 64 tokens on that decoder
+with prompt-lookup drafts verified up to 8 rows a step; host-driven, timed end to
+end, against plain one-token decoding).
 
 value      effective weight GB/s: algorithmic weight bytes (codes + scales +
            biases) of all calls / device time of the timed region.
@@ -467,7 +469,7 @@ class MoE(Workload):
         return e0, 128, "expert 0's gate matrix"
 
 
-WORKLOADS = ("gateup", "proj", "wide", "wide_rht", "readout", "step", "moe4", "moe8")
+WORKLOADS = ("gateup", "proj", "wide", "wide_rht", "readout", "step", "moe4", "moe8", "verify")
 
 
 def make_workload(name, T, torch, l2_bytes):
@@ -621,6 +623,90 @@ def run_tfq(args):
         pg.destroy_process_group()
 
 
+def run_verify(args):
+    """Greedy generation with the M = 8 verify block on the 28-layer decoder: a host-driven
+    loop (one synchronisation a step), timed end to end with CUDA events around whole
+    generations, against plain one-token decoding on the same prompt."""
+    import torch
+    world, rank, local, pg = dist_setup()
+    torch.cuda.set_device(local)
+    import __graft_entry__
+    __graft_entry__.build()
+    from skinny_gemm_bit_gb300 import tfq as T
+    wl = Step(T, torch, 0)  # the full-size decoder; its descriptor and weights
+    dec = wl.dec
+    n_new = 64
+    start = int(np.random.default_rng(5).integers(0, dec.readout.N))
+    ws = T.workspace(T.tf_generate_workspace_bytes(dec))
+    cont, _, _ = T.tf_generate_greedy(dec, [start], n_new, max_draft=0, ws=ws)
+    prompt = [start] + cont[: 3 * n_new // 4] + [start]  # holds most of the continuation
+    K, W = args.steps, args.warmup
+    K = max(1, min(K, 20))  # a generation is ~20-40 ms: 20 of them time well within the budget
+
+    def timed(max_draft):
+        for _ in range(W):
+            T.tf_generate_greedy(dec, prompt, n_new, max_draft=max_draft, ws=ws)
+        torch.cuda.synchronize()
+        barrier(pg)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        steps = acc = 0
+        for _ in range(K):
+            toks, st, ac = T.tf_generate_greedy(dec, prompt, n_new, max_draft=max_draft, ws=ws)
+            steps, acc = steps + st, acc + ac
+        e1.record()
+        torch.cuda.synchronize()
+        barrier(pg)
+        return max_over_ranks(e0.elapsed_time(e1), pg, f"cuda:{local}"), steps, acc, toks
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    ms, steps, acc, toks = timed(7)
+    clocks = sampler.stop()
+    ms_plain, steps_plain, _, toks_plain = timed(0)
+    if rank != 0:
+        if pg is not None:
+            pg.destroy_process_group()
+        return
+    assert toks == toks_plain, "the verify block changed the generated tokens"
+    peak, peak_kind = measured_peaks()
+    step_bytes = dec.weight_bytes()
+    value = world * step_bytes * steps / (ms * 1e-3) / 1e9
+    us_step = ms * 1e3 / steps
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": W,
+        "ms_per_step": round(ms / K, 6), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic (seeded random 4-bit weights; prompt from the model's own greedy output)",
+        "config": {"workload": (f"greedy generation of {n_new} tokens with prompt-lookup drafts and an up-to-8-row "
+                                f"verify block, 28-layer dense decoder d_model 1024, tied readout 151936; a bench step "
+                                f"is one generation"),
+                   "name": "verify", "tokens_per_generation": n_new, "prompt_len": len(prompt),
+                   "decoder_steps_per_generation": round(steps / K, 2),
+                   "drafts_kept_per_generation": round(acc / K, 2),
+                   "tokens_per_s": round(world * n_new * K / (ms * 1e-3), 1),
+                   "plain_tokens_per_s": round(world * n_new * K / (ms_plain * 1e-3), 1),
+                   "plain_decoder_steps_per_generation": round(steps_plain / K, 2),
+                   "us_per_decoder_step": round(us_step, 2),
+                   "graph": "none (host-driven loop; one synchronisation per decoder step)",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "pct_of_hbm_measured": round(100 * value / world / peak, 2),
+        "roofline": {"bound": "hbm", "achieved": round(step_bytes / (us_step * 1e-6) / 1e9, 1), "peak": peak,
+                     "unit": "GB/s", "frac": round(step_bytes / (us_step * 1e-6) / 1e9 / peak, 4),
+                     "traffic": recorded_traffic("step_b4_l28_d1024"), "peak_source": peak_kind,
+                     "kernel": "decoder step at M = 1 + drafts, embedding and argmax kernels",
+                     "bytes_per_launch": step_bytes, "launch_us": round(us_step, 3)},
+        "cpu_baseline": cpu_baseline(wl, args.cpu_seconds),
+        "e2e": {"value": round(value, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": int(4 * (steps + acc) / K), "d2h_bytes_per_step": int(36 * steps / K),
+                "note": "the loop is host-driven: value is already end to end"},
+        "gpu_launches": steps * (Step.launches_per_call + 2),
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+    if pg is not None:
+        pg.destroy_process_group()
+
+
 def cpu_baseline(wl, seconds):
     done, el, desc = wl.oracle_sample(seconds)
     return {"value": round(done / el / 1e9, 6), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": desc}
@@ -654,7 +740,7 @@ class _HostOnly:
                     self.impl.host_signs = synth.rht_signs(np.random.default_rng(2), 12800)
                 self.K, self.N, self.bits = w["K"], w["N"], 4
                 self.desc = f"{name} 4-bit group-64 projection, K={w['K']}, N={w['N']}"
-            elif name == "step":
+            elif name in ("step", "verify"):
                 cfg = synth.decoder(M=8, n_layers=1)  # layer 0 of the same seeded model
                 w, x8, rows, what = cfg["layers"][0]["qkv"], cfg["x"], 256, "layer 0's QKV matrix"
                 self.impl.step_ms = (1, 8)
@@ -725,12 +811,15 @@ def main():
                          "K=1024, N=3072, M=1; wide: K=12800, N=2560, M=1 and 8; wide_rht: the same with the "
                          "input Hadamard transform; readout: RMSNorm + tied "
                          "readout, K=1024, N=151936, M=1 and 8; step: 28-layer decoder weight stream, M=1 and 8; "
-                         "moe4 / moe8: MoE layer, M=8")
+                         "moe4 / moe8: MoE layer, M=8; verify: greedy generation with prompt-lookup drafts and "
+                         "an up-to-8-row verify block on the 28-layer decoder")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload == "verify":
+        run_verify(args)
     else:
         run_tfq(args)
 

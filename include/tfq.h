@@ -26,7 +26,7 @@
  *     Calls are asynchronous on it: they enqueue kernels and return. They never
  *     allocate, synchronise or print, so a sequence of calls can be captured
  *     into a CUDA graph. Exceptions (they synchronise): tf_qweight_check,
- *     tf_workspace_status.
+ *     tf_workspace_status, tf_generate_greedy (a host-driven loop).
  *   - Workspaces: each run entry point has a *_workspace_bytes query. The
  *     workspace must be zero-filled once before its first use (every call
  *     leaves it in the state it found it); one workspace must not be used by
@@ -288,6 +288,66 @@ size_t tf_decode_step_workspace_bytes(const tf_decoder_desc* d, int64_t M);
 size_t tf_decode_step_debug_elems(const tf_decoder_desc* d, int64_t M);
 int tf_decode_step_run(const tf_decoder_desc* d, const uint16_t* x, int64_t M, uint16_t* logits,
                        void* ws, size_t ws_bytes, uint16_t* debug, unsigned flags, void* stream);
+
+/* ---------------------------------------------------------------- verify block */
+
+/*
+ * Greedy decoding with an M = 8 verify block (Husky page, the passage before "Flash
+ * draft model and candidate selection": when the last tokens just generated also
+ * occur in the prompt, the 7 tokens that followed them there are proposed; one
+ * step verifies the block, the matching drafts are kept, and the text is the one
+ * plain decoding gives). The pages fix no n-gram length or choice among several
+ * occurrences; here the longest suffix of at most max_ngram tokens is tried first,
+ * and its first occurrence in the prompt with a token after it is used.
+ */
+
+/*
+ * idx[m] = the lowest index n of the largest value of row m of the bf16 array
+ * v[M][ld] over n < N (-0 equals +0; NaN is never chosen unless the row holds
+ * nothing else). v device, idx device int32 [M]; 1 <= M <= 65535, N < 2^31.
+ */
+int tf_argmax_rows(const uint16_t* v, int64_t ld, int64_t M, int64_t N, int32_t* idx, void* stream);
+
+/*
+ * x[m][k] = bf16(s q + b) of row ids[m] of a packed matrix (batch 1), k < K:
+ * the dequantised row, rounded to nearest even (exact whenever |b| / |s| < 2^15).
+ * ids device int32 [M], x device bf16 [M][K]. ws: 256 zeroed, 256-aligned bytes; an
+ * id outside [0, N) records TF_E_INVALID_ARG there (tf_workspace_status) and gives
+ * a zero row. Used as the token embedding of a tied readout.
+ */
+int tf_embed_rows(const tf_qweight* w, const int32_t* ids, int64_t M, uint16_t* x, void* ws, size_t ws_bytes,
+                  void* stream);
+
+/*
+ * The draft of one step (host only, no GPU): for ng = min(max_ngram, tail_len)
+ * down to 1, the first occurrence prompt[p, p + ng) of the tail's last ng tokens
+ * with p + ng < prompt_len; the draft is prompt[p + ng, p + ng + cnt), cnt =
+ * min(max_draft, prompt_len - p - ng). Returns cnt (0: no occurrence), -1 on bad
+ * arguments. prompt, tail, draft: host int32.
+ */
+int64_t tf_draft_prompt_lookup(const int32_t* prompt, int64_t prompt_len, const int32_t* tail, int64_t tail_len,
+                               int max_ngram, int max_draft, int32_t* draft);
+
+/*
+ * Greedy generation with the decoder step (tf_decode_step_run) and the tied readout
+ * as token embedding: each step embeds the block [last token, draft...] (1 + cnt <=
+ * 8 rows, cnt = tf_draft_prompt_lookup(prompt, ..., max_draft) capped by the tokens
+ * still wanted), runs one decoder step at M = 1 + cnt, takes the per-row argmax,
+ * keeps the drafts that match the predictions in order and appends the prediction
+ * after the last kept one. max_draft = 0 is plain one-token decoding; any max_draft
+ * gives the same tokens (a row's logits do not depend on the rows beside it).
+ *   prompt      host int32 [prompt_len], tokens in [0, vocab), prompt_len >= 1
+ *   max_new     tokens to generate; out host int32 [max_new]
+ *   max_draft   0..7; max_ngram 1..64
+ *   n_out       host: tokens written (= max_new); n_steps, n_accepted (host, may be
+ *               NULL): decoder steps run, drafts kept
+ *   ws          tf_generate_workspace_bytes(d) bytes, 256-aligned, zeroed once
+ * Synchronises `stream` once per step (the predictions decide the next block).
+ */
+size_t tf_generate_workspace_bytes(const tf_decoder_desc* d);
+int tf_generate_greedy(const tf_decoder_desc* d, const int32_t* prompt, int64_t prompt_len, int64_t max_new,
+                       int max_draft, int max_ngram, int32_t* out, int64_t* n_out, int64_t* n_steps,
+                       int64_t* n_accepted, void* ws, size_t ws_bytes, void* stream);
 
 /* ---------------------------------------------------------------- diagnostics */
 

@@ -173,5 +173,7 @@ cudaError_t launch_moe_route(const float* logits, int M, int E, int top_k, int32
 cudaError_t launch_moe_combine(const MoeMeta* meta, const float* o, int M, int top_k, int H, uint16_t* y,
                                cudaStream_t stream);
 cudaError_t launch_timeout_probe(int* status, uint64_t limit_ns, cudaStream_t stream);
+cudaError_t launch_embed_rows(const uint8_t* packed, int64_t N, int64_t K, int bits, const int32_t* ids, int64_t M,
+                              uint16_t* x, int64_t ldx, int* status, cudaStream_t stream);
 
 }  // namespace tfq

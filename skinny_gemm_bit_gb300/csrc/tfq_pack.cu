@@ -16,6 +16,8 @@
 // 8-bit: words 2kb + jp of lane l; byte bp is row gi + 8*(bp&1), column
 //   2t + 8*jp + (bp>>1). The low nibbles of a word give registers 2jp, 2jp+1 of
 //   the "low" fragment, the high nibbles the same registers of the "high" one.
+#include <cuda_bf16.h>
+
 #include "tfq_internal.h"
 
 namespace tfq {
@@ -152,6 +154,42 @@ __global__ void unpack_scales_kernel(const uint8_t* __restrict__ packed, int64_t
     }
 }
 
+// Rows of a packed matrix (batch 0) dequantised to bf16: x[m][k] = bf16(s q + b) of
+// row ids[m], column k, rounded to nearest even (s q + b is exact in fp32 whenever
+// |b| / |s| < 2^15, so the rounding is that of the exact value). An id outside
+// [0, N) records TF_E_INVALID_ARG in *status and gives a zero row.
+__global__ void embed_rows_kernel(const uint8_t* __restrict__ packed, int64_t N, int64_t K, int bits,
+                                  const int32_t* __restrict__ ids, int64_t M, uint16_t* __restrict__ x, int64_t ldx,
+                                  int* status)
+{
+    const int64_t G = K / kGroup;
+    const int tile_words = tile_bytes_for(bits) / 4;
+    const int q_words = tile_q_bytes_for(bits) / 4;
+    const uint32_t* tiles = reinterpret_cast<const uint32_t*>(packed + TF_PACK_HEADER_BYTES);
+    for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < M * K;
+         idx += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t m = idx / K, k = idx - m * K;
+        const int64_t row = __ldg(ids + m);
+        float v = 0.f;
+        if (row < 0 || row >= N) {
+            if (k == 0)
+                atomicCAS(status, 0, TF_E_INVALID_ARG);
+        } else {
+            const int rr = (int)(row % kRowsPerBlock);
+            int w, sh;
+            locate(rr, (int)(k % kGroup), bits, w, sh);
+            const uint32_t* tw = tiles + ((row / kRowsPerBlock) * G + k / kGroup) * tile_words;
+            const uint32_t q = (__ldg(tw + w) >> sh) & ((1u << bits) - 1u);
+            const int shs = (rr >> 3) * 16;
+            const float sc = __uint_as_float(((__ldg(tw + q_words + 2 * (rr & 7)) >> shs) & 0xFFFFu) << 16);
+            const float bi = __uint_as_float(((__ldg(tw + q_words + 2 * (rr & 7) + 1) >> shs) & 0xFFFFu) << 16);
+            v = fmaf(sc, (float)q, bi);
+        }
+        const __nv_bfloat16 h = __float2bfloat16_rn(v);
+        x[m * ldx + k] = *reinterpret_cast<const uint16_t*>(&h);
+    }
+}
+
 int grid_for(int64_t total, int threads)
 {
     int64_t blocks = (total + threads - 1) / threads;
@@ -191,6 +229,13 @@ cudaError_t launch_unpack(const uint8_t* packed, int64_t batch, int64_t N, int64
         return e;
     const int64_t groups = batch * N * (K / kGroup);
     unpack_scales_kernel<<<grid_for(groups, 256), 256, 0, stream>>>(packed, batch, N, K, bits, s, b);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_embed_rows(const uint8_t* packed, int64_t N, int64_t K, int bits, const int32_t* ids, int64_t M,
+                              uint16_t* x, int64_t ldx, int* status, cudaStream_t stream)
+{
+    embed_rows_kernel<<<grid_for(M * K, 256), 256, 0, stream>>>(packed, N, K, bits, ids, M, x, ldx, status);
     return cudaGetLastError();
 }
 

@@ -11,6 +11,7 @@ from __future__ import annotations
 import ctypes
 import os
 
+import numpy as np
 import torch
 
 from . import build as _build
@@ -93,6 +94,12 @@ _SIGS = {
     "tf_decode_step_debug_elems": (SZ, [ctypes.POINTER(tf_decoder_desc), I64]),
     "tf_decode_step_run": (ctypes.c_int, [ctypes.POINTER(tf_decoder_desc), P, I64, P, P, SZ, P, ctypes.c_uint,
                                           P]),
+    "tf_argmax_rows": (ctypes.c_int, [P, I64, I64, I64, P, P]),
+    "tf_embed_rows": (ctypes.c_int, [ctypes.POINTER(tf_qweight), P, I64, P, P, ctypes.c_size_t, P]),
+    "tf_draft_prompt_lookup": (I64, [P, I64, P, I64, ctypes.c_int, ctypes.c_int, P]),
+    "tf_generate_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(tf_decoder_desc)]),
+    "tf_generate_greedy": (ctypes.c_int, [ctypes.POINTER(tf_decoder_desc), P, I64, I64, ctypes.c_int, ctypes.c_int, P,
+                                          P, P, P, P, ctypes.c_size_t, P]),
     "tf_workspace_status": (ctypes.c_int, [P, P]),
     "tf_selftest_wait_timeout": (ctypes.c_int, [P, ctypes.c_uint64, P]),
     "tf_tune_set": (ctypes.c_int, [ctypes.c_int, ctypes.c_int]),
@@ -392,3 +399,52 @@ def tf_decode_step_run(dec: Decoder, x: torch.Tensor, out=None, ws=None, debug=N
     _check(lib().tf_decode_step_run(ctypes.byref(dec.desc), _ptr(x), M, _ptr(out), _ptr(ws), ws.numel(),
                                     _ptr(debug), flags, _stream(stream)))
     return out
+
+
+# ---------------------------------------------------------------- verify block
+
+def tf_argmax_rows(v: torch.Tensor, stream=None) -> torch.Tensor:
+    """idx[m] = lowest index of the largest value of row m of a bf16 [M, N] tensor."""
+    M, N = v.shape
+    idx = torch.empty(M, dtype=torch.int32, device=v.device)
+    _check(lib().tf_argmax_rows(_ptr(v), v.stride(0), M, N, _ptr(idx), _stream(stream)))
+    return idx
+
+
+def tf_embed_rows(w: QWeight, ids: torch.Tensor, ws=None, stream=None) -> torch.Tensor:
+    """bf16 [M, K]: the dequantised rows ids (device int32 [M]) of a packed matrix."""
+    M = ids.numel()
+    out = torch.empty((M, w.K), dtype=torch.bfloat16, device=ids.device)
+    if ws is None:
+        ws = workspace(256, ids.device)
+    _check(lib().tf_embed_rows(ctypes.byref(w.desc), _ptr(ids), M, _ptr(out), _ptr(ws), ws.numel(), _stream(stream)))
+    return out
+
+
+def tf_draft_prompt_lookup(prompt, tail, max_ngram: int = 3, max_draft: int = 7):
+    """The draft (list of ints) the prompt proposes after the tail (host only)."""
+    p = np.ascontiguousarray(prompt, dtype=np.int32)
+    t = np.ascontiguousarray(tail, dtype=np.int32)
+    d = np.zeros(max(1, max_draft), dtype=np.int32)
+    n = lib().tf_draft_prompt_lookup(p.ctypes.data, p.size, t.ctypes.data, t.size, max_ngram, max_draft, d.ctypes.data)
+    if n < 0:
+        raise TfqError(TF_E_INVALID_ARG, "tf_draft_prompt_lookup: bad arguments")
+    return d[:n].tolist()
+
+
+def tf_generate_workspace_bytes(dec: Decoder) -> int:
+    return lib().tf_generate_workspace_bytes(ctypes.byref(dec.desc))
+
+
+def tf_generate_greedy(dec: Decoder, prompt, max_new: int, max_draft: int = 7, max_ngram: int = 3, ws=None,
+                       stream=None):
+    """(tokens, steps, drafts kept) of greedy generation with a verify block."""
+    p = np.ascontiguousarray(prompt, dtype=np.int32)
+    out = np.zeros(max(1, max_new), dtype=np.int32)
+    n_out, n_steps, n_acc = ctypes.c_int64(0), ctypes.c_int64(0), ctypes.c_int64(0)
+    if ws is None:
+        ws = workspace(tf_generate_workspace_bytes(dec))
+    _check(lib().tf_generate_greedy(ctypes.byref(dec.desc), p.ctypes.data, p.size, max_new, max_draft, max_ngram,
+                                    out.ctypes.data, ctypes.byref(n_out), ctypes.byref(n_steps), ctypes.byref(n_acc),
+                                    _ptr(ws), ws.numel(), _stream(stream)))
+    return out[:n_out.value].tolist(), n_steps.value, n_acc.value
