@@ -23,7 +23,11 @@ pages describe:
 
 Weights are passed as dicts with keys ``wq`` (uint32 [N, K*bits/32]),
 ``scales`` / ``biases`` (uint16 bf16 bits [N, K/64]), ``N``, ``K``, ``bits``.
-Stacks of experts use a leading batch axis on the three arrays.
+Stacks of experts use a leading batch axis on the three arrays. NVFP4 weights
+(TensorFold page, "qualified" model table: NVFP4 checkpoints; format as read in
+``oracle.c``) are dicts with ``code`` = "nvfp4", ``codes`` (uint8 [N, K/2], even
+column in the low nibble), ``scales`` (uint8 E4M3 [N, K/16]), ``gscale`` (fp32),
+``N``, ``K``; ``dequant``, ``qlinear`` and ``gateup`` accept them.
 """
 from __future__ import annotations
 
@@ -75,6 +79,15 @@ def _load():
     lib.oracle_topk_softmax.restype = I
     lib.oracle_rht.argtypes = [P, I64, I64, P, I64, P]
     lib.oracle_rht.restype = I
+    D = ctypes.c_double
+    lib.oracle_e2m1.argtypes = [I]
+    lib.oracle_e2m1.restype = D
+    lib.oracle_e4m3.argtypes = [I]
+    lib.oracle_e4m3.restype = D
+    lib.oracle_nvfp4_dequant.argtypes = [P, P, D, I64, I64, P]
+    lib.oracle_nvfp4_dequant.restype = I
+    lib.oracle_nvfp4_qlinear.argtypes = [P, I64, I64, P, P, D, I64, I64, P, P]
+    lib.oracle_nvfp4_qlinear.restype = I
     _lib = lib
     return lib
 
@@ -107,8 +120,35 @@ def unpack(wq, N: int, K: int, bits: int) -> np.ndarray:
     return q
 
 
+def is_nvfp4(w: dict) -> bool:
+    return w.get("code") == "nvfp4"
+
+
+def e2m1(code: int) -> float:
+    """Value of a 4-bit E2M1 code (NVFP4 element)."""
+    return _load().oracle_e2m1(int(code))
+
+
+def e4m3(code: int) -> float:
+    """Value of an E4M3 byte (NVFP4 block scale); NaN for S.1111.111."""
+    return _load().oracle_e4m3(int(code))
+
+
+def nvfp4_dequant(w: dict) -> np.ndarray:
+    """w[n][k] = gscale * e4m3(scales[n][k/16]) * e2m1(q[n][k]) in float64 [N, K]."""
+    N, K = w["N"], w["K"]
+    out = np.empty((N, K), dtype=np.float64)
+    rc = _load().oracle_nvfp4_dequant(_ptr(_c(w["codes"], np.uint8)), _ptr(_c(w["scales"], np.uint8)),
+                                      float(np.float32(w["gscale"])), N, K, _ptr(out))
+    if rc:
+        raise ValueError("oracle_nvfp4_dequant rejected the weights")
+    return out
+
+
 def dequant(w: dict) -> np.ndarray:
-    """w[n][k] = scale*q + bias in float64 [N, K]."""
+    """w[n][k] = scale*q + bias in float64 [N, K] (NVFP4 weights: ``nvfp4_dequant``)."""
+    if is_nvfp4(w):
+        return nvfp4_dequant(w)
     N, K, bits = w["N"], w["K"], w["bits"]
     out = np.empty((N, K), dtype=np.float64)
     rc = _load().oracle_dequant(_ptr(_c(w["wq"], np.uint32)), _ptr(_c(w["scales"], np.uint16)),
@@ -130,6 +170,13 @@ def qlinear(x, w: dict):
     N = w["N"]
     y = np.empty((M, N), dtype=np.float64)
     ad = np.empty((M, N), dtype=np.float64)
+    if is_nvfp4(w):
+        rc = _load().oracle_nvfp4_qlinear(_ptr(x), K, M, _ptr(_c(w["codes"], np.uint8)),
+                                          _ptr(_c(w["scales"], np.uint8)), float(np.float32(w["gscale"])),
+                                          N, K, _ptr(y), _ptr(ad))
+        if rc:
+            raise ValueError("oracle_nvfp4_qlinear rejected the weights")
+        return y, ad
     rc = _load().oracle_qlinear(_ptr(x), K, M, _ptr(_c(w["wq"], np.uint32)),
                                 _ptr(_c(w["scales"], np.uint16)), _ptr(_c(w["biases"], np.uint16)),
                                 N, K, w["bits"], GROUP, _ptr(y), _ptr(ad))

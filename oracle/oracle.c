@@ -33,6 +33,10 @@
  *     consecutive columns (64 = one quantisation group), xr = H (d .* x) /
  *     sqrt(block) with H the Sylvester-ordered Walsh-Hadamard matrix and d a
  *     +-1 vector stored as bits, least-significant first, bit set = -1.
+ *   - NVFP4 weights (TensorFold page, "qualified" model table: NVFP4 checkpoints):
+ *     the pages give no layout; the reading is NVIDIA's published NVFP4 format
+ *     (E2M1 codes, an E4M3 scale per 16 K elements, an fp32 scale per matrix),
+ *     weights only, spelled out above oracle_e2m1 below.
  *
  * Parity pins for every function live in tests/test_oracle_pins.py.
  */
@@ -239,5 +243,81 @@ int oracle_rht(const double *x, int64_t M, int64_t K, const uint8_t *signs, int6
                 v[j] *= scale;
         }
     }
+    return 0;
+}
+
+/* ---------------------------------------------------------------- NVFP4 weight code
+ *
+ * The TensorFold page lists NVFP4 checkpoints among the weight formats it serves but
+ * gives no layout. The reading used is NVIDIA's published NVFP4 format, weights only
+ * (activations stay bf16, as for every other code here):
+ *   - element: 4-bit E2M1, bit 3 sign, bits 2-1 exponent (bias 1), bit 0 mantissa;
+ *     exponent 0 is subnormal (0 or 0.5);
+ *   - block scale: one E4M3 byte per 16 consecutive K elements, bit 7 sign, bits
+ *     6-3 exponent (bias 7), bits 2-0 mantissa, exponent 0 subnormal, S.1111.111
+ *     NaN, no infinities;
+ *   - one fp32 scale per matrix: w[n][k] = global * e4m3(scale[n][k/16]) * e2m1(q[n][k]);
+ *   - codes two per byte along K, the even column in the low nibble. */
+
+double oracle_e2m1(int code)
+{
+    const int sign = (code >> 3) & 1, e = (code >> 1) & 3, m = code & 1;
+    const double v = e == 0 ? 0.5 * m : ldexp(1.0 + 0.5 * m, e - 1);
+    return sign ? -v : v;
+}
+
+double oracle_e4m3(int code)
+{
+    const int sign = (code >> 7) & 1, e = (code >> 3) & 15, m = code & 7;
+    double v;
+    if (e == 15 && m == 7)
+        v = NAN;
+    else if (e == 0)
+        v = ldexp(m / 8.0, -6);
+    else
+        v = ldexp(1.0 + m / 8.0, e - 7);
+    return sign ? -v : v;
+}
+
+/* w[n][k] in double, [N][K]. codes uint8 [N][K/2], scales uint8 [N][K/16]. */
+int oracle_nvfp4_dequant(const uint8_t *codes, const uint8_t *scales, double global, int64_t N, int64_t K,
+                         double *w)
+{
+    if (K <= 0 || K % 16 != 0)
+        return 1;
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t k = 0; k < K; ++k) {
+            const uint8_t byte = codes[n * (K / 2) + k / 2];
+            const int q = (k % 2) ? byte >> 4 : byte & 15;
+            w[n * K + k] = global * oracle_e4m3(scales[n * (K / 16) + k / 16]) * oracle_e2m1(q);
+        }
+    return 0;
+}
+
+/* y[m][n] = sum_k x[m][k] * w[n][k] over NVFP4 weights, one dequantised row at a time
+ * (as oracle_qlinear); absdot[m][n] = sum_k |x[m][k] * w[n][k]| (may be NULL). */
+int oracle_nvfp4_qlinear(const double *x, int64_t ldx, int64_t M, const uint8_t *codes, const uint8_t *scales,
+                         double global, int64_t N, int64_t K, double *y, double *absdot)
+{
+    if (K <= 0 || K % 16 != 0)
+        return 1;
+    double *wrow = (double *)malloc((size_t)K * sizeof(double));
+    if (!wrow)
+        return 2;
+    for (int64_t n = 0; n < N; ++n) {
+        oracle_nvfp4_dequant(codes + n * (K / 2), scales + n * (K / 16), global, 1, K, wrow);
+        for (int64_t m = 0; m < M; ++m) {
+            double acc = 0.0, acc_abs = 0.0;
+            for (int64_t k = 0; k < K; ++k) {
+                const double p = x[m * ldx + k] * wrow[k];
+                acc += p;
+                acc_abs += fabs(p);
+            }
+            y[m * N + n] = acc;
+            if (absdot)
+                absdot[m * N + n] = acc_abs;
+        }
+    }
+    free(wrow);
     return 0;
 }

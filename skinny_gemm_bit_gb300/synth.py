@@ -16,6 +16,11 @@ Recipes (numpy ``default_rng`` / PCG64, draws in the order written here):
   to bf16; bias = -2^(bits-1) * scale + N(0, 0.002), formed in fp32 from the
   bf16 scale, then rounded to bf16;
 * RMSNorm gamma ~ N(1, 0.1) in bf16; router logits ~ N(0, 1) in fp32.
+* NVFP4 weights: code bytes uniform in [0, 255] (two E2M1 codes each, every code
+  equally likely, -0 included); block-scale bytes positive E4M3 with exponent field
+  uniform in [4, 11] and mantissa uniform in [0, 7] (0.125 .. 15), one block in 64
+  replaced by an edge byte (0x00 zero, 0x01 smallest subnormal, 0x07 largest
+  subnormal, 0x7E largest normal, 448); global scale 0.004 (fp32).
 """
 from __future__ import annotations
 
@@ -91,6 +96,21 @@ def quant_weights(rng, N: int, K: int, bits: int = 4, batch: int | None = None) 
     b32 = np.float32(-(2 ** (bits - 1))) * bf16_bits_to_f32(scales) + noise
     biases = f32_to_bf16_bits(b32)
     return {"wq": wq, "scales": scales, "biases": biases, "N": N, "K": K, "bits": bits}
+
+
+def nvfp4_weights(rng, N: int, K: int) -> dict:
+    """Random NVFP4 weights: codes uint8 [N, K/2] (even column in the low nibble),
+    E4M3 block scales uint8 [N, K/16], fp32 global scale."""
+    if K % GROUP:
+        raise ValueError("K must be a multiple of 64")
+    codes = rng.integers(0, 256, size=(N, K // 2), dtype=np.uint8)
+    e = rng.integers(4, 12, size=(N, K // 16), dtype=np.uint8)
+    m = rng.integers(0, 8, size=(N, K // 16), dtype=np.uint8)
+    scales = (e << 3) | m
+    edge = rng.integers(0, 64, size=(N, K // 16)) == 0
+    pick = np.array([0x00, 0x01, 0x07, 0x7E], dtype=np.uint8)[rng.integers(0, 4, size=(N, K // 16))]
+    scales = np.where(edge, pick, scales).astype(np.uint8)
+    return {"code": "nvfp4", "codes": codes, "scales": scales, "gscale": np.float32(0.004), "N": N, "K": K}
 
 
 def concat_rows(*ws) -> dict:

@@ -365,3 +365,81 @@ def test_rht_single_column_block_flips_signs_only():
 def test_rht_rejects_a_block_that_is_not_a_power_of_two():
     with pytest.raises(ValueError):
         oracle.rht(np.zeros((1, 96)), np.zeros(12, np.uint8), block=48)
+
+
+# ---------------------------------------------------------------- NVFP4 weight code
+
+# FP4 E2M1 magnitudes as tabulated in the OCP Microscaling Formats specification
+# (v1.0, element data types): codes 0..7 in order; codes 8..15 are their negatives.
+E2M1_MAGNITUDES = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+
+
+def _torch_e4m3(byte_values):
+    torch = pytest.importorskip("torch")
+    b = torch.from_numpy(np.ascontiguousarray(byte_values, dtype=np.uint8))
+    return b.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+
+
+def test_e4m3_matches_the_library_float8_for_every_byte():
+    lib = _torch_e4m3(np.arange(256))
+    mine = np.array([oracle.e4m3(c) for c in range(256)])
+    np.testing.assert_array_equal(np.isnan(mine), np.isnan(lib))
+    assert np.isnan(mine).sum() == 2  # S.1111.111 only; no infinities
+    ok = ~np.isnan(lib)
+    np.testing.assert_array_equal(mine[ok], lib[ok])
+    np.testing.assert_array_equal(np.signbit(mine[ok]), np.signbit(lib[ok]))
+
+
+def test_e2m1_is_the_published_fp4_grid():
+    vals = [oracle.e2m1(c) for c in range(16)]
+    assert vals[:8] == E2M1_MAGNITUDES
+    assert [-v for v in vals[8:]] == E2M1_MAGNITUDES
+    assert math.copysign(1.0, vals[8]) == -1.0  # code 8 is -0
+
+
+def _nvfp4(codes, scales, gscale, N, K):
+    return {"code": "nvfp4", "codes": np.asarray(codes, np.uint8), "scales": np.asarray(scales, np.uint8),
+            "gscale": np.float32(gscale), "N": N, "K": K}
+
+
+def test_nvfp4_dequant_low_nibble_first_and_16_column_blocks():
+    N, K = 2, 64
+    codes = np.zeros((N, K // 2), np.uint8)
+    scales = np.zeros((N, K // 16), np.uint8)
+    codes[1, 5] = 0x21   # columns 10 (low nibble: 0.5) and 11 (high nibble: 1.0)
+    codes[1, 8] = 0xF3   # columns 16 (1.5) and 17 (-6)
+    codes[0, 31] = 0x70  # columns 62 (0) and 63 (6)
+    scales[1, 0] = 0x38  # 1.0 for columns 0..15
+    scales[1, 1] = 0x40  # 2.0 for columns 16..31
+    scales[0, 3] = 0x01  # 2^-9 for columns 48..63
+    w = oracle.dequant(_nvfp4(codes, scales, 0.25, N, K))
+    expect = np.zeros((N, K))
+    expect[1, 10], expect[1, 11] = 0.25 * 0.5, 0.25 * 1.0
+    expect[1, 16], expect[1, 17] = 0.25 * 2.0 * 1.5, -0.25 * 2.0 * 6.0
+    expect[0, 63] = 0.25 * 2.0 ** -9 * 6.0
+    np.testing.assert_array_equal(w, expect)
+
+
+def test_nvfp4_projection_equals_a_matmul_of_an_independent_dequantisation():
+    rng = np.random.default_rng(77)
+    N, K, M = 40, 192, 3
+    w = synth.nvfp4_weights(rng, N, K)
+    x = rng.standard_normal((M, K))
+    # dequantised separately: nibble split by numpy, the published E2M1 grid, the
+    # library's E4M3 conversion, scales repeated over their 16 columns
+    lo, hi = w["codes"] & 15, w["codes"] >> 4
+    q = np.stack([lo, hi], axis=-1).reshape(N, K)
+    grid = np.array(E2M1_MAGNITUDES + [-v for v in E2M1_MAGNITUDES])
+    W = float(w["gscale"]) * np.repeat(_torch_e4m3(w["scales"]), 16, axis=1) * grid[q]
+    y, ad = oracle.qlinear(x, w)
+    np.testing.assert_allclose(y, x @ W.T, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(ad, np.abs(x) @ np.abs(W).T, rtol=1e-12, atol=1e-12)
+
+
+def test_nvfp4_global_scale_scales_the_projection():
+    rng = np.random.default_rng(78)
+    w = synth.nvfp4_weights(rng, 16, 128)
+    x = rng.standard_normal((2, 128))
+    y1, _ = oracle.qlinear(x, w)
+    y2, _ = oracle.qlinear(x, dict(w, gscale=np.float32(w["gscale"]) * np.float32(8.0)))
+    np.testing.assert_array_equal(y2, 8.0 * y1)  # a power of two changes no rounding
