@@ -7,7 +7,8 @@ whose total is more than four times the L2 cache, so every call streams its
 weights from HBM. Steps are captured once into a CUDA graph and replayed.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl tfq|reference]
-                  [--workload gateup|proj|wide|wide_rht|readout|step|moe4|moe8|verify]
+                  [--workload gateup|proj|wide|wide_rht|readout|step|moe4|moe8|verify|
+                              wide_nvfp4|readout_nvfp4]
 
 The other workloads: proj (one K=1024, N=3072 projection, M=1), wide (K=12800,
 N=2560, one M=1 and one M=8 call), wide_rht (the same with the input Hadamard
@@ -16,7 +17,8 @@ K=1024, N=151936, one M=1 and one M=8 call), step (the whole per-token weight
 stream of a 28-layer dense decoder, one M=1 and one M=8 step), moe4 / moe8 (the
 MoE layer, M=8, one call), verify (greedy generation of 64 tokens on that decoder
 with prompt-lookup drafts verified up to 8 rows a step; host-driven, timed end to
-end, against plain one-token decoding).
+end, against plain one-token decoding), wide_nvfp4 / readout_nvfp4 (the wide and
+readout shapes with NVFP4 weights: E2M1 codes, an E4M3 scale per 16 columns).
 
 value      effective weight GB/s: algorithmic weight bytes (codes + scales +
            biases) of all calls / device time of the timed region.
@@ -238,11 +240,15 @@ class Workload:
         for about `seconds`; returns (weight bytes covered, seconds, description)."""
         import oracle
         w, rows, what = self.sample_matrix()
-        sub = {"wq": w["wq"][:rows], "scales": w["scales"][:rows], "biases": w["biases"][:rows],
-               "N": rows, "K": w["K"], "bits": w["bits"]}
+        if w.get("code") == "nvfp4":
+            sub = dict(w, codes=w["codes"][:rows], scales=w["scales"][:rows], N=rows)
+            per = rows * w["K"] * (4 / 8 + 1 / 16)
+        else:
+            sub = {"wq": w["wq"][:rows], "scales": w["scales"][:rows], "biases": w["biases"][:rows],
+                   "N": rows, "K": w["K"], "bits": w["bits"]}
+            per = rows * w["K"] * (w["bits"] / 8 + 4 / 64)
         x = oracle.bf16_to_f64(self.sample_x)
         signs = getattr(self, "host_signs", None)  # input Hadamard transform, when the workload has one
-        per = rows * w["K"] * (w["bits"] / 8 + 4 / 64)
         done, t0, reps = 0, time.perf_counter(), 0
         while True:
             for M in self.step_ms:
@@ -274,7 +280,24 @@ def _clone_qweight(T, qw):
 
 
 def _pack(T, w):
+    if w.get("code") == "nvfp4":
+        return T.tf_qlinear_pack_nvfp4(w["codes"], w["scales"], float(w["gscale"]))
     return T.tf_qlinear_pack(w["wq"], w["scales"], w["biases"], w["bits"])
+
+
+def _weights_word(wl):
+    return "NVFP4" if wl.name.endswith("_nvfp4") else f"{wl.bits}-bit"
+
+
+def _proj_config(kind):
+    """Seeded inputs of the single-matrix workloads (also used by the host-only reference arm)."""
+    from skinny_gemm_bit_gb300 import synth
+    return {"wide": lambda: synth.wide_verify(seed=2, M=8),
+            "wide_rht": lambda: synth.wide_verify(seed=2, M=8),
+            "readout": lambda: synth.single_projection(seed=3, M=8, K=1024, N=151936),
+            "proj": lambda: synth.single_projection(seed=0, M=1),
+            "wide_nvfp4": lambda: synth.nvfp4_projection(seed=8, M=8, K=12800, N=2560),
+            "readout_nvfp4": lambda: synth.nvfp4_projection(seed=9, M=8, K=1024, N=151936)}[kind]()
 
 
 class GateUp(Workload):
@@ -333,33 +356,39 @@ class GateUp(Workload):
 class Proj(Workload):
     """One 4-bit projection per step: K=1024, N=3072, M=1 (single projection); K=12800,
     N=2560 at M=1 and M=8 (wide verify projection); or the decoder's tied readout with
-    its RMSNorm, K=1024, N=151936, at M=1 and M=8."""
+    its RMSNorm, K=1024, N=151936, at M=1 and M=8. The *_nvfp4 kinds are the wide and
+    readout shapes with NVFP4 weights."""
 
     def __init__(self, T, torch, l2_bytes, kind: str):
         super().__init__(T, torch)
         from skinny_gemm_bit_gb300 import synth
         self.gamma, self.eps, self.signs = None, 1e-6, None
-        if kind == "wide_rht":
-            cfg = synth.wide_verify(seed=2, M=8)
+        cfg = _proj_config(kind)
+        if kind == "wide_nvfp4":
+            self.name, self.step_ms = kind, (1, 8)
+            self.kernel_key = "qproj_nvfp4_k12800_n2560"
+            self.kernel = "qproj_warp_kernel<NVFP4> (warp workers, K split in 5)"
+        elif kind == "readout_nvfp4":
+            self.name, self.step_ms = kind, (1, 8)
+            self.kernel_key, self.kernel = "qproj_nvfp4_k1024_n151936_norm", "qproj_warp_kernel<NVFP4> (warp workers)"
+            self.gamma = _dev_bf16(torch, synth.gamma(np.random.default_rng(5), 1024))
+        elif kind == "wide_rht":
             self.name, self.step_ms = "wide_rht", (1, 8)
             self.kernel_key = "qproj_b4_k12800_n2560_rht"
             self.kernel = "qproj_warp_kernel<4> (warp workers, K split, input Hadamard transform at staging)"
             self.host_signs = synth.rht_signs(np.random.default_rng(2), 12800)
             self.signs = torch.from_numpy(self.host_signs).cuda()
         elif kind == "wide":
-            cfg = synth.wide_verify(seed=2, M=8)
             self.name, self.step_ms = "wide", (1, 8)
-            self.kernel_key, self.kernel = "qproj_b4_k12800_n2560", "qproj_kernel<4> (long-row team schedule, K split)"
+            self.kernel_key = "qproj_b4_k12800_n2560"
+            self.kernel = "qproj_warp_kernel<4> (warp workers, K split in 5)"
         elif kind == "readout":
-            cfg = synth.single_projection(seed=3, M=8, K=1024, N=151936)
             self.name, self.step_ms = "readout", (1, 8)
             self.kernel_key, self.kernel = "qproj_b4_k1024_n151936_norm", "qproj_warp_kernel<4> (warp workers)"
             self.gamma = _dev_bf16(torch, synth.gamma(np.random.default_rng(5), 1024))
         else:
-            cfg = synth.single_projection(seed=0, M=1)
             self.name, self.step_ms = "proj", (1,)
             self.kernel_key, self.kernel = "qproj_b4_k1024_n3072", "qproj_kernel<4> (light team schedule)"
-        wide = kind in ("wide", "wide_rht")
         w0 = _pack(T, cfg["w"])
         self.w = cfg["w"]
         self.K, self.N, self.bits = w0.K, w0.N, 4
@@ -372,9 +401,11 @@ class Proj(Workload):
         self.ws = T.workspace(T.tf_qlinear_workspace_bytes(w0, 8))
         self.sample_x = x8
         ms = " and ".join(f"M={M}" for M in self.step_ms)
-        what = {"wide": "wide verify", "wide_rht": "input Hadamard transform + wide verify",
-                "readout": "RMSNorm + tied readout", "proj": "single"}[kind]
-        self.desc = f"{what} 4-bit group-64 projection, K={self.K}, N={self.N}; one {ms} call per step"
+        what = {"wide": "wide verify 4-bit group-64", "wide_rht": "input Hadamard transform + wide verify 4-bit group-64",
+                "readout": "RMSNorm + tied readout 4-bit group-64", "proj": "single 4-bit group-64",
+                "wide_nvfp4": "wide verify NVFP4 (E2M1, E4M3 scale per 16)",
+                "readout_nvfp4": "RMSNorm + tied readout NVFP4 (E2M1, E4M3 scale per 16)"}[kind]
+        self.desc = f"{what} projection, K={self.K}, N={self.N}; one {ms} call per step"
 
     def call(self, i, M, flags, x, out):
         if self.signs is not None:
@@ -469,13 +500,15 @@ class MoE(Workload):
         return e0, 128, "expert 0's gate matrix"
 
 
-WORKLOADS = ("gateup", "proj", "wide", "wide_rht", "readout", "step", "moe4", "moe8", "verify")
+WORKLOADS = ("gateup", "proj", "wide", "wide_rht", "readout", "step", "moe4", "moe8", "verify", "wide_nvfp4",
+             "readout_nvfp4")
+PROJ_KINDS = ("proj", "wide", "wide_rht", "readout", "wide_nvfp4", "readout_nvfp4")
 
 
 def make_workload(name, T, torch, l2_bytes):
     if name == "gateup":
         return GateUp(T, torch, l2_bytes)
-    if name in ("proj", "wide", "wide_rht", "readout"):
+    if name in PROJ_KINDS:
         return Proj(T, torch, l2_bytes, kind=name)
     if name == "step":
         return Step(T, torch, l2_bytes)
@@ -595,7 +628,7 @@ def run_tfq(args):
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": W,
         "ms_per_step": round(ms_max / K, 6), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16", "data": f"synthetic (seeded random {wl.bits}-bit weights and N(0,1) activations)",
+        "dtype": "bf16", "data": f"synthetic (seeded random {_weights_word(wl)} weights and N(0,1) activations)",
         "config": {"workload": wl.desc, "name": wl.name, "K": wl.K, "N": wl.N, "M": ms_list, "bits": wl.bits,
                    "group": 64,
                    "l2": (f"weights rotate over {wl.n_copies} copies, more than four times L2, every call reads HBM"
@@ -727,11 +760,8 @@ class _HostOnly:
             self.K, self.N, self.ms, self.bits = 1024, 3072, [1, 8], 4
         else:
             self.impl = Workload.__new__(Workload)
-            if name in ("proj", "wide", "wide_rht", "readout"):
-                cfg = {"wide": lambda: synth.wide_verify(seed=2, M=8),
-                       "wide_rht": lambda: synth.wide_verify(seed=2, M=8),
-                       "readout": lambda: synth.single_projection(seed=3, M=8, K=1024, N=151936),
-                       "proj": lambda: synth.single_projection(seed=0, M=1)}[name]()
+            if name in PROJ_KINDS:
+                cfg = _proj_config(name)
                 w = cfg["w"]
                 x8 = cfg["x"] if cfg["x"].shape[0] == 8 else np.repeat(cfg["x"], 8, axis=0)
                 rows, what = (256, "the weight matrix") if w["K"] <= 2048 else (32, "the weight matrix")
@@ -739,7 +769,8 @@ class _HostOnly:
                 if name == "wide_rht":
                     self.impl.host_signs = synth.rht_signs(np.random.default_rng(2), 12800)
                 self.K, self.N, self.bits = w["K"], w["N"], 4
-                self.desc = f"{name} 4-bit group-64 projection, K={w['K']}, N={w['N']}"
+                code = "NVFP4" if w.get("code") == "nvfp4" else "4-bit group-64"
+                self.desc = f"{name} {code} projection, K={w['K']}, N={w['N']}"
             elif name in ("step", "verify"):
                 cfg = synth.decoder(M=8, n_layers=1)  # layer 0 of the same seeded model
                 w, x8, rows, what = cfg["layers"][0]["qkv"], cfg["x"], 256, "layer 0's QKV matrix"
@@ -788,7 +819,7 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * total_s / args.steps, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": f"synthetic (seeded random {host.bits}-bit weights and N(0,1) activations)",
+        "data": f"synthetic (seeded random {_weights_word(host)} weights and N(0,1) activations)",
         "config": {"workload": host.desc, "name": host.name, "K": host.K, "N": host.N, "M": host.ms,
                    "bits": host.bits, "group": 64},
         "cpu_baseline": {"value": round(value, 6), "unit": "GB/s", "kind": "oracle", "cores": 1,
@@ -812,7 +843,8 @@ def main():
                          "input Hadamard transform; readout: RMSNorm + tied "
                          "readout, K=1024, N=151936, M=1 and 8; step: 28-layer decoder weight stream, M=1 and 8; "
                          "moe4 / moe8: MoE layer, M=8; verify: greedy generation with prompt-lookup drafts and "
-                         "an up-to-8-row verify block on the 28-layer decoder")
+                         "an up-to-8-row verify block on the 28-layer decoder; wide_nvfp4 / readout_nvfp4: the "
+                         "wide and readout shapes with NVFP4 weights")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

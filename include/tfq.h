@@ -6,7 +6,7 @@
  *
  *   y[m][n] = sum_k x[m][k] * w[n][k],   w[n][k] = scale[n][k/64] * q[n][k] + bias[n][k/64]
  *
- * over MLX affine group-quantised weights: q in [0, 2^bits), one bf16 scale and
+ * over MLX affine group-quantised weights (code TF_CODE_AFFINE): q in [0, 2^bits), one bf16 scale and
  * one bf16 bias per 64 consecutive K elements, q packed 32/bits values per
  * uint32 along K (uzu page, "Internals 1: models are assembled from
  * configuration", weight_matrix row: MLX 4/8-bit originals consumed as-is;
@@ -14,6 +14,15 @@
  * (decode) to 8 (an 8-row speculative verify block; Husky page, "Limits of
  * plain writing and how editing is accelerated": 8-token blocks are verified at
  * about 1.5x the cost of one token).
+ *
+ * A second weight code, TF_CODE_NVFP4 (tf_qlinear_pack_nvfp4), holds
+ *   w[n][k] = global_scale * e4m3(block_scale[n][k/16]) * e2m1(q[n][k])
+ * with 4-bit E2M1 codes, one E4M3 scale per 16 consecutive K elements and one
+ * fp32 scale per matrix (TensorFold page, "qualified" model table: NVFP4
+ * checkpoints; the pages give no layout, the format read here is NVIDIA's
+ * published NVFP4, weights only: activations stay bf16). tf_qlinear_run,
+ * tf_qlinear_run_rht, tf_qlinear_run_noalloc and tf_qmlp_gateup_run accept it;
+ * the MoE, decoder-step and embedding calls return TF_E_UNSUPPORTED_SHAPE.
  *
  * Conventions shared by every call:
  *   - Pointers named x, y, h, logits, residual, gamma, ws, packed and the
@@ -66,20 +75,26 @@ extern "C" {
                           while that kernel finishes. */
 
 #define TF_QWEIGHT_MAGIC 0x31515446u /* "TFQ1" */
-#define TF_PACK_VERSION 1u
+#define TF_PACK_VERSION 2u
+
+/* weight codes */
+#define TF_CODE_AFFINE 0 /* MLX affine: w = scale * q + bias, bits 4 or 8, group 64 */
+#define TF_CODE_NVFP4 1  /* NVFP4: w = global * e4m3 scale * e2m1 q, bits 4, group 16 */
 #define TF_PACK_HEADER_BYTES 256
 
 /* Host-side descriptor of a packed weight buffer, filled by tf_qlinear_pack. */
 typedef struct tf_qweight {
     uint32_t magic;        /* TF_QWEIGHT_MAGIC once filled by tf_qlinear_pack */
     uint32_t version;      /* TF_PACK_VERSION */
-    int32_t bits;          /* 4 or 8 */
-    int32_t group;         /* 64 */
+    int32_t bits;          /* 4 or 8 (NVFP4: 4) */
+    int32_t group;         /* 64 (NVFP4: 16, the K elements sharing one block scale) */
+    int32_t code;          /* TF_CODE_AFFINE or TF_CODE_NVFP4 */
+    float global_scale;    /* NVFP4: the matrix's fp32 scale; 1 for TF_CODE_AFFINE */
     int64_t batch;         /* number of matrices (experts); 1 for a plain projection */
     int64_t N;             /* output rows per matrix */
     int64_t K;             /* input columns per matrix */
     int64_t n_pad;         /* N rounded up to a multiple of 16 */
-    int64_t tile_bytes;    /* bytes of one 16-row x 64-column tile (576 for 4-bit, 1088 for 8-bit) */
+    int64_t tile_bytes;    /* bytes of one 16-row x 64-column tile (576 for 4-bit and NVFP4, 1088 for 8-bit) */
     int64_t matrix_bytes;  /* bytes of one packed matrix (tiles only) */
     const void* data;      /* device pointer: start of the packed buffer (header first) */
 } tf_qweight;
@@ -97,8 +112,8 @@ int tf_version(void);
 
 /*
  * Bytes of the packed buffer for `batch` matrices of N x K at `bits` with
- * `group`. Returns 0 for an unsupported combination (bits not 4/8, group not
- * 64, K not a multiple of 64, N < 1, batch < 1).
+ * `group` (bits 4 with group 16: the NVFP4 code). Returns 0 for an unsupported
+ * combination (not 4/64, 8/64 or 4/16, K not a multiple of 64, N < 1, batch < 1).
  */
 size_t tf_qlinear_packed_bytes(int64_t batch, int64_t N, int64_t K, int bits, int group);
 
@@ -120,9 +135,28 @@ int tf_qlinear_pack(const uint32_t* wq, const uint16_t* scales, const uint16_t* 
                     void* packed, size_t packed_bytes, tf_qweight* desc, void* stream);
 
 /*
+ * Repack NVFP4 weights into the kernels' tile order (a 16 x 64 tile is 512 bytes
+ * of codes and 64 bytes of block scales, the size of an MLX 4-bit tile).
+ *   codes         uint8 [N][K/2]: two E2M1 codes a byte along K, the even column in
+ *                 bits 0-3 (bit 3 sign, bits 2-1 exponent with bias 1, bit 0 mantissa)
+ *   block_scales  uint8 [N][K/16]: E4M3 (bit 7 sign, bits 6-3 exponent with bias 7,
+ *                 bits 2-0 mantissa, S.1111.111 NaN) for columns 16 j .. 16 j + 15
+ *   global_scale  fp32 scale of the whole matrix (finite)
+ *   packed        output, `packed_bytes` >= tf_qlinear_packed_bytes(1, N, K, 4, 16),
+ *                 16-byte aligned
+ *   desc          output host descriptor (code TF_CODE_NVFP4, bits 4, group 16, batch 1)
+ * Requirements: K % 64 == 0, N >= 1. Asynchronous on `stream` as tf_qlinear_pack.
+ */
+int tf_qlinear_pack_nvfp4(const uint8_t* codes, const uint8_t* block_scales, float global_scale,
+                          int64_t N, int64_t K, void* packed, size_t packed_bytes, tf_qweight* desc,
+                          void* stream);
+
+/*
  * Inverse of tf_qlinear_pack: write the MLX-layout arrays back out of a packed
  * buffer (same shapes as the packer's inputs). Used to prove the packing is a
- * lossless permutation.
+ * lossless permutation. For NVFP4 weights: the codes go to `wq` (the bytes of
+ * uint8 [N][K/2]), the block scales to `scales` (the bytes of uint8 [N][K/16]),
+ * and `biases` is not written (may be NULL).
  */
 int tf_qlinear_unpack_debug(const tf_qweight* w, uint32_t* wq, uint16_t* scales, uint16_t* biases,
                             void* stream);

@@ -1,6 +1,7 @@
 // Host side of the C ABI declared in tfq.h: argument validation, the launch
 // planner and the entry points. Nothing here allocates, synchronises or prints
 // (except the two documented diagnostics that read device memory back).
+#include <cmath>
 #include <cstdarg>
 #include <cstdio>
 #include <algorithm>
@@ -21,6 +22,9 @@ size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// The kernels' BITS argument for a descriptor's weight code.
+int kernel_bits(const tf_qweight* w) { return w->code == TF_CODE_NVFP4 ? kNvfp4 : w->bits; }
+
 int fail(int status, const char* fmt, ...)
 {
     va_list ap;
@@ -35,18 +39,22 @@ int cuda_fail(cudaError_t e, const char* what)
     return fail(TF_E_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }
 
-// Validate a descriptor filled by tf_qlinear_pack.
+// Validate a descriptor filled by tf_qlinear_pack or tf_qlinear_pack_nvfp4.
 int check_desc(const tf_qweight* w, const char* name)
 {
     if (w == nullptr)
         return fail(TF_E_INVALID_ARG, "%s: descriptor is NULL", name);
     if (w->magic != TF_QWEIGHT_MAGIC || w->version != TF_PACK_VERSION)
         return fail(TF_E_BAD_PACK, "%s: descriptor magic/version mismatch (not filled by tf_qlinear_pack?)", name);
-    if (w->bits != 4 && w->bits != 8)
-        return fail(TF_E_BAD_PACK, "%s: bits=%d", name, w->bits);
-    if (w->group != kGroup || w->K <= 0 || w->K % kGroup != 0 || w->N <= 0 || w->batch <= 0)
+    const bool nvfp4 = w->code == TF_CODE_NVFP4;
+    if (w->code != TF_CODE_AFFINE && !nvfp4)
+        return fail(TF_E_BAD_PACK, "%s: unknown weight code %d", name, w->code);
+    if (nvfp4 ? (w->bits != 4 || w->group != 16 || w->batch != 1 || !std::isfinite(w->global_scale))
+              : ((w->bits != 4 && w->bits != 8) || w->group != kGroup))
+        return fail(TF_E_BAD_PACK, "%s: bits=%d group=%d do not match the weight code", name, w->bits, w->group);
+    if (w->K <= 0 || w->K % kGroup != 0 || w->N <= 0 || w->batch <= 0)
         return fail(TF_E_BAD_PACK, "%s: bad shape", name);
-    if (w->n_pad != (w->N + 15) / 16 * 16 || w->tile_bytes != tile_bytes_for(w->bits) ||
+    if (w->n_pad != (w->N + 15) / 16 * 16 || w->tile_bytes != tile_bytes_for(kernel_bits(w)) ||
         w->matrix_bytes != w->n_pad / 16 * (w->K / kGroup) * w->tile_bytes)
         return fail(TF_E_BAD_PACK, "%s: inconsistent sizes", name);
     if (w->data == nullptr || !aligned(w->data, 16))
@@ -73,6 +81,16 @@ const uint8_t* tiles_of(const tf_qweight* w)
 }
 
 size_t plan_scratch(const Plan& p) { return p.ws_counters + p.ws_partials; }
+
+// For the calls whose kernels read MLX affine codes only.
+int check_affine(const tf_qweight* w, const char* name)
+{
+    int rc = check_desc(w, name);
+    if (rc == TF_OK && w->code != TF_CODE_AFFINE)
+        rc = fail(TF_E_UNSUPPORTED_SHAPE,
+                  "%s: NVFP4 weights are accepted by tf_qlinear_run(_rht/_noalloc) and tf_qmlp_gateup_run only", name);
+    return rc;
+}
 
 void fill_common(QProjParams& p, const Plan& pl, void* ws, uint8_t* scratch)
 {
@@ -216,6 +234,7 @@ Plan plan_qproj(int n_rb, int groups, int mats, int bits, int slots, int k_full,
     // warp workers over K splits of at most 40 groups, 8 workers a CTA (on GB300 this
     // measured 12.8 / 14.8 us at M = 1 / 8 for K = 12800, N = 2560, against 14.6 / 17.0
     // for lock-step teams over two splits)
+    const bool nvfp4 = bits == kNvfp4;  // warp workers only
     const bool long_plain = slots == 1 && mats == 1 && k_full == 0 && groups >= 64 && n_rb <= 2 * sms &&
                             (double)n_rb * groups * tile > 8.0 * 1024 * 1024 && g_tune[TF_TUNE_MODE] <= 0;
     int S = 1;
@@ -305,6 +324,7 @@ Plan plan_qproj(int n_rb, int groups, int mats, int bits, int slots, int k_full,
     bool light = light_ok && g_tune[TF_TUNE_MODE] <= 0;
     if (g_tune[TF_TUNE_MODE] == 3 || g_tune[TF_TUNE_MODE] == 4)
         light = light_ok;
+    light = light && !nvfp4;
     if (light) {
         pl.nw = 8;
         pl.C = (int)std::max<int64_t>(items, 1);
@@ -340,7 +360,7 @@ Plan plan_qproj(int n_rb, int groups, int mats, int bits, int slots, int k_full,
     // ---- one large matrix: streaming CTAs (selected with TF_TUNE_MODE 5; on GB300 it
     // measured no faster than the long-row teams and warp workers below: every schedule
     // is bound by the instructions per tile, ~90-110, not by the memory system)
-    if (slots == 1 && mats == 1 && g_tune[TF_TUNE_MODE] == 5) {
+    if (slots == 1 && mats == 1 && g_tune[TF_TUNE_MODE] == 5 && !nvfp4) {
         Plan sp;
         if (plan_stream(n_rb, groups, bits, k_full, sms, sp))
             return sp;
@@ -351,22 +371,31 @@ Plan plan_qproj(int n_rb, int groups, int mats, int bits, int slots, int k_full,
     // MoE layers (many problems, each with its own activation rows): 8 workers a CTA
     // measured fastest; otherwise all 16
     const int nw_default = slots > 1 || long_plain ? 8 : kConsumerWarps;
-    const int nw = g_tune[TF_TUNE_WARPS] > 0 ? std::min(g_tune[TF_TUNE_WARPS], kConsumerWarps) : nw_default;
-    const int64_t W = (int64_t)sms * nw;
+    int nw = g_tune[TF_TUNE_WARPS] > 0 ? std::min(g_tune[TF_TUNE_WARPS], kConsumerWarps) : nw_default;
+    int64_t W = (int64_t)sms * nw;
     const int64_t upc_max_all = (U + pl.C - 1) / pl.C;  // units per CTA with every slot active
     bool warp_mode = (long_plain || (!long_rows && U >= 4 * W)) && upc_max_all <= per_ps;
     if (g_tune[TF_TUNE_MODE] > 0)
         warp_mode = g_tune[TF_TUNE_MODE] == 2 && upc_max_all <= per_ps;
-    if (warp_mode) {
-        // the activation buffers (two unless a single problem and split, or an RMSNorm)
-        // and two ring slots per worker must fit, else lock-step teams
+    if (nvfp4)
+        warp_mode = upc_max_all <= per_ps;
+    // the activation buffers (two unless a single problem and split, or an RMSNorm)
+    // and two ring slots per worker must fit, else lock-step teams (NVFP4: fewer workers)
+    auto warp_fits = [&](int nw_) {
         const bool norm_rows = k_full > 0;
         const int bufs = (!norm_rows && (int64_t)slots * S > 1) ? 2 : 1;
         const int xcols = norm_rows ? k_full : pl.Gs * kGroup;
         const int Tw = std::max(1, (mats == 2 && slots == 1 ? 2304 : 4608) / tile);
         const size_t need = 16384 + (size_t)bufs * kMaxM * (xcols * 2 + 16) +
-                            (size_t)2 * nw * mats * std::min(Tw, pl.Gs) * tile;
-        warp_mode = need <= 227 * 1024;
+                            (size_t)2 * nw_ * mats * std::min(Tw, pl.Gs) * tile;
+        return need <= 227 * 1024;
+    };
+    if (warp_mode && nvfp4)
+        while (nw > 1 && !warp_fits(nw))
+            nw /= 2;
+    if (warp_mode) {
+        warp_mode = warp_fits(nw);
+        W = (int64_t)sms * nw;
     }
     if (warp_mode) {
         pl.mode = 1;
@@ -424,6 +453,8 @@ Plan plan_qproj(int n_rb, int groups, int mats, int bits, int slots, int k_full,
         pl.smem = pl.stage_off + (size_t)nw * pl.nst * slot;
         pl.KW = 1;
         pl.R = nw;
+    } else if (nvfp4) {
+        pl.mode = -1;
     }
 
     const bool partials = S > 1 || !pl.aligned;
@@ -445,6 +476,7 @@ int report_error(int status, const char* fmt, ...)
 }
 
 int validate_desc(const tf_qweight* w, const char* name) { return check_desc(w, name); }
+int validate_affine(const tf_qweight* w, const char* name) { return check_affine(w, name); }
 
 }  // namespace tfq
 
@@ -482,7 +514,8 @@ int tf_tune_set(int key, int value)
 
 size_t tf_qlinear_packed_bytes(int64_t batch, int64_t N, int64_t K, int bits, int group)
 {
-    if ((bits != 4 && bits != 8) || group != kGroup || K <= 0 || K % kGroup != 0 || N < 1 || batch < 1)
+    const bool ok_code = (group == kGroup && (bits == 4 || bits == 8)) || (group == 16 && bits == 4);
+    if (!ok_code || K <= 0 || K % kGroup != 0 || N < 1 || batch < 1)
         return 0;
     const int64_t n_pad = (N + 15) / 16 * 16;
     return (size_t)TF_PACK_HEADER_BYTES + (size_t)batch * (n_pad / 16) * (K / kGroup) * tile_bytes_for(bits);
@@ -516,6 +549,8 @@ int tf_qlinear_pack(const uint32_t* wq, const uint16_t* scales, const uint16_t* 
     desc->version = TF_PACK_VERSION;
     desc->bits = bits;
     desc->group = group;
+    desc->code = TF_CODE_AFFINE;
+    desc->global_scale = 1.f;
     desc->batch = batch;
     desc->N = N;
     desc->K = K;
@@ -526,11 +561,69 @@ int tf_qlinear_pack(const uint32_t* wq, const uint16_t* scales, const uint16_t* 
     return TF_OK;
 }
 
+int tf_qlinear_pack_nvfp4(const uint8_t* codes, const uint8_t* block_scales, float global_scale, int64_t N, int64_t K,
+                          void* packed, size_t packed_bytes, tf_qweight* desc, void* stream)
+{
+    if (K <= 0 || K % kGroup != 0)
+        return fail(TF_E_UNSUPPORTED_SHAPE, "tf_qlinear_pack_nvfp4: K must be a positive multiple of 64");
+    if (N < 1)
+        return fail(TF_E_INVALID_ARG, "tf_qlinear_pack_nvfp4: N must be >= 1");
+    if (!std::isfinite(global_scale))
+        return fail(TF_E_INVALID_ARG, "tf_qlinear_pack_nvfp4: global_scale must be finite");
+    if (codes == nullptr || block_scales == nullptr || packed == nullptr || desc == nullptr)
+        return fail(TF_E_INVALID_ARG, "tf_qlinear_pack_nvfp4: NULL pointer");
+    if (!aligned(packed, 16))
+        return fail(TF_E_INVALID_ARG, "tf_qlinear_pack_nvfp4: packed must be 16-byte aligned");
+    const size_t need = tf_qlinear_packed_bytes(1, N, K, 4, 16);
+    if (packed_bytes < need)
+        return fail(TF_E_WORKSPACE_TOO_SMALL, "tf_qlinear_pack_nvfp4: packed buffer has %zu bytes, needs %zu",
+                    packed_bytes, need);
+    PackHeader h{};
+    h.magic = TF_QWEIGHT_MAGIC;
+    h.version = TF_PACK_VERSION;
+    h.bits = 4;
+    h.group = 16;
+    h.code = TF_CODE_NVFP4;
+    h.global_scale = global_scale;
+    h.batch = 1;
+    h.N = N;
+    h.K = K;
+    h.n_pad = (N + 15) / 16 * 16;
+    h.tile_bytes = tile_bytes_for(kNvfp4);
+    h.matrix_bytes = h.n_pad / 16 * (K / kGroup) * h.tile_bytes;
+    cudaError_t e = launch_pack_nvfp4(codes, block_scales, N, K, static_cast<uint8_t*>(packed), h,
+                                      static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess)
+        return cuda_fail(e, "tf_qlinear_pack_nvfp4");
+    desc->magic = h.magic;
+    desc->version = h.version;
+    desc->bits = h.bits;
+    desc->group = h.group;
+    desc->code = h.code;
+    desc->global_scale = h.global_scale;
+    desc->batch = h.batch;
+    desc->N = N;
+    desc->K = K;
+    desc->n_pad = h.n_pad;
+    desc->tile_bytes = h.tile_bytes;
+    desc->matrix_bytes = h.matrix_bytes;
+    desc->data = packed;
+    return TF_OK;
+}
+
 int tf_qlinear_unpack_debug(const tf_qweight* w, uint32_t* wq, uint16_t* scales, uint16_t* biases, void* stream)
 {
     int rc = check_desc(w, "tf_qlinear_unpack_debug");
     if (rc)
         return rc;
+    if (w->code == TF_CODE_NVFP4) {
+        if (wq == nullptr || scales == nullptr)
+            return fail(TF_E_INVALID_ARG, "tf_qlinear_unpack_debug: NULL output");
+        cudaError_t e = launch_unpack_nvfp4(static_cast<const uint8_t*>(w->data), w->N, w->K,
+                                            reinterpret_cast<uint8_t*>(wq), reinterpret_cast<uint8_t*>(scales),
+                                            static_cast<cudaStream_t>(stream));
+        return e == cudaSuccess ? TF_OK : cuda_fail(e, "tf_qlinear_unpack_debug");
+    }
     if (wq == nullptr || scales == nullptr || biases == nullptr)
         return fail(TF_E_INVALID_ARG, "tf_qlinear_unpack_debug: NULL output");
     cudaError_t e = launch_unpack(static_cast<const uint8_t*>(w->data), w->batch, w->N, w->K, w->bits, wq, scales,
@@ -553,6 +646,7 @@ int tf_qweight_check(const tf_qweight* w, void* stream)
     if (e != cudaSuccess)
         return cuda_fail(e, "tf_qweight_check");
     if (h.magic != w->magic || h.version != w->version || h.bits != w->bits || h.group != w->group ||
+        h.code != w->code || !(h.global_scale == w->global_scale) ||
         h.batch != w->batch || h.N != w->N || h.K != w->K || h.n_pad != w->n_pad || h.tile_bytes != w->tile_bytes ||
         h.matrix_bytes != w->matrix_bytes)
         return fail(TF_E_BAD_PACK, "tf_qweight_check: device header does not match the descriptor");
@@ -569,7 +663,7 @@ static size_t qlinear_scratch_all_m(const tf_qweight* w, const tf_qweight* w_up)
     for (int rows = 1; rows <= kMaxM; ++rows)
         for (int k_full : {0, (int)w->K}) {  // with and without an RMSNorm prologue
             const Plan pl =
-                plan_qproj((int)(w->n_pad / 16), (int)(w->K / kGroup), w_up ? 2 : 1, w->bits, 1, k_full, rows);
+                plan_qproj((int)(w->n_pad / 16), (int)(w->K / kGroup), w_up ? 2 : 1, kernel_bits(w), 1, k_full, rows);
             r = std::max(r, plan_scratch(pl));
         }
     return r;
@@ -590,8 +684,11 @@ static int qlinear_impl(const tf_qweight* w, const tf_qweight* w_up, const uint1
                         const char* name, const uint8_t* rht = nullptr)
 {
     const bool dual = w_up != nullptr;
-    const Plan pl = plan_qproj((int)(w->n_pad / 16), (int)(w->K / kGroup), dual ? 2 : 1, w->bits, 1,
+    const Plan pl = plan_qproj((int)(w->n_pad / 16), (int)(w->K / kGroup), dual ? 2 : 1, kernel_bits(w), 1,
                                gamma != nullptr ? (int)w->K : 0, (int)M);
+    if (pl.mode < 0)
+        return fail(TF_E_UNSUPPORTED_SHAPE, "%s: NVFP4 weights run on warp workers, which this shape does not fit",
+                    name);
     if (pl.smem > 227 * 1024)
         return fail(TF_E_UNSUPPORTED_SHAPE,
                     gamma != nullptr ? "%s: K too large for the RMSNorm prologue (rows do not fit on chip)"
@@ -619,7 +716,9 @@ static int qlinear_impl(const tf_qweight* w, const tf_qweight* w_up, const uint1
     p.y_f32 = y_dtype == TF_DTYPE_F32;
     fill_common(p, pl, ws, scratch);
     p.rht = rht;
-    cudaError_t e = launch_qproj(w->bits, dual, false, pl, p, stream, pdl);
+    p.wscale0 = w->global_scale;
+    p.wscale1 = dual ? w_up->global_scale : 1.f;
+    cudaError_t e = launch_qproj(kernel_bits(w), dual, false, pl, p, stream, pdl);
     if (e != cudaSuccess)
         return cuda_fail(e, name);
     return TF_OK;
@@ -687,8 +786,10 @@ int tf_qmlp_gateup_run(const tf_qweight* gate, const tf_qweight* up, const uint1
     int rc = check_desc(gate, "tf_qmlp_gateup_run: gate");
     if (rc || (rc = check_desc(up, "tf_qmlp_gateup_run: up")))
         return rc;
-    if (gate->batch != 1 || up->batch != 1 || gate->N != up->N || gate->K != up->K || gate->bits != up->bits)
-        return fail(TF_E_UNSUPPORTED_SHAPE, "tf_qmlp_gateup_run: gate and up must have equal N, K, bits and batch 1");
+    if (gate->batch != 1 || up->batch != 1 || gate->N != up->N || gate->K != up->K || gate->bits != up->bits ||
+        gate->code != up->code)
+        return fail(TF_E_UNSUPPORTED_SHAPE,
+                    "tf_qmlp_gateup_run: gate and up must have equal N, K, bits, weight code and batch 1");
     if (M < 1 || M > kMaxM)
         return fail(TF_E_UNSUPPORTED_SHAPE, "tf_qmlp_gateup_run: M must be in [1, 8]");
     if ((rc = check_act(x, ldx, gate->K, "tf_qmlp_gateup_run: x")))
@@ -734,8 +835,8 @@ MoeLayout moe_layout(const tf_qweight* gate, const tf_qweight* down, int64_t M, 
 int check_moe(const tf_qweight* gate, const tf_qweight* up, const tf_qweight* down, int64_t M, int top_k,
               const char* name)
 {
-    int rc = check_desc(gate, "gate");
-    if (rc || (rc = check_desc(up, "up")) || (rc = check_desc(down, "down")))
+    int rc = check_affine(gate, "gate");
+    if (rc || (rc = check_affine(up, "up")) || (rc = check_affine(down, "down")))
         return rc;
     if (up->batch != gate->batch || down->batch != gate->batch || up->N != gate->N || up->K != gate->K ||
         down->K != gate->N || down->N != gate->K || up->bits != gate->bits || down->bits != gate->bits)
@@ -857,8 +958,9 @@ int check_decoder(const tf_decoder_desc* d, int64_t M, const char* name)
     int rc;
     for (int l = 0; l < d->n_layers; ++l) {
         const tf_decoder_layer& L = d->layers[l];
-        if ((rc = check_desc(&L.qkv, "qkv")) || (rc = check_desc(&L.o, "o")) || (rc = check_desc(&L.gate, "gate")) ||
-            (rc = check_desc(&L.up, "up")) || (rc = check_desc(&L.down, "down")))
+        if ((rc = check_affine(&L.qkv, "qkv")) || (rc = check_affine(&L.o, "o")) ||
+            (rc = check_affine(&L.gate, "gate")) || (rc = check_affine(&L.up, "up")) ||
+            (rc = check_affine(&L.down, "down")))
             return rc;
         if (L.qkv.N != Q + 2 * KV || L.qkv.K != D || L.o.N != D || L.o.K != Q || L.gate.N != F || L.gate.K != D ||
             L.up.N != F || L.up.K != D || L.down.N != D || L.down.K != F || L.gate.bits != L.up.bits ||
@@ -867,7 +969,7 @@ int check_decoder(const tf_decoder_desc* d, int64_t M, const char* name)
         if (L.attn_norm == nullptr || L.mlp_norm == nullptr || !aligned(L.attn_norm, 16) || !aligned(L.mlp_norm, 16))
             return fail(TF_E_INVALID_ARG, "%s: layer %d norm weights NULL or misaligned", name, l);
     }
-    if ((rc = check_desc(&d->readout, "readout")))
+    if ((rc = check_affine(&d->readout, "readout")))
         return rc;
     if (d->readout.N != d->vocab || d->readout.K != D || d->readout.batch != 1)
         return fail(TF_E_UNSUPPORTED_SHAPE, "%s: readout must be [vocab][d_model]", name);

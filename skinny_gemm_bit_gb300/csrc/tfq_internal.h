@@ -18,15 +18,21 @@ constexpr int kMaxStages = 8;
 constexpr int kMaxSlots = 64;                 // MoE: distinct experts per call (M * top_k <= 64)
 constexpr uint64_t kDefaultWaitLimitNs = 2000000000ull;  // 2 s
 
-__host__ __device__ constexpr int tile_bytes_for(int bits) { return bits == 4 ? 576 : 1088; }
-__host__ __device__ constexpr int tile_q_bytes_for(int bits) { return bits == 4 ? 512 : 1024; }
+// The kernels' BITS template argument: 4 or 8 for MLX affine codes of that width,
+// kNvfp4 for NVFP4 (E2M1 codes, an E4M3 scale per 16 columns; 576-byte tiles).
+constexpr int kNvfp4 = -4;
+
+__host__ __device__ constexpr int tile_bytes_for(int bits) { return bits == 8 ? 1088 : 576; }
+__host__ __device__ constexpr int tile_q_bytes_for(int bits) { return bits == 8 ? 1024 : 512; }
 
 // Device header written at the start of every packed buffer.
 struct PackHeader {
     uint32_t magic, version;
     int32_t bits, group;
+    int32_t code;
+    float global_scale;
     int64_t batch, N, K, n_pad, tile_bytes, matrix_bytes;
-    uint8_t reserved[TF_PACK_HEADER_BYTES - 8 * 8];
+    uint8_t reserved[TF_PACK_HEADER_BYTES - 9 * 8];
 };
 static_assert(sizeof(PackHeader) == TF_PACK_HEADER_BYTES, "header size");
 
@@ -87,10 +93,12 @@ struct QProjParams {
     int gamma_off;  // staged RMSNorm weight (K bf16)
     int x_direct;   // activations loaded straight into registers (unsplit calls), not by bulk copy
     const uint8_t* rht;  // input Hadamard transform signs (K bits, LSB first, set = -1) or nullptr
+    float wscale0, wscale1;  // NVFP4: global scale of matrix 0 / 1 (unused by affine codes)
 };
 
 struct Plan {
-    int mode;  // 0: teams in lock-step (latency-bound calls), 1: warp workers, 2: streaming (one large matrix)
+    int mode;  // 0: teams in lock-step (latency-bound calls), 1: warp workers, 2: streaming (one large matrix),
+               // -1: none fits (NVFP4 weights run on warp workers only)
     int KW, R, S, Gs, cg, nst, C, aligned, kmax, segmax, slots;
     int red_off, seg_off, round_off, last_off, xraw_off, x_rs, stage_off;
     int nw, pw, xsum1_off, xraw1_off, gamma_off;
@@ -146,6 +154,7 @@ Plan plan_qproj(int n_rb, int groups, int mats, int bits, int slots, int k_full,
 // Error reporting and descriptor validation shared by the entry points (tfq_api.cu).
 int report_error(int status, const char* fmt, ...);
 int validate_desc(const tf_qweight* w, const char* name);
+int validate_affine(const tf_qweight* w, const char* name);  // validate_desc, and MLX affine codes only
 
 // launchers (tfq_qproj_b*_*.cu, one instantiation unit per bit width and matrix count)
 cudaError_t launch_qproj_b4_single(bool moe, const Plan& plan, const QProjParams& p, cudaStream_t stream, bool pdl);
@@ -153,9 +162,13 @@ cudaError_t launch_qproj_b4_dual(bool moe, const Plan& plan, const QProjParams& 
 cudaError_t launch_qproj_b8_single(bool moe, const Plan& plan, const QProjParams& p, cudaStream_t stream, bool pdl);
 cudaError_t launch_qproj_b8_dual(bool moe, const Plan& plan, const QProjParams& p, cudaStream_t stream, bool pdl);
 
+cudaError_t launch_qproj_nvfp4(bool dual, const Plan& plan, const QProjParams& p, cudaStream_t stream, bool pdl);
+
 inline cudaError_t launch_qproj(int bits, bool dual, bool moe, const Plan& plan, const QProjParams& p,
                                 cudaStream_t stream, bool pdl)
 {
+    if (bits == kNvfp4)
+        return moe ? cudaErrorInvalidValue : launch_qproj_nvfp4(dual, plan, p, stream, pdl);
     if (bits == 4)
         return dual ? launch_qproj_b4_dual(moe, plan, p, stream, pdl) : launch_qproj_b4_single(moe, plan, p, stream, pdl);
     return dual ? launch_qproj_b8_dual(moe, plan, p, stream, pdl) : launch_qproj_b8_single(moe, plan, p, stream, pdl);
@@ -166,6 +179,10 @@ cudaError_t launch_pack(const uint32_t* wq, const uint16_t* s, const uint16_t* b
                         int64_t K, int bits, uint8_t* packed, cudaStream_t stream);
 cudaError_t launch_unpack(const uint8_t* packed, int64_t batch, int64_t N, int64_t K, int bits, uint32_t* wq,
                           uint16_t* s, uint16_t* b, cudaStream_t stream);
+cudaError_t launch_pack_nvfp4(const uint8_t* codes, const uint8_t* scales, int64_t N, int64_t K, uint8_t* packed,
+                              const PackHeader& hdr, cudaStream_t stream);
+cudaError_t launch_unpack_nvfp4(const uint8_t* packed, int64_t N, int64_t K, uint8_t* codes, uint8_t* scales,
+                                cudaStream_t stream);
 
 // MoE helpers (tfq_moe.cu)
 cudaError_t launch_moe_route(const float* logits, int M, int E, int top_k, int32_t* idx, float* w, MoeMeta* meta,

@@ -16,6 +16,12 @@
 // 8-bit: words 2kb + jp of lane l; byte bp is row gi + 8*(bp&1), column
 //   2t + 8*jp + (bp>>1). The low nibbles of a word give registers 2jp, 2jp+1 of
 //   the "low" fragment, the high nibbles the same registers of the "high" one.
+//
+// NVFP4 (E2M1 codes, one E4M3 scale per 16 columns): byte r of word kb of lane l is
+//   register r of k-block kb as two codes, the even column in the low nibble (the
+//   order in which one cvt.rn.f16x2.e2m1x2 turns a byte into a register); the 64
+//   scale bytes follow as 8 groups of 8, group gi = {row gi, row gi + 8} for k-blocks
+//   0..3 in turn, so one 16-bit half converts to the (row gi, row gi + 8) pair.
 #include <cuda_bf16.h>
 
 #include "tfq_internal.h"
@@ -190,6 +196,68 @@ __global__ void embed_rows_kernel(const uint8_t* __restrict__ packed, int64_t N,
     }
 }
 
+__global__ void pack_nvfp4_kernel(const uint8_t* __restrict__ codes, const uint8_t* __restrict__ scales, int64_t N,
+                                  int64_t K, uint8_t* __restrict__ packed, PackHeader hdr)
+{
+    const int64_t G = K / kGroup;
+    const int64_t n_rb = (N + kRowsPerBlock - 1) / kRowsPerBlock;
+    constexpr int tile_words = tile_bytes_for(kNvfp4) / 4, q_words = tile_q_bytes_for(kNvfp4) / 4;
+    const int64_t total = n_rb * G * tile_words;
+    uint32_t* out = reinterpret_cast<uint32_t*>(packed + TF_PACK_HEADER_BYTES);
+    if (blockIdx.x == 0 && threadIdx.x == 0)
+        *reinterpret_cast<PackHeader*>(packed) = hdr;
+    for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
+         idx += (int64_t)gridDim.x * blockDim.x) {
+        const int wi = (int)(idx % tile_words);
+        const int64_t tile = idx / tile_words;
+        const int64_t g = tile % G, rb = tile / G;
+        uint32_t word = 0;
+        if (wi < q_words) {
+            const int lane = wi >> 2, kb = wi & 3, gi = lane >> 2, t = lane & 3;
+            for (int r = 0; r < 4; ++r) {
+                const int64_t row = rb * kRowsPerBlock + gi + 8 * (r & 1);
+                const int64_t col = g * kGroup + kb * 16 + 2 * t + 8 * (r >> 1);  // even
+                if (row < N)
+                    word |= (uint32_t)codes[row * (K / 2) + col / 2] << (8 * r);
+            }
+        } else {
+            const int j = wi - q_words, gi = j >> 1;
+            for (int b = 0; b < 4; ++b) {
+                const int kb = 2 * (j & 1) + (b >> 1);
+                const int64_t row = rb * kRowsPerBlock + gi + 8 * (b & 1);
+                if (row < N)
+                    word |= (uint32_t)scales[row * (K / 16) + g * 4 + kb] << (8 * b);
+            }
+        }
+        out[idx] = word;
+    }
+}
+
+// Inverse of pack_nvfp4_kernel: one thread per code byte, then per scale byte.
+__global__ void unpack_nvfp4_kernel(const uint8_t* __restrict__ packed, int64_t N, int64_t K,
+                                    uint8_t* __restrict__ codes, uint8_t* __restrict__ scales)
+{
+    const int64_t G = K / kGroup;
+    constexpr int tile_b = tile_bytes_for(kNvfp4), q_b = tile_q_bytes_for(kNvfp4);
+    const uint8_t* tiles = packed + TF_PACK_HEADER_BYTES;
+    const int64_t n_codes = N * (K / 2), total = n_codes + N * (K / 16);
+    for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
+         idx += (int64_t)gridDim.x * blockDim.x) {
+        if (idx < n_codes) {
+            const int64_t row = idx / (K / 2), col = 2 * (idx % (K / 2));
+            const int rr = (int)(row % kRowsPerBlock), c = (int)(col % kGroup), cc = c & 15;
+            const int lane = (rr & 7) * 4 + ((cc & 7) >> 1), r = (rr >> 3) + 2 * (cc >> 3);
+            const uint8_t* tb = tiles + ((row / kRowsPerBlock) * G + col / kGroup) * tile_b;
+            codes[idx] = tb[lane * 16 + (c >> 4) * 4 + r];
+        } else {
+            const int64_t i = idx - n_codes, row = i / (K / 16), sj = i % (K / 16);
+            const int rr = (int)(row % kRowsPerBlock), kb = (int)(sj % 4);
+            const uint8_t* tb = tiles + ((row / kRowsPerBlock) * G + sj / 4) * tile_b;
+            scales[i] = tb[q_b + (rr & 7) * 8 + 2 * kb + (rr >> 3)];
+        }
+    }
+}
+
 int grid_for(int64_t total, int threads)
 {
     int64_t blocks = (total + threads - 1) / threads;
@@ -208,6 +276,8 @@ cudaError_t launch_pack(const uint32_t* wq, const uint16_t* s, const uint16_t* b
     h.version = TF_PACK_VERSION;
     h.bits = bits;
     h.group = kGroup;
+    h.code = TF_CODE_AFFINE;
+    h.global_scale = 1.f;
     h.batch = batch;
     h.N = N;
     h.K = K;
@@ -229,6 +299,22 @@ cudaError_t launch_unpack(const uint8_t* packed, int64_t batch, int64_t N, int64
         return e;
     const int64_t groups = batch * N * (K / kGroup);
     unpack_scales_kernel<<<grid_for(groups, 256), 256, 0, stream>>>(packed, batch, N, K, bits, s, b);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_pack_nvfp4(const uint8_t* codes, const uint8_t* scales, int64_t N, int64_t K, uint8_t* packed,
+                              const PackHeader& hdr, cudaStream_t stream)
+{
+    const int64_t total = (hdr.n_pad / kRowsPerBlock) * (K / kGroup) * (tile_bytes_for(kNvfp4) / 4);
+    pack_nvfp4_kernel<<<grid_for(total, 256), 256, 0, stream>>>(codes, scales, N, K, packed, hdr);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_unpack_nvfp4(const uint8_t* packed, int64_t N, int64_t K, uint8_t* codes, uint8_t* scales,
+                                cudaStream_t stream)
+{
+    const int64_t total = N * (K / 2) + N * (K / 16);
+    unpack_nvfp4_kernel<<<grid_for(total, 256), 256, 0, stream>>>(packed, N, K, codes, scales);
     return cudaGetLastError();
 }
 

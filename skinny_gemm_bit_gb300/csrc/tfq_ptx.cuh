@@ -5,6 +5,7 @@
 
 #include <cstdint>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 namespace tfq {
 
@@ -195,6 +196,50 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t pair)
     uint32_t r;
     asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(bf16hi_f32(pair)), "f"(bf16lo_f32(pair)));
     return r;
+}
+
+// ---------------------------------------------------------------- NVFP4 conversions
+
+// The four bytes of w, each two E2M1 codes (low nibble first), as four fp16 pairs:
+// r0 from byte 0 ... r3 from byte 3, the low nibble in the low half. Exact: every
+// E2M1 value (0, +-0.5 ... +-6) is an fp16 value.
+__device__ __forceinline__ void e2m1x8_to_f16x2(uint32_t w, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3)
+{
+    asm("{\n .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %4;\n"
+        " cvt.rn.f16x2.e2m1x2 %0, b0;\n cvt.rn.f16x2.e2m1x2 %1, b1;\n"
+        " cvt.rn.f16x2.e2m1x2 %2, b2;\n cvt.rn.f16x2.e2m1x2 %3, b3;\n}"
+        : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+        : "r"(w));
+}
+
+// Bits 0-15 of v, two E4M3 bytes, as an fp16 pair (low byte in the low half). Exact:
+// every finite E4M3 value is an fp16 value.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t v)
+{
+    uint32_t d;
+    const unsigned short h = (unsigned short)(v & 0xFFFFu);
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(d) : "h"(h));
+    return d;
+}
+
+// a * (low half of s, twice) and a * (high half of s, twice), fp16 pairs.
+__device__ __forceinline__ uint32_t hmul2_lo(uint32_t a, uint32_t s)
+{
+    const __half2 r = __hmul2(*reinterpret_cast<const __half2*>(&a), __low2half2(*reinterpret_cast<const __half2*>(&s)));
+    return *reinterpret_cast<const uint32_t*>(&r);
+}
+__device__ __forceinline__ uint32_t hmul2_hi(uint32_t a, uint32_t s)
+{
+    const __half2 r = __hmul2(*reinterpret_cast<const __half2*>(&a), __high2half2(*reinterpret_cast<const __half2*>(&s)));
+    return *reinterpret_cast<const uint32_t*>(&r);
+}
+
+// An fp16 pair as a bf16 pair, rounded to nearest even (exact when the values have
+// at most 8 significant bits and lie in bf16's normal range).
+__device__ __forceinline__ uint32_t f16x2_to_bf16x2(uint32_t a)
+{
+    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&a));
+    return f32x2_to_bf16x2(f.x, f.y);
 }
 
 }  // namespace tfq

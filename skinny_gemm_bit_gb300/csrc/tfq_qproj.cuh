@@ -216,11 +216,45 @@ __device__ __forceinline__ void tile_mac_f16(const uint8_t* tile, int lane, cons
     }
 }
 
+// The tile math of an NVFP4 tile. Each A register (two E2M1 codes of one row) becomes
+// an fp16 pair and is multiplied by the row's E4M3 block scale, also converted to
+// fp16: a 2-bit times a 4-bit significand is exact in fp16 (|w| <= 6 * 448, nonzero
+// |w| >= 2^-10), so the MMA accumulates the weights themselves and there is no group
+// epilogue; the matrix's global scale multiplies the finished sums. With bf16
+// activations (F16 false) the exact fp16 weights are converted, again exactly, to bf16.
+template <bool F16>
+__device__ __forceinline__ void tile_mac_nvfp4(const uint8_t* tile, int lane, const uint4& xa, const uint4& xb,
+                                               float (&acc)[4])
+{
+    const uint4 wv = *reinterpret_cast<const uint4*>(tile + lane * 16);
+    const uint2 sv = *reinterpret_cast<const uint2*>(tile + tile_q_bytes_for(kNvfp4) + (lane >> 2) * 8);
+    const uint32_t w[4] = {wv.x, wv.y, wv.z, wv.w};
+    const uint32_t sp[4] = {e4m3x2_to_f16x2(sv.x), e4m3x2_to_f16x2(sv.x >> 16), e4m3x2_to_f16x2(sv.y),
+                            e4m3x2_to_f16x2(sv.y >> 16)};
+    const uint32_t b0[4] = {xa.x, xa.z, xb.x, xb.z}, b1[4] = {xa.y, xa.w, xb.y, xb.w};
+#pragma unroll
+    for (int kb = 0; kb < 4; ++kb) {
+        uint32_t a0, a1, a2, a3;  // registers r: rows gi + 8 (r & 1), columns 2 t + 8 (r >> 1) + {0, 1}
+        e2m1x8_to_f16x2(w[kb], a0, a1, a2, a3);
+        a0 = hmul2_lo(a0, sp[kb]);
+        a1 = hmul2_hi(a1, sp[kb]);
+        a2 = hmul2_lo(a2, sp[kb]);
+        a3 = hmul2_hi(a3, sp[kb]);
+        if constexpr (F16)
+            mma_f16_16816(acc, a0, a1, a2, a3, b0[kb], b1[kb]);
+        else
+            mma_bf16_16816(acc, f16x2_to_bf16x2(a0), f16x2_to_bf16x2(a1), f16x2_to_bf16x2(a2), f16x2_to_bf16x2(a3),
+                           b0[kb], b1[kb]);
+    }
+}
+
 template <int BITS, bool F16>
 __device__ __forceinline__ void tile_mac_x(const uint8_t* tile, int lane, const uint4& xa, const uint4& xb,
                                            const float2& xs, float (&acc)[4])
 {
-    if constexpr (F16)
+    if constexpr (BITS == kNvfp4)
+        tile_mac_nvfp4<F16>(tile, lane, xa, xb, acc);
+    else if constexpr (F16)
         tile_mac_f16<BITS>(tile, lane, xa, xb, xs, acc);
     else
         tile_mac_chain<BITS>(tile, lane, xa, xb, xs, acc);
@@ -1361,9 +1395,9 @@ __global__ void __launch_bounds__(kThreads, 1) qproj_warp_kernel(const __grid_co
         if (two)
             x_rht(xb1, p.x_rs, xs1, M1, xg0_1, p.Gs, p.rht, cw, lane, kConsumerWarps, kBarConsumers);
     }
-    // fp16 activations when every staged value converts exactly and, for 4-bit codes,
-    // |x| < 4096 (the group sums above are of the same values): the codes then unpack
-    // with fewer instructions. The decision is the CTA's, from one snapshot.
+    // fp16 activations when every staged value converts exactly and, for 4-bit affine
+    // codes, |x| < 4096 (the group sums above are of the same values): the codes then
+    // unpack with fewer instructions. The decision is the CTA's, from one snapshot.
     {
         constexpr int kLimExp = BITS == 4 ? 12 : 16;
         const int t = cw * 32 + lane, nt = kConsumerWarps * 32;
@@ -1424,6 +1458,14 @@ __global__ void __launch_bounds__(kThreads, 1) qproj_warp_kernel(const __grid_co
                     for (int i = 0; i < 4; ++i) {
                         acc0[i] += acc1[i];
                         acc1[i] = 0.f;
+                    }
+                }
+                if constexpr (BITS == kNvfp4) {  // the matrices' global scales
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        acc0[i] *= p.wscale0;
+                        if constexpr (DUAL)
+                            acc1[i] *= p.wscale1;
                     }
                 }
                 if (S == 1 && len == p.groups) {

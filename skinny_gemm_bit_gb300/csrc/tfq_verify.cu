@@ -107,7 +107,7 @@ int tf_argmax_rows(const uint16_t* v, int64_t ld, int64_t M, int64_t N, int32_t*
 int tf_embed_rows(const tf_qweight* w, const int32_t* ids, int64_t M, uint16_t* x, void* ws, size_t ws_bytes,
                   void* stream)
 {
-    int rc = validate_desc(w, "tf_embed_rows");
+    int rc = validate_affine(w, "tf_embed_rows");
     if (rc)
         return rc;
     if (ids == nullptr || x == nullptr || ws == nullptr)

@@ -125,6 +125,13 @@ def concat_rows(*ws) -> dict:
 # the five workloads
 # ----------------------------------------------------------------------------
 
+def nvfp4_projection(seed: int, M: int, K: int, N: int) -> dict:
+    """One NVFP4 projection: activations, then the weights (``nvfp4_weights``)."""
+    rng = np.random.default_rng(seed)
+    x = activations(rng, M, K)
+    return {"x": x, "w": nvfp4_weights(rng, N, K)}
+
+
 def single_projection(seed: int = 0, M: int = 1, K: int = 1024, N: int = 3072, bits: int = 4) -> dict:
     """One 4-bit projection (default: M=1, K=1024, N=3072, seed 0)."""
     rng = np.random.default_rng(seed)

@@ -27,7 +27,9 @@ TF_DTYPE_BF16 = 0
 TF_DTYPE_F32 = 1
 TF_RUN_PDL = 1
 TF_QWEIGHT_MAGIC = 0x31515446
-TF_PACK_VERSION = 1
+TF_PACK_VERSION = 2
+TF_CODE_AFFINE = 0
+TF_CODE_NVFP4 = 1
 TF_TUNE_ROWBLOCKS = 0
 TF_TUNE_SPLITK = 1
 TF_TUNE_STAGE_GROUPS = 2
@@ -44,7 +46,7 @@ SZ = ctypes.c_size_t
 
 class tf_qweight(ctypes.Structure):
     _fields_ = [("magic", ctypes.c_uint32), ("version", ctypes.c_uint32), ("bits", I32), ("group", I32),
-                ("batch", I64), ("N", I64), ("K", I64), ("n_pad", I64), ("tile_bytes", I64),
+                ("code", I32), ("global_scale", ctypes.c_float), ("batch", I64), ("N", I64), ("K", I64), ("n_pad", I64), ("tile_bytes", I64),
                 ("matrix_bytes", I64), ("data", P)]
 
 
@@ -75,6 +77,7 @@ _SIGS = {
     "tf_qlinear_packed_bytes": (SZ, [I64, I64, I64, ctypes.c_int, ctypes.c_int]),
     "tf_qlinear_pack": (ctypes.c_int, [P, P, P, I64, I64, I64, ctypes.c_int, ctypes.c_int, P, SZ,
                                        ctypes.POINTER(tf_qweight), P]),
+    "tf_qlinear_pack_nvfp4": (ctypes.c_int, [P, P, ctypes.c_float, I64, I64, P, SZ, ctypes.POINTER(tf_qweight), P]),
     "tf_qlinear_unpack_debug": (ctypes.c_int, [ctypes.POINTER(tf_qweight), P, P, P, P]),
     "tf_qweight_check": (ctypes.c_int, [ctypes.POINTER(tf_qweight), P]),
     "tf_qlinear_workspace_bytes": (SZ, [ctypes.POINTER(tf_qweight), I64]),
@@ -177,9 +180,14 @@ class QWeight:
     def batch(self):
         return self.desc.batch
 
+    @property
+    def code(self):
+        return self.desc.code
+
     def weight_bytes(self) -> int:
-        """Algorithmic bytes of the codes, scales and biases (excluding row padding)."""
-        return int(self.batch * self.N * self.K * (self.bits / 8 + 4 / 64))
+        """Algorithmic bytes of the codes and scales/biases (excluding row padding): 4/64 B a
+        weight for a bf16 scale and bias per 64, or 1/16 for an E4M3 scale per 16 (NVFP4)."""
+        return int(self.batch * self.N * self.K * (self.bits / 8 + (1 / 16 if self.code == TF_CODE_NVFP4 else 4 / 64)))
 
 
 def packed_bytes(batch: int, N: int, K: int, bits: int, group: int = 64) -> int:
@@ -218,9 +226,34 @@ def tf_qlinear_pack(wq, scales, biases, bits: int, device="cuda", stream=None) -
     return QWeight(buf, desc)
 
 
+def tf_qlinear_pack_nvfp4(codes, block_scales, global_scale: float, device="cuda", stream=None) -> QWeight:
+    """Pack NVFP4 weights (codes uint8 [N, K/2], E4M3 block scales uint8 [N, K/16], fp32
+    global scale) into a QWeight."""
+    codes = _as_dev(codes, torch.uint8, device)
+    block_scales = _as_dev(block_scales, torch.uint8, device)
+    N, K = codes.shape[0], codes.shape[1] * 2
+    if codes.dtype != torch.uint8 or block_scales.dtype != torch.uint8 or tuple(block_scales.shape) != (N, K // 16):
+        raise TfqError(TF_E_INVALID_ARG, "codes must be uint8 [N, K/2] and block_scales uint8 [N, K/16]")
+    nbytes = packed_bytes(1, N, K, 4, 16)
+    if nbytes == 0:
+        raise TfqError(TF_E_UNSUPPORTED_SHAPE, f"unsupported NVFP4 packing N={N} K={K}")
+    buf = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    desc = tf_qweight()
+    _check(lib().tf_qlinear_pack_nvfp4(_ptr(codes), _ptr(block_scales), float(global_scale), N, K, _ptr(buf), nbytes,
+                                       ctypes.byref(desc), _stream(stream)))
+    torch.cuda.current_stream().synchronize() if stream is None else stream.synchronize()
+    return QWeight(buf, desc)
+
+
 def tf_qlinear_unpack_debug(w: QWeight, stream=None):
-    """(wq int32, scales int16, biases int16) in MLX layout, read back out of the packed buffer."""
+    """(wq int32, scales int16, biases int16) in MLX layout, read back out of the packed buffer;
+    for NVFP4 weights (codes uint8 [N, K/2], block scales uint8 [N, K/16], None)."""
     dev = w.buf.device
+    if w.code == TF_CODE_NVFP4:
+        codes = torch.empty((w.N, w.K // 2), dtype=torch.uint8, device=dev)
+        sc = torch.empty((w.N, w.K // 16), dtype=torch.uint8, device=dev)
+        _check(lib().tf_qlinear_unpack_debug(ctypes.byref(w.desc), _ptr(codes), _ptr(sc), None, _stream(stream)))
+        return codes, sc, None
     lead = (w.batch,) if w.batch > 1 else ()
     wq = torch.empty(lead + (w.N, w.K * w.bits // 32), dtype=torch.int32, device=dev)
     s = torch.empty(lead + (w.N, w.K // 64), dtype=torch.int16, device=dev)

@@ -55,8 +55,11 @@ def test_packed_bytes(T):
     assert L.tf_qlinear_packed_bytes(1, 3072, 1024, 4, 64) == 256 + 192 * 16 * 576
     assert L.tf_qlinear_packed_bytes(1, 3073, 1024, 4, 64) == 256 + 193 * 16 * 576   # ragged N pads to 16
     assert L.tf_qlinear_packed_bytes(128, 768, 2048, 8, 64) == 256 + 128 * 48 * 32 * 1088
-    for bad in [(1, 64, 64, 3, 64), (1, 64, 64, 4, 32), (1, 64, 100, 4, 64), (1, 0, 64, 4, 64), (0, 64, 64, 4, 64)]:
+    for bad in [(1, 64, 64, 3, 64), (1, 64, 64, 4, 32), (1, 64, 100, 4, 64), (1, 0, 64, 4, 64), (0, 64, 64, 4, 64),
+                (1, 64, 64, 8, 16), (1, 64, 96, 4, 16)]:
         assert L.tf_qlinear_packed_bytes(*bad) == 0
+    # NVFP4 (bits 4, group 16): 512 bytes of codes + 64 of block scales a 16 x 64 tile
+    assert L.tf_qlinear_packed_bytes(1, 2560, 12800, 4, 16) == 256 + 160 * 200 * 576
 
 
 FAKE = ctypes.c_void_p(0x10000)  # aligned, never dereferenced: validation fails first
@@ -81,7 +84,8 @@ def test_pack_refuses_bad_arguments(T):
 
 def _desc(T, N=64, K=128, bits=4, batch=1):
     d = T.tf_qweight()
-    d.magic, d.version, d.bits, d.group, d.batch, d.N, d.K = 0x31515446, 1, bits, 64, batch, N, K
+    d.magic, d.version, d.bits, d.group, d.batch, d.N, d.K = 0x31515446, T.TF_PACK_VERSION, bits, 64, batch, N, K
+    d.code, d.global_scale = T.TF_CODE_AFFINE, 1.0
     d.n_pad = (N + 15) // 16 * 16
     d.tile_bytes = 576 if bits == 4 else 1088
     d.matrix_bytes = d.n_pad // 16 * (K // 64) * d.tile_bytes
@@ -141,3 +145,54 @@ def test_workspace_query_is_independent_of_m(T):
     L = T.lib()
     sizes = {L.tf_qlinear_workspace_bytes(ctypes.byref(d), m) for m in range(1, 9)}
     assert len(sizes) == 1
+
+
+def _nvfp4_desc(T, N=64, K=128):
+    d = _desc(T, N, K, 4)
+    d.group, d.code, d.global_scale = 16, T.TF_CODE_NVFP4, 0.004
+    return d
+
+
+def test_nvfp4_descriptors_are_validated(T):
+    L = T.lib()
+    good = _nvfp4_desc(T)
+    assert L.tf_qlinear_workspace_bytes(ctypes.byref(good), 8) >= 256
+    for field, value in [("group", 64), ("bits", 8), ("batch", 2), ("global_scale", float("nan")),
+                         ("global_scale", float("inf")), ("code", 7)]:
+        d = _nvfp4_desc(T)
+        setattr(d, field, value)
+        assert L.tf_qlinear_workspace_bytes(ctypes.byref(d), 8) == 0, field
+    d = _desc(T)
+    d.code = T.TF_CODE_NVFP4  # an affine layout (group 64) labelled NVFP4
+    assert L.tf_qlinear_workspace_bytes(ctypes.byref(d), 8) == 0
+
+
+def test_nvfp4_pack_refuses_bad_arguments(T):
+    L = T.lib()
+    d = T.tf_qweight()
+    need = L.tf_qlinear_packed_bytes(1, 64, 128, 4, 16)
+    assert L.tf_qlinear_pack_nvfp4(FAKE, FAKE, 1.0, 64, 100, FAKE, need, ctypes.byref(d), None) == \
+        T.TF_E_UNSUPPORTED_SHAPE
+    assert L.tf_qlinear_pack_nvfp4(FAKE, FAKE, float("nan"), 64, 128, FAKE, need, ctypes.byref(d), None) == \
+        T.TF_E_INVALID_ARG
+    assert L.tf_qlinear_pack_nvfp4(None, FAKE, 1.0, 64, 128, FAKE, need, ctypes.byref(d), None) == T.TF_E_INVALID_ARG
+    assert L.tf_qlinear_pack_nvfp4(FAKE, FAKE, 1.0, 64, 128, ctypes.c_void_p(0x10008), need, ctypes.byref(d), None) == \
+        T.TF_E_INVALID_ARG
+    assert L.tf_qlinear_pack_nvfp4(FAKE, FAKE, 1.0, 64, 128, FAKE, need - 1, ctypes.byref(d), None) == \
+        T.TF_E_WORKSPACE_TOO_SMALL
+    assert d.magic == 0
+
+
+def test_nvfp4_weights_are_refused_where_only_affine_codes_run(T):
+    L = T.lib()
+    d = _nvfp4_desc(T)
+    # MoE (three NVFP4 expert stacks) and the embedding lookup
+    assert L.tf_qmoe_workspace_bytes(ctypes.byref(d), ctypes.byref(d), ctypes.byref(d), 1, 1) == 0
+    assert "NVFP4" in T.last_error()
+    rc = L.tf_embed_rows(ctypes.byref(d), FAKE, 1, FAKE, FAKE, 256, None)
+    assert rc == T.TF_E_UNSUPPORTED_SHAPE
+    # gate and up must carry the same code
+    a = _desc(T)
+    ws = L.tf_qmlp_gateup_run(ctypes.byref(a), ctypes.byref(d), FAKE, 128, 1, None, 1e-6, FAKE, FAKE, 1 << 20, 0,
+                              None)
+    assert ws == T.TF_E_UNSUPPORTED_SHAPE
