@@ -64,6 +64,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity)
     return ok != 0;
 }
 
+// Device-scope fetch-and-add with acquire-release semantics: the caller's earlier
+// writes (and those ordered before them by a warp or CTA barrier) are visible to
+// whoever reads the counter after it, and the caller sees the writes released by
+// the earlier adders.
+__device__ __forceinline__ unsigned atom_add_acq_rel_gpu(unsigned* ptr, unsigned v)
+{
+    unsigned old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(ptr), "r"(v) : "memory");
+    return old;
+}
+
 __device__ __forceinline__ uint64_t globaltimer_ns()
 {
     uint64_t t;

@@ -1187,8 +1187,9 @@ __device__ __forceinline__ void warp_chunk(const uint8_t* sb, const uint8_t* xb,
 // by lane w of the producer warp, so the workers of a CTA never wait for each other
 // (a slot is only ever waited on by its owner, at most one phase ahead). A
 // segment that is a whole row block of an unsplit problem is stored directly;
-// boundary segments become fp32 partials summed, after the CTA's workers are done,
-// by the last contributor of the row block.
+// boundary segments become fp32 partials: when its range is done, a worker counts
+// each of its row blocks with one acquire-release add, and the worker whose add
+// completes a count sums that row block's slots (no CTA barrier on the way).
 template <int BITS, bool DUAL, bool MOE>
 __global__ void __launch_bounds__(kThreads, 1) qproj_warp_kernel(const __grid_constant__ QProjParams p)
 {
@@ -1213,9 +1214,7 @@ __global__ void __launch_bounds__(kThreads, 1) qproj_warp_kernel(const __grid_co
     uint64_t* empty = full + NW * SW;
     float* inv1 = reinterpret_cast<float*>(smem + p.round_off);
     int* rows1 = reinterpret_cast<int*>(smem + p.round_off + 32);
-    int* npend = reinterpret_cast<int*>(smem + p.round_off + 64);      // [16]
     int4* pending = reinterpret_cast<int4*>(smem + p.seg_off);         // [NW][pw] {problem, row block, split, k}
-    int* lastf = reinterpret_cast<int*>(smem + p.last_off);            // [NW][pw]
     uint8_t* xb0 = smem + p.xraw_off;
     uint8_t* xb1 = smem + p.xraw1_off;
     uint8_t* ring = smem + p.stage_off;
@@ -1235,8 +1234,6 @@ __global__ void __launch_bounds__(kThreads, 1) qproj_warp_kernel(const __grid_co
         flags[2] = 0;  // a staged value has no exact fp16 copy
         fence_mbar_init();
     }
-    if (threadIdx.x < 16)
-        npend[threadIdx.x] = 0;
     __syncthreads();
     pdl_launch_dependents();
 
@@ -1503,8 +1500,43 @@ __global__ void __launch_bounds__(kThreads, 1) qproj_warp_kernel(const __grid_co
                 }
             }
         }
-        if (lane == 0)
-            npend[cw] = np;
+        // publish the worker's partial slots: one acquire-release count per row block
+        // (after the warp barrier, so every lane's slot stores are covered); the worker
+        // whose count completes a row block sums its slots in fixed order and stores it
+        if (alive && np > 0) {
+            __syncwarp();
+            for (int j0 = 0; j0 < np; j0 += 32) {
+                const int j = j0 + lane;
+                bool last = false;
+                int4 e = make_int4(0, 0, 0, 0);
+                if (j < np) {
+                    e = pending[cw * p.pw + j];
+                    int expected = S;
+                    if (!pt.aligned) {
+                        expected = 0;
+                        for (int s2 = 0; s2 < S; ++s2)
+                            expected += pt.contributors((int64_t)e.x * pt.per_p + (int64_t)s2 * pt.per_ps +
+                                                        (int64_t)e.y * p.Gs);
+                    }
+                    const unsigned old = atom_add_acq_rel_gpu(
+                        reinterpret_cast<unsigned*>(&p.counters[(int64_t)e.x * p.n_rb + e.y]), 1u);
+                    last = old == (unsigned)(expected - 1);
+                }
+                unsigned mask = __ballot_sync(0xffffffffu, last);
+                while (mask) {
+                    const int src = __ffs(mask) - 1;
+                    mask &= mask - 1;
+                    const int px = __shfl_sync(0xffffffffu, e.x, src), ry = __shfl_sync(0xffffffffu, e.y, src);
+                    __syncwarp();
+                    float t0[4] = {0.f, 0.f, 0.f, 0.f}, t1[4] = {0.f, 0.f, 0.f, 0.f};
+                    sum_partials<DUAL>(p, pt, px, ry, lane, t0, t1);
+                    const int Mr = MOE ? slot_ec[px].y : p.M;
+                    store_outputs<DUAL, MOE>(p, px, Mr, ry * kRowsPerBlock, lane, t0, t1);
+                    if (lane == 0)
+                        p.counters[(int64_t)px * p.n_rb + ry] = 0;
+                }
+            }
+        }
     }
 
     // abort is decided once for the whole CTA
@@ -1519,44 +1551,6 @@ __global__ void __launch_bounds__(kThreads, 1) qproj_warp_kernel(const __grid_co
                 mbar_wait_bounded(&xbar[1], 0, p.limit_ns);
         }
         return;
-    }
-
-    // ------------------------------------------------------------ last contributor of a row block sums it
-    int total = 0;
-    for (int w = 0; w < NW; ++w)
-        total += npend[w];
-    if (total == 0)
-        return;
-    __threadfence();
-    named_bar_sync(kBarConsumers, kConsumerWarps * 32);
-    for (int i = threadIdx.x; i < NW * p.pw; i += kConsumerWarps * 32) {
-        const int w = i / p.pw, j = i % p.pw;
-        int last = 0;
-        if (j < npend[w]) {
-            const int4 e = pending[i];
-            int expected = S;
-            if (!pt.aligned) {
-                expected = 0;
-                for (int s2 = 0; s2 < S; ++s2)
-                    expected += pt.contributors((int64_t)e.x * pt.per_p + (int64_t)s2 * pt.per_ps + (int64_t)e.y * p.Gs);
-            }
-            const int old = atomicAdd(&p.counters[(int64_t)e.x * p.n_rb + e.y], 1);
-            last = old == expected - 1;
-        }
-        lastf[i] = last;
-    }
-    named_bar_sync(kBarConsumers, kConsumerWarps * 32);
-    for (int i = cw; i < NW * p.pw; i += kConsumerWarps) {
-        if (!lastf[i])
-            continue;
-        const int4 e = pending[i];
-        __threadfence();
-        float t0[4] = {0.f, 0.f, 0.f, 0.f}, t1[4] = {0.f, 0.f, 0.f, 0.f};
-        sum_partials<DUAL>(p, pt, e.x, e.y, lane, t0, t1);
-        const int Mr = MOE ? slot_ec[e.x].y : p.M;
-        store_outputs<DUAL, MOE>(p, e.x, Mr, e.y * kRowsPerBlock, lane, t0, t1);
-        if (lane == 0)
-            p.counters[(int64_t)e.x * p.n_rb + e.y] = 0;
     }
 }
 
