@@ -441,9 +441,12 @@ Plan plan_qproj(int n_rb, int groups, int mats, int bits, int slots, int k_full,
         pl.xraw_off = (int)align_up(pl.gamma_off + (size_t)std::max(k_full, 0) * 2, 128);
         const int xcols = norm ? k_full : pl.Gs * kGroup;
         pl.x_rs = xcols * 2 + 16;
-        // all 8 rows of each buffer (the rows past M are zero-filled)
-        pl.xraw1_off = (int)align_up(pl.xraw_off + (size_t)kMaxM * pl.x_rs, 128);
-        pl.stage_off = (int)align_up(pl.xraw1_off + (two_bufs ? (size_t)kMaxM * pl.x_rs : 0), 128);
+        // M rows of each buffer and a zero row that the fragment loads of rows M..7 read
+        // (8 rows for MoE, whose problems stage up to 8); only the ring depth below
+        // depends on M, never the partition, so a row's result does not
+        const int xrows = std::min(rows + 1, kMaxM);
+        pl.xraw1_off = (int)align_up(pl.xraw_off + (size_t)xrows * pl.x_rs, 128);
+        pl.stage_off = (int)align_up(pl.xraw1_off + (two_bufs ? (size_t)xrows * pl.x_rs : 0), 128);
         const size_t budget = 227 * 1024;
         int SW = budget > pl.stage_off + 2 * nw * slot ? (int)((budget - pl.stage_off) / (nw * slot)) : 1;
         SW = std::min(SW, kMaxStages);

@@ -582,15 +582,20 @@ __device__ __forceinline__ void x_frag(const uint8_t* buf, int x_rs, int gi, int
 
 // B fragments of group g_rel of a buffer whose 8 rows are all staged (rows >= M
 // zero-filled): the same two ldmatrix as x_frag, without the row clamp.
-__device__ __forceinline__ void x_frag8(const uint8_t* buf, int x_rs, int lane, int g_rel, uint4& xa, uint4& xb)
+__device__ __forceinline__ void x_frag8_row(const uint8_t* xrow, int lane, int g_rel, uint4& xa, uint4& xb)
 {
-    const uint32_t a = smem_u32(buf + (lane & 7) * x_rs + g_rel * 128 + (lane >> 3) * 16);
+    const uint32_t a = smem_u32(xrow + g_rel * 128 + (lane >> 3) * 16);
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
                  : "=r"(xa.x), "=r"(xa.y), "=r"(xa.z), "=r"(xa.w)
                  : "r"(a));
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
                  : "=r"(xb.x), "=r"(xb.y), "=r"(xb.z), "=r"(xb.w)
                  : "r"(a + 64));
+}
+
+__device__ __forceinline__ void x_frag8(const uint8_t* buf, int x_rs, int lane, int g_rel, uint4& xa, uint4& xb)
+{
+    x_frag8_row(buf + (lane & 7) * x_rs, lane, g_rel, xa, xb);
 }
 
 // True when some bf16 value in rows [0, rows) of a staged buffer (cols columns) has
@@ -1150,18 +1155,19 @@ __global__ void __launch_bounds__((NWT + 1) * 32, NWT == 8 ? 2 : 1) qproj_kernel
 
 // One chunk of a warp worker: cnt tiles of one row block (and, for gate + up, the
 // matching tiles of the second matrix T tiles further), groups g0.. of the staged
-// buffer, group sums from xs0; a single matrix takes two tiles per iteration into
-// separate accumulators (gate and up are two independent chains already).
+// buffer (xrow: the lane's activation row, lane & 7, or the zero row past M), group
+// sums from xs0; a single matrix takes two tiles per iteration into separate
+// accumulators (gate and up are two independent chains already).
 template <int BITS, bool DUAL, bool F16>
-__device__ __forceinline__ void warp_chunk(const uint8_t* sb, const uint8_t* xb, const float* xs, int x_rs, int lane,
-                                           int tq, int g0, int xs0, int cnt, int T, float (&acc0)[4], float (&acc1)[4])
+__device__ __forceinline__ void warp_chunk(const uint8_t* sb, const uint8_t* xrow, const float* xs, int lane, int tq,
+                                           int g0, int xs0, int cnt, int T, float (&acc0)[4], float (&acc1)[4])
 {
     constexpr int TILE = tile_bytes_for(BITS);
     int j = 0;
     for (; !DUAL && j + 1 < cnt; j += 2) {
         uint4 xa, xbv, ya, ybv;
-        x_frag8(xb, x_rs, lane, g0 + j, xa, xbv);
-        x_frag8(xb, x_rs, lane, g0 + j + 1, ya, ybv);
+        x_frag8_row(xrow, lane, g0 + j, xa, xbv);
+        x_frag8_row(xrow, lane, g0 + j + 1, ya, ybv);
         const float2 xsv = *reinterpret_cast<const float2*>(xs + (xs0 + j) * kMaxM + 2 * tq);
         const float2 ysv = *reinterpret_cast<const float2*>(xs + (xs0 + j + 1) * kMaxM + 2 * tq);
         tile_mac_x<BITS, F16>(sb + j * TILE, lane, xa, xbv, xsv, acc0);
@@ -1169,7 +1175,7 @@ __device__ __forceinline__ void warp_chunk(const uint8_t* sb, const uint8_t* xb,
     }
     for (; j < cnt; ++j) {
         uint4 xa, xbv;
-        x_frag8(xb, x_rs, lane, g0 + j, xa, xbv);
+        x_frag8_row(xrow, lane, g0 + j, xa, xbv);
         const float2 xsv = *reinterpret_cast<const float2*>(xs + (xs0 + j) * kMaxM + 2 * tq);
         tile_mac_x<BITS, F16>(sb + j * TILE, lane, xa, xbv, xsv, acc0);
         if constexpr (DUAL)
@@ -1358,14 +1364,16 @@ __global__ void __launch_bounds__(kThreads, 1) qproj_warp_kernel(const __grid_co
     const int xg0_0 = norm ? 0 : (run0 % S) * p.Gs, xg0_1 = (run1 % S) * p.Gs;
     const int xgc = norm ? p.groups : p.Gs;
     bool alive = ca < cb && !flags[0];
-    // rows M..7 of each activation buffer read as zero (no per-tile row clamp); the
-    // bulk copies write only rows below M, and x_prepare's closing barrier orders
-    // these stores before any fragment load
-    for (int i = (cw * 32 + lane) * 16 + M0 * p.x_rs; i < kMaxM * p.x_rs; i += kConsumerWarps * 32 * 16)
-        *reinterpret_cast<uint4*>(xb0 + i) = make_uint4(0u, 0u, 0u, 0u);
-    if (two)
-        for (int i = (cw * 32 + lane) * 16 + M1 * p.x_rs; i < kMaxM * p.x_rs; i += kConsumerWarps * 32 * 16)
-            *reinterpret_cast<uint4*>(xb1 + i) = make_uint4(0u, 0u, 0u, 0u);
+    // row M of each activation buffer (allocated when M < 8) is a zero row that the
+    // fragment loads of rows M..7 read (no per-tile row clamp); the bulk copies write
+    // only rows below M, and x_prepare's closing barrier orders these stores before
+    // any fragment load
+    if (M0 < kMaxM)
+        for (int i = (cw * 32 + lane) * 16; i < p.x_rs; i += kConsumerWarps * 32 * 16)
+            *reinterpret_cast<uint4*>(xb0 + M0 * p.x_rs + i) = make_uint4(0u, 0u, 0u, 0u);
+    if (two && M1 < kMaxM)
+        for (int i = (cw * 32 + lane) * 16; i < p.x_rs; i += kConsumerWarps * 32 * 16)
+            *reinterpret_cast<uint4*>(xb1 + M1 * p.x_rs + i) = make_uint4(0u, 0u, 0u, 0u);
     if (cw == 0) {
         __syncwarp();
         if (lane == 0 && alive) {
@@ -1425,7 +1433,7 @@ __global__ void __launch_bounds__(kThreads, 1) qproj_warp_kernel(const __grid_co
             while (u < u1 && alive) {
                 const int len = (int)min((int64_t)(p.Gs - gl), u1 - u);
                 const bool b1 = two && (pp * S + ss) == run1;
-                const uint8_t* xb = b1 ? xb1 : xb0;
+                const uint8_t* xrow = (b1 ? xb1 : xb0) + min(lane & 7, b1 ? M1 : M0) * p.x_rs;
                 const float* xs = b1 ? xs1 : xs0;
                 const int Mr = MOE ? slot_ec[pp].y : p.M;
                 const int grel0 = norm ? ss * p.Gs + gl : gl;  // group of the buffer at the segment start
@@ -1441,9 +1449,9 @@ __global__ void __launch_bounds__(kThreads, 1) qproj_warp_kernel(const __grid_co
                     const uint8_t* sb = ring + s * slot_bytes;
                     const int xs0 = norm ? ss * p.Gs + gl + g : gl + g;  // group sums of the chunk start
                     if (f16)
-                        warp_chunk<BITS, DUAL, true>(sb, xb, xs, p.x_rs, lane, tq, grel0 + g, xs0, cnt, T, acc0, acc1);
+                        warp_chunk<BITS, DUAL, true>(sb, xrow, xs, lane, tq, grel0 + g, xs0, cnt, T, acc0, acc1);
                     else
-                        warp_chunk<BITS, DUAL, false>(sb, xb, xs, p.x_rs, lane, tq, grel0 + g, xs0, cnt, T, acc0, acc1);
+                        warp_chunk<BITS, DUAL, false>(sb, xrow, xs, lane, tq, grel0 + g, xs0, cnt, T, acc0, acc1);
                     __syncwarp();
                     if (lane == 0)
                         mbar_arrive(&empty[s]);
