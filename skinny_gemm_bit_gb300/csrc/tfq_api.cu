@@ -234,7 +234,7 @@ Plan plan_qproj(int n_rb, int groups, int mats, int bits, int slots, int k_full,
     // warp workers over K splits of at most 40 groups, 8 workers a CTA (on GB300 this
     // measured 12.8 / 14.8 us at M = 1 / 8 for K = 12800, N = 2560, against 14.6 / 17.0
     // for lock-step teams over two splits)
-    const bool nvfp4 = bits == kNvfp4;  // warp workers only
+    const bool nvfp4 = bits == kNvfp4;  // no streaming schedule
     const bool long_plain = slots == 1 && mats == 1 && k_full == 0 && groups >= 64 && n_rb <= 2 * sms &&
                             (double)n_rb * groups * tile > 8.0 * 1024 * 1024 && g_tune[TF_TUNE_MODE] <= 0;
     int S = 1;
@@ -324,7 +324,6 @@ Plan plan_qproj(int n_rb, int groups, int mats, int bits, int slots, int k_full,
     bool light = light_ok && g_tune[TF_TUNE_MODE] <= 0;
     if (g_tune[TF_TUNE_MODE] == 3 || g_tune[TF_TUNE_MODE] == 4)
         light = light_ok;
-    light = light && !nvfp4;
     if (light) {
         pl.nw = 8;
         pl.C = (int)std::max<int64_t>(items, 1);
@@ -377,10 +376,8 @@ Plan plan_qproj(int n_rb, int groups, int mats, int bits, int slots, int k_full,
     bool warp_mode = (long_plain || (!long_rows && U >= 4 * W)) && upc_max_all <= per_ps;
     if (g_tune[TF_TUNE_MODE] > 0)
         warp_mode = g_tune[TF_TUNE_MODE] == 2 && upc_max_all <= per_ps;
-    if (nvfp4)
-        warp_mode = upc_max_all <= per_ps;
     // the activation buffers (two unless a single problem and split, or an RMSNorm)
-    // and two ring slots per worker must fit, else lock-step teams (NVFP4: fewer workers)
+    // and two ring slots per worker must fit, else lock-step teams
     auto warp_fits = [&](int nw_) {
         const bool norm_rows = k_full > 0;
         const int bufs = (!norm_rows && (int64_t)slots * S > 1) ? 2 : 1;
@@ -390,9 +387,6 @@ Plan plan_qproj(int n_rb, int groups, int mats, int bits, int slots, int k_full,
                             (size_t)2 * nw_ * mats * std::min(Tw, pl.Gs) * tile;
         return need <= 227 * 1024;
     };
-    if (warp_mode && nvfp4)
-        while (nw > 1 && !warp_fits(nw))
-            nw /= 2;
     if (warp_mode) {
         warp_mode = warp_fits(nw);
         W = (int64_t)sms * nw;
@@ -456,8 +450,6 @@ Plan plan_qproj(int n_rb, int groups, int mats, int bits, int slots, int k_full,
         pl.smem = pl.stage_off + (size_t)nw * pl.nst * slot;
         pl.KW = 1;
         pl.R = nw;
-    } else if (nvfp4) {
-        pl.mode = -1;
     }
 
     const bool partials = S > 1 || !pl.aligned;
@@ -689,9 +681,6 @@ static int qlinear_impl(const tf_qweight* w, const tf_qweight* w_up, const uint1
     const bool dual = w_up != nullptr;
     const Plan pl = plan_qproj((int)(w->n_pad / 16), (int)(w->K / kGroup), dual ? 2 : 1, kernel_bits(w), 1,
                                gamma != nullptr ? (int)w->K : 0, (int)M);
-    if (pl.mode < 0)
-        return fail(TF_E_UNSUPPORTED_SHAPE, "%s: NVFP4 weights run on warp workers, which this shape does not fit",
-                    name);
     if (pl.smem > 227 * 1024)
         return fail(TF_E_UNSUPPORTED_SHAPE,
                     gamma != nullptr ? "%s: K too large for the RMSNorm prologue (rows do not fit on chip)"

@@ -97,8 +97,7 @@ struct QProjParams {
 };
 
 struct Plan {
-    int mode;  // 0: teams in lock-step (latency-bound calls), 1: warp workers, 2: streaming (one large matrix),
-               // -1: none fits (NVFP4 weights run on warp workers only)
+    int mode;  // 0: teams in lock-step (latency-bound calls), 1: warp workers, 2: streaming (one large matrix)
     int KW, R, S, Gs, cg, nst, C, aligned, kmax, segmax, slots;
     int red_off, seg_off, round_off, last_off, xraw_off, x_rs, stage_off;
     int nw, pw, xsum1_off, xraw1_off, gamma_off;

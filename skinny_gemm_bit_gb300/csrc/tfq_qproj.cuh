@@ -87,10 +87,11 @@ __device__ __forceinline__ float warp_sum(float v)
     return v;
 }
 
-// One 16x64 tile against the B fragments (xa, xb) and group sums (xs) of its group.
+// One 16x64 tile of affine codes against the B fragments (xa, xb) and group sums (xs)
+// of its group.
 template <int BITS>
-__device__ __forceinline__ void tile_mac(const uint8_t* tile, int lane, const uint4& xa, const uint4& xb,
-                                         const float2& xs, float (&acc)[4])
+__device__ __forceinline__ void tile_mac_affine(const uint8_t* tile, int lane, const uint4& xa, const uint4& xb,
+                                                const float2& xs, float (&acc)[4])
 {
     constexpr int QB = tile_q_bytes_for(BITS);
     const uint2 sb = *reinterpret_cast<const uint2*>(tile + QB + (lane >> 2) * 8);
@@ -165,7 +166,7 @@ __device__ __forceinline__ void tile_mac_chain(const uint8_t* tile, int lane, co
         acc[2] = fmaf(s_hi, d[2], fmaf(c_hi, xs.x, acc[2]));
         acc[3] = fmaf(s_hi, d[3], fmaf(c_hi, xs.y, acc[3]));
     } else {
-        tile_mac<BITS>(tile, lane, xa, xb, xs, acc);
+        tile_mac_affine<BITS>(tile, lane, xa, xb, xs, acc);
     }
 }
 
@@ -246,6 +247,17 @@ __device__ __forceinline__ void tile_mac_nvfp4(const uint8_t* tile, int lane, co
             mma_bf16_16816(acc, f16x2_to_bf16x2(a0), f16x2_to_bf16x2(a1), f16x2_to_bf16x2(a2), f16x2_to_bf16x2(a3),
                            b0[kb], b1[kb]);
     }
+}
+
+// One tile on bf16 activations, any code (the lock-step team schedules).
+template <int BITS>
+__device__ __forceinline__ void tile_mac(const uint8_t* tile, int lane, const uint4& xa, const uint4& xb,
+                                         const float2& xs, float (&acc)[4])
+{
+    if constexpr (BITS == kNvfp4)
+        tile_mac_nvfp4<false>(tile, lane, xa, xb, acc);
+    else
+        tile_mac_affine<BITS>(tile, lane, xa, xb, xs, acc);
 }
 
 template <int BITS, bool F16>
@@ -1072,6 +1084,15 @@ __global__ void __launch_bounds__((NWT + 1) * 32, NWT == 8 ? 2 : 1) qproj_kernel
                         acc1[3] += o1.w;
                     }
                 }
+            }
+        }
+
+        if constexpr (BITS == kNvfp4) {  // the matrices' global scales
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                acc0[i] *= p.wscale0;
+                if constexpr (DUAL)
+                    acc1[i] *= p.wscale1;
             }
         }
 

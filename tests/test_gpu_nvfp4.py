@@ -170,8 +170,8 @@ def test_activation_edges(T, case):
 
 @pytest.mark.parametrize("warps,chunk", [(8, 8), (16, 4), (4, 16)])
 def test_worker_shapes_match(T, warps, chunk):
-    # workers a CTA and tiles a chunk as tuned (the planner halves the workers until
-    # their ring slots fit: 16 do not at K = 12800 with two staged K splits)
+    # workers a CTA and tiles a chunk as tuned (16 workers' ring slots do not fit at
+    # K = 12800 with two staged K splits: the planner falls back to lock-step teams)
     rng = np.random.default_rng(350 + warps)
     M, K, N = 8, 12800, 2560
     w = synth.nvfp4_weights(rng, N, K)
@@ -200,3 +200,30 @@ def test_rows_are_independent_bit_exact(T):
     for m in (0, 5):
         y1 = T.tf_qlinear_run(qw, dev_bf16(x[m:m + 1]), gamma=dev_bf16(g), eps=1e-6)
         assert torch.equal(y1[0].view(torch.int16), y8[m].view(torch.int16)), m
+
+
+@pytest.mark.parametrize("mode", [-1, 1, 2, 3, 4])
+@pytest.mark.parametrize("M,K,N,dual", [(1, 1024, 3072, False), (8, 12800, 2560, False), (8, 1024, 3072, True),
+                                        (3, 640, 1000, True)])
+def test_every_schedule_matches(T, mode, M, K, N, dual):
+    # the planner's choice, lock-step teams, warp workers, light teams with register-loaded
+    # and with bulk-copied activations: NVFP4 tiles in the bf16 and fp16 tile math
+    rng = np.random.default_rng(370 + M + N + mode)
+    w = synth.nvfp4_weights(rng, N, K)
+    x = x_bf16(rng, M, K)
+    T.tune_set(T.TF_TUNE_MODE, mode)
+    try:
+        if dual:
+            u = synth.nvfp4_weights(rng, N, K)
+            g = synth.gamma(rng, K)
+            h = T.tf_qmlp_gateup_run(pack4(T, w), pack4(T, u), dev_bf16(x), gamma=dev_bf16(g), eps=1e-6)
+        else:
+            y = T.tf_qlinear_run(pack4(T, w), dev_bf16(x), out_dtype=torch.float32)
+    finally:
+        T.tune_set(T.TF_TUNE_MODE, -1)
+    if dual:
+        ref = oracle.gateup(oracle.bf16_to_f64(x), w, u, oracle.bf16_to_f64(g), 1e-6)
+        assert_close(host_f64(h), ref["h"], tol_swiglu(ref["g"], ref["u"], ref["g_abs"], ref["u_abs"]), f"mode {mode}")
+    else:
+        y_ref, ad = oracle.qlinear(oracle.bf16_to_f64(x), w)
+        assert_close(host_f64(y), y_ref, tol_linear(ad), f"mode {mode}")
