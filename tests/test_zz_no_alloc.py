@@ -88,3 +88,16 @@ def test_noalloc_refuses_a_shape_beyond_the_fixed_scratch(T):
     assert rc == T.TF_E_WORKSPACE_TOO_SMALL
     msg = T.lib().tf_last_error().decode()
     assert "4194304" in msg and "tf_qlinear_run" in msg, msg
+
+
+@pytest.mark.parametrize("M,K,N", [(8, 12800, 2560), (1, 1024, 3072)])
+def test_noalloc_nvfp4_matches_workspace_call(T, M, K, N):
+    # NVFP4 descriptors through the fixed-array entry point: the same kernels, the same bits
+    rng = np.random.default_rng(7200 + M)
+    w = synth.nvfp4_weights(rng, N, K)
+    x = dev_bf16(synth.activations(rng, M, K))
+    qw = T.tf_qlinear_pack_nvfp4(w["codes"], w["scales"], float(w["gscale"]))
+    y_ws = T.tf_qlinear_run(qw, x)
+    y = T.tf_qlinear_run_noalloc(qw, x)
+    torch.cuda.synchronize()
+    assert torch.equal(y.view(torch.int16), y_ws.view(torch.int16))
