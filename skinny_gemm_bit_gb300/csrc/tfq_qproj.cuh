@@ -1340,6 +1340,14 @@ __global__ void __launch_bounds__(kThreads, 1) qproj_warp_kernel(const __grid_co
                             ok = false;
                             break;
                         }
+                        // a worker's second chunk is requested once its first has landed: every
+                        // CTA requests its whole ring at the start, and without this the first
+                        // chunks land only when that burst has drained (readout M=1: 20.8 ->
+                        // 19.9 us)
+                        if (k == 1 && !wait_or_abort(&full[lane * SW], 0u, flags, p.status, p.limit_ns)) {
+                            ok = false;
+                            break;
+                        }
                         mbar_arrive_expect_tx(&full[s], (uint32_t)(MATS * cnt * TILE));
 #pragma unroll
                         for (int mat = 0; mat < MATS; ++mat)
