@@ -21,8 +21,10 @@
  * fp32 scale per matrix (TensorFold page, "qualified" model table: NVFP4
  * checkpoints; the pages give no layout, the format read here is NVIDIA's
  * published NVFP4, weights only: activations stay bf16). tf_qlinear_run,
- * tf_qlinear_run_rht, tf_qlinear_run_noalloc and tf_qmlp_gateup_run accept it;
- * the MoE, decoder-step and embedding calls return TF_E_UNSUPPORTED_SHAPE.
+ * tf_qlinear_run_rht, tf_qlinear_run_noalloc, tf_qmlp_gateup_run,
+ * tf_decode_step_run (every matrix of the decoder in the one code; not the
+ * single-kernel step of TF_TUNE_CHAIN = 2), tf_embed_rows and tf_generate_greedy
+ * accept it; tf_qmoe_run returns TF_E_UNSUPPORTED_SHAPE.
  *
  * Conventions shared by every call:
  *   - Pointers named x, y, h, logits, residual, gamma, ws, packed and the

@@ -316,8 +316,11 @@ def decode_step(x, layers, final_norm, readout: dict, q_dim: int, eps: float = 1
     ro = readout
     if readout_rows is not None:
         rows = np.asarray(readout_rows)
-        ro = {"wq": readout["wq"][rows], "scales": readout["scales"][rows],
-              "biases": readout["biases"][rows], "N": len(rows), "K": readout["K"],
-              "bits": readout["bits"]}
+        if is_nvfp4(readout):
+            ro = dict(readout, codes=readout["codes"][rows], scales=readout["scales"][rows], N=len(rows))
+        else:
+            ro = {"wq": readout["wq"][rows], "scales": readout["scales"][rows],
+                  "biases": readout["biases"][rows], "N": len(rows), "K": readout["K"],
+                  "bits": readout["bits"]}
     logits, l_abs = qlinear(xf, ro)
     return {"stages": stages, "h": h, "xf": xf, "logits": logits, "logits_abs": l_abs}

@@ -82,13 +82,12 @@ const uint8_t* tiles_of(const tf_qweight* w)
 
 size_t plan_scratch(const Plan& p) { return p.ws_counters + p.ws_partials; }
 
-// For the calls whose kernels read MLX affine codes only.
+// For the calls whose kernels read MLX affine codes only (the MoE layer).
 int check_affine(const tf_qweight* w, const char* name)
 {
     int rc = check_desc(w, name);
     if (rc == TF_OK && w->code != TF_CODE_AFFINE)
-        rc = fail(TF_E_UNSUPPORTED_SHAPE,
-                  "%s: NVFP4 weights are accepted by tf_qlinear_run(_rht/_noalloc) and tf_qmlp_gateup_run only", name);
+        rc = fail(TF_E_UNSUPPORTED_SHAPE, "%s: the MoE layer takes MLX affine codes only (not NVFP4)", name);
     return rc;
 }
 
@@ -471,7 +470,6 @@ int report_error(int status, const char* fmt, ...)
 }
 
 int validate_desc(const tf_qweight* w, const char* name) { return check_desc(w, name); }
-int validate_affine(const tf_qweight* w, const char* name) { return check_affine(w, name); }
 
 }  // namespace tfq
 
@@ -950,10 +948,14 @@ int check_decoder(const tf_decoder_desc* d, int64_t M, const char* name)
     int rc;
     for (int l = 0; l < d->n_layers; ++l) {
         const tf_decoder_layer& L = d->layers[l];
-        if ((rc = check_affine(&L.qkv, "qkv")) || (rc = check_affine(&L.o, "o")) ||
-            (rc = check_affine(&L.gate, "gate")) || (rc = check_affine(&L.up, "up")) ||
-            (rc = check_affine(&L.down, "down")))
+        if ((rc = check_desc(&L.qkv, "qkv")) || (rc = check_desc(&L.o, "o")) || (rc = check_desc(&L.gate, "gate")) ||
+            (rc = check_desc(&L.up, "up")) || (rc = check_desc(&L.down, "down")))
             return rc;
+        // one weight code for the whole step (the workspace is planned from layer 0)
+        const int code = d->layers[0].qkv.code;
+        if (L.qkv.code != code || L.o.code != code || L.gate.code != code || L.up.code != code ||
+            L.down.code != code || d->readout.code != code)
+            return fail(TF_E_UNSUPPORTED_SHAPE, "%s: layer %d mixes weight codes", name, l);
         if (L.qkv.N != Q + 2 * KV || L.qkv.K != D || L.o.N != D || L.o.K != Q || L.gate.N != F || L.gate.K != D ||
             L.up.N != F || L.up.K != D || L.down.N != D || L.down.K != F || L.gate.bits != L.up.bits ||
             L.qkv.batch != 1 || L.o.batch != 1 || L.gate.batch != 1 || L.up.batch != 1 || L.down.batch != 1)
@@ -961,7 +963,7 @@ int check_decoder(const tf_decoder_desc* d, int64_t M, const char* name)
         if (L.attn_norm == nullptr || L.mlp_norm == nullptr || !aligned(L.attn_norm, 16) || !aligned(L.mlp_norm, 16))
             return fail(TF_E_INVALID_ARG, "%s: layer %d norm weights NULL or misaligned", name, l);
     }
-    if ((rc = check_affine(&d->readout, "readout")))
+    if ((rc = check_desc(&d->readout, "readout")))
         return rc;
     if (d->readout.N != d->vocab || d->readout.K != D || d->readout.batch != 1)
         return fail(TF_E_UNSUPPORTED_SHAPE, "%s: readout must be [vocab][d_model]", name);
@@ -978,12 +980,12 @@ StepLayout step_layout(const tf_decoder_desc* d, int64_t M)
     (void)bits;
     if (d->n_layers > 0) {
         const tf_decoder_layer& l0 = d->layers[0];
-        L.p_qkv = plan_qproj((int)(l0.qkv.n_pad / 16), D / kGroup, 1, l0.qkv.bits, 1, 0, kMaxM);
-        L.p_o = plan_qproj((int)(l0.o.n_pad / 16), Q / kGroup, 1, l0.o.bits, 1, 0, kMaxM);
-        L.p_gu = plan_qproj((int)(l0.gate.n_pad / 16), D / kGroup, 2, l0.gate.bits, 1, 0, kMaxM);
-        L.p_dn = plan_qproj((int)(l0.down.n_pad / 16), F / kGroup, 1, l0.down.bits, 1, 0, kMaxM);
+        L.p_qkv = plan_qproj((int)(l0.qkv.n_pad / 16), D / kGroup, 1, kernel_bits(&l0.qkv), 1, 0, kMaxM);
+        L.p_o = plan_qproj((int)(l0.o.n_pad / 16), Q / kGroup, 1, kernel_bits(&l0.o), 1, 0, kMaxM);
+        L.p_gu = plan_qproj((int)(l0.gate.n_pad / 16), D / kGroup, 2, kernel_bits(&l0.gate), 1, 0, kMaxM);
+        L.p_dn = plan_qproj((int)(l0.down.n_pad / 16), F / kGroup, 1, kernel_bits(&l0.down), 1, 0, kMaxM);
     }
-    L.p_ro = plan_qproj((int)(d->readout.n_pad / 16), D / kGroup, 1, d->readout.bits, 1, 0, kMaxM);
+    L.p_ro = plan_qproj((int)(d->readout.n_pad / 16), D / kGroup, 1, kernel_bits(&d->readout), 1, 0, kMaxM);
     L.qkv_e = (size_t)kMaxM * (Q + 2 * KV);
     L.h_e = (size_t)kMaxM * D;
     L.a_e = (size_t)kMaxM * F;
@@ -1060,7 +1062,8 @@ int tf_decode_step_run(const tf_decoder_desc* d, const uint16_t* x, int64_t M, u
     // its grid-wide stage barriers cost more than the kernel boundaries of the chain of
     // projections with programmatic dependent launch, which is therefore the default
     int bits = d->readout.bits;
-    bool chain = g_tune[TF_TUNE_CHAIN] == 2 && d->n_layers <= kChainMaxLayers && D <= 1024 &&
+    bool chain = g_tune[TF_TUNE_CHAIN] == 2 && d->readout.code == TF_CODE_AFFINE && d->n_layers <= kChainMaxLayers &&
+                 D <= 1024 &&
                  std::max<int64_t>(D, std::max<int64_t>(Q, F)) <= (int64_t)kChainMaxGroups * kGroup &&
                  d->vocab <= INT32_MAX;
     for (int l = 0; chain && l < d->n_layers; ++l) {

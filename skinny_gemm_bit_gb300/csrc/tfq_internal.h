@@ -153,7 +153,6 @@ Plan plan_qproj(int n_rb, int groups, int mats, int bits, int slots, int k_full,
 // Error reporting and descriptor validation shared by the entry points (tfq_api.cu).
 int report_error(int status, const char* fmt, ...);
 int validate_desc(const tf_qweight* w, const char* name);
-int validate_affine(const tf_qweight* w, const char* name);  // validate_desc, and MLX affine codes only
 
 // launchers (tfq_qproj_b*_*.cu, one instantiation unit per bit width and matrix count)
 cudaError_t launch_qproj_b4_single(bool moe, const Plan& plan, const QProjParams& p, cudaStream_t stream, bool pdl);
@@ -189,7 +188,10 @@ cudaError_t launch_moe_route(const float* logits, int M, int E, int top_k, int32
 cudaError_t launch_moe_combine(const MoeMeta* meta, const float* o, int M, int top_k, int H, uint16_t* y,
                                cudaStream_t stream);
 cudaError_t launch_timeout_probe(int* status, uint64_t limit_ns, cudaStream_t stream);
-cudaError_t launch_embed_rows(const uint8_t* packed, int64_t N, int64_t K, int bits, const int32_t* ids, int64_t M,
-                              uint16_t* x, int64_t ldx, int* status, cudaStream_t stream);
+// bits: the kernels' BITS value (kNvfp4 for NVFP4, whose matrix scale is gscale)
+cudaError_t launch_embed_rows(const uint8_t* packed, int64_t N, int64_t K, int bits, float gscale, const int32_t* ids,
+                              int64_t M, uint16_t* x, int64_t ldx, int* status, cudaStream_t stream);
+// The kernels' BITS value of a descriptor's weight code.
+inline int desc_kernel_bits(const tf_qweight* w) { return w->code == TF_CODE_NVFP4 ? kNvfp4 : w->bits; }
 
 }  // namespace tfq

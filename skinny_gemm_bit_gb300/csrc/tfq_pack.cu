@@ -25,6 +25,7 @@
 #include <cuda_bf16.h>
 
 #include "tfq_internal.h"
+#include "tfq_ptx.cuh"
 
 namespace tfq {
 namespace {
@@ -162,9 +163,11 @@ __global__ void unpack_scales_kernel(const uint8_t* __restrict__ packed, int64_t
 
 // Rows of a packed matrix (batch 0) dequantised to bf16: x[m][k] = bf16(s q + b) of
 // row ids[m], column k, rounded to nearest even (s q + b is exact in fp32 whenever
-// |b| / |s| < 2^15, so the rounding is that of the exact value). An id outside
-// [0, N) records TF_E_INVALID_ARG in *status and gives a zero row.
-__global__ void embed_rows_kernel(const uint8_t* __restrict__ packed, int64_t N, int64_t K, int bits,
+// |b| / |s| < 2^15, so the rounding is that of the exact value). NVFP4 (bits ==
+// kNvfp4): bf16(gscale * (e4m3 scale * e2m1 code)), the inner product exact in fp32, so
+// the fp32 value is the exact product rounded once. An id outside [0, N) records
+// TF_E_INVALID_ARG in *status and gives a zero row.
+__global__ void embed_rows_kernel(const uint8_t* __restrict__ packed, int64_t N, int64_t K, int bits, float gscale,
                                   const int32_t* __restrict__ ids, int64_t M, uint16_t* __restrict__ x, int64_t ldx,
                                   int* status)
 {
@@ -180,6 +183,17 @@ __global__ void embed_rows_kernel(const uint8_t* __restrict__ packed, int64_t N,
         if (row < 0 || row >= N) {
             if (k == 0)
                 atomicCAS(status, 0, TF_E_INVALID_ARG);
+        } else if (bits == kNvfp4) {
+            const int rr = (int)(row % kRowsPerBlock), c = (int)(k % kGroup), cc = c & 15, kb = c >> 4;
+            const uint8_t* tb = reinterpret_cast<const uint8_t*>(tiles) +
+                                ((row / kRowsPerBlock) * G + k / kGroup) * (int64_t)tile_bytes_for(kNvfp4);
+            const int lane = (rr & 7) * 4 + ((cc & 7) >> 1), r = (rr >> 3) + 2 * (cc >> 3);
+            uint32_t q2, u1, u2, u3;  // the byte's two codes as an fp16 pair, even column low
+            e2m1x8_to_f16x2(__ldg(tb + lane * 16 + kb * 4 + r), q2, u1, u2, u3);
+            const uint32_t s2 = e4m3x2_to_f16x2(__ldg(tb + tile_q_bytes_for(kNvfp4) + (rr & 7) * 8 + 2 * kb + (rr >> 3)));
+            const __half2 qh = *reinterpret_cast<const __half2*>(&q2), sh = *reinterpret_cast<const __half2*>(&s2);
+            const float q = (cc & 1) ? __high2float(qh) : __low2float(qh);
+            v = gscale * (__low2float(sh) * q);
         } else {
             const int rr = (int)(row % kRowsPerBlock);
             int w, sh;
@@ -318,10 +332,10 @@ cudaError_t launch_unpack_nvfp4(const uint8_t* packed, int64_t N, int64_t K, uin
     return cudaGetLastError();
 }
 
-cudaError_t launch_embed_rows(const uint8_t* packed, int64_t N, int64_t K, int bits, const int32_t* ids, int64_t M,
-                              uint16_t* x, int64_t ldx, int* status, cudaStream_t stream)
+cudaError_t launch_embed_rows(const uint8_t* packed, int64_t N, int64_t K, int bits, float gscale, const int32_t* ids,
+                              int64_t M, uint16_t* x, int64_t ldx, int* status, cudaStream_t stream)
 {
-    embed_rows_kernel<<<grid_for(M * K, 256), 256, 0, stream>>>(packed, N, K, bits, ids, M, x, ldx, status);
+    embed_rows_kernel<<<grid_for(M * K, 256), 256, 0, stream>>>(packed, N, K, bits, gscale, ids, M, x, ldx, status);
     return cudaGetLastError();
 }
 

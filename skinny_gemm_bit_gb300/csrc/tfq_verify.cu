@@ -107,7 +107,7 @@ int tf_argmax_rows(const uint16_t* v, int64_t ld, int64_t M, int64_t N, int32_t*
 int tf_embed_rows(const tf_qweight* w, const int32_t* ids, int64_t M, uint16_t* x, void* ws, size_t ws_bytes,
                   void* stream)
 {
-    int rc = validate_affine(w, "tf_embed_rows");
+    int rc = validate_desc(w, "tf_embed_rows");
     if (rc)
         return rc;
     if (ids == nullptr || x == nullptr || ws == nullptr)
@@ -116,8 +116,9 @@ int tf_embed_rows(const tf_qweight* w, const int32_t* ids, int64_t M, uint16_t* 
         return report_error(TF_E_UNSUPPORTED_SHAPE, "tf_embed_rows: batch must be 1 and 1 <= M");
     if (ws_bytes < 256 || reinterpret_cast<uintptr_t>(ws) % 256 != 0)
         return report_error(TF_E_WORKSPACE_TOO_SMALL, "tf_embed_rows: workspace of 256 aligned bytes needed");
-    const cudaError_t e = launch_embed_rows(static_cast<const uint8_t*>(w->data), w->N, w->K, w->bits, ids, M, x, w->K,
-                                            static_cast<int*>(ws), static_cast<cudaStream_t>(stream));
+    const cudaError_t e = launch_embed_rows(static_cast<const uint8_t*>(w->data), w->N, w->K, desc_kernel_bits(w),
+                                            w->global_scale, ids, M, x, w->K, static_cast<int*>(ws),
+                                            static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? TF_OK : report_error(TF_E_CUDA, "tf_embed_rows: %s", cudaGetErrorString(e));
 }
 
@@ -204,8 +205,8 @@ int tf_generate_greedy(const tf_decoder_desc* d, const int32_t* prompt, int64_t 
             block[i + 1] = draft[i];
         if ((e = cudaMemcpyAsync(ids, block, (size_t)M * sizeof(int32_t), cudaMemcpyHostToDevice, s)) != cudaSuccess)
             return cuda_err(e, "ids to device");
-        if ((e = launch_embed_rows(static_cast<const uint8_t*>(E.data), E.N, E.K, E.bits, ids, M, x, E.K, status, s)) !=
-            cudaSuccess)
+        if ((e = launch_embed_rows(static_cast<const uint8_t*>(E.data), E.N, E.K, desc_kernel_bits(&E), E.global_scale,
+                                   ids, M, x, E.K, status, s)) != cudaSuccess)
             return cuda_err(e, "embed");
         int rc = tf_decode_step_run(d, x, M, logits, wsb + L.step, L.step_bytes, nullptr, 0, stream);
         if (rc)

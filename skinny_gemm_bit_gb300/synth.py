@@ -157,25 +157,30 @@ def wide_verify(seed: int = 2, M: int = 8, K: int = 12800, N: int = 2560, bits: 
 
 def decoder(seed: int = 3, n_layers: int = 28, d_model: int = 1024, d_ff: int = 3072,
             n_q_heads: int = 16, n_kv_heads: int = 8, head_dim: int = 128,
-            vocab: int = 151936, M: int = 1, bits: int = 4) -> dict:
-    """Random weights of a dense decoder's projections plus a tied readout."""
+            vocab: int = 151936, M: int = 1, bits: int = 4, code: str = "mlx") -> dict:
+    """Random weights of a dense decoder's projections plus a tied readout (MLX affine
+    codes of `bits`, or NVFP4 with code="nvfp4")."""
     rng = np.random.default_rng(seed)
     q_dim = n_q_heads * head_dim
     kv_dim = n_kv_heads * head_dim
     x = activations(rng, M, d_model)
+
+    def weights(N, K):
+        return nvfp4_weights(rng, N, K) if code == "nvfp4" else quant_weights(rng, N, K, bits)
+
     layers = []
     for _ in range(n_layers):
         layers.append({
             "attn_norm": gamma(rng, d_model),
-            "qkv": quant_weights(rng, q_dim + 2 * kv_dim, d_model, bits),
-            "o": quant_weights(rng, d_model, q_dim, bits),
+            "qkv": weights(q_dim + 2 * kv_dim, d_model),
+            "o": weights(d_model, q_dim),
             "mlp_norm": gamma(rng, d_model),
-            "gate": quant_weights(rng, d_ff, d_model, bits),
-            "up": quant_weights(rng, d_ff, d_model, bits),
-            "down": quant_weights(rng, d_model, d_ff, bits),
+            "gate": weights(d_ff, d_model),
+            "up": weights(d_ff, d_model),
+            "down": weights(d_model, d_ff),
         })
     final_norm = gamma(rng, d_model)
-    readout = quant_weights(rng, vocab, d_model, bits)
+    readout = weights(vocab, d_model)
     return {"x": x, "layers": layers, "final_norm": final_norm, "readout": readout,
             "dims": {"n_layers": n_layers, "d_model": d_model, "d_ff": d_ff, "q_dim": q_dim,
                      "kv_dim": kv_dim, "vocab": vocab}, "eps": 1e-6}

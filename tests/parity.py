@@ -62,6 +62,8 @@ def assert_close(y, ref, tol, what=""):
 
 
 def pack(T, w: dict):
+    if w.get("code") == "nvfp4":
+        return T.tf_qlinear_pack_nvfp4(w["codes"], w["scales"], float(w["gscale"]))
     return T.tf_qlinear_pack(w["wq"], w["scales"], w["biases"], w["bits"])
 
 

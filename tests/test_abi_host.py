@@ -186,13 +186,36 @@ def test_nvfp4_pack_refuses_bad_arguments(T):
 def test_nvfp4_weights_are_refused_where_only_affine_codes_run(T):
     L = T.lib()
     d = _nvfp4_desc(T)
-    # MoE (three NVFP4 expert stacks) and the embedding lookup
+    # the MoE layer (three NVFP4 expert stacks)
     assert L.tf_qmoe_workspace_bytes(ctypes.byref(d), ctypes.byref(d), ctypes.byref(d), 1, 1) == 0
     assert "NVFP4" in T.last_error()
-    rc = L.tf_embed_rows(ctypes.byref(d), FAKE, 1, FAKE, FAKE, 256, None)
-    assert rc == T.TF_E_UNSUPPORTED_SHAPE
     # gate and up must carry the same code
     a = _desc(T)
     ws = L.tf_qmlp_gateup_run(ctypes.byref(a), ctypes.byref(d), FAKE, 128, 1, None, 1e-6, FAKE, FAKE, 1 << 20, 0,
                               None)
     assert ws == T.TF_E_UNSUPPORTED_SHAPE
+
+
+def test_decoder_step_takes_one_weight_code(T):
+    # a one-layer decoder (d_model 128, d_ff 128, q 64, kv 32, vocab 64): all NVFP4 is
+    # planned; one affine matrix among NVFP4 ones is refused
+    L = T.lib()
+
+    def m(N, K, nv):
+        return _nvfp4_desc(T, N, K) if nv else _desc(T, N, K)
+
+    def step(nv_o):
+        layer = T.tf_decoder_layer()
+        layer.qkv, layer.o = m(128, 128, True), m(128, 64, nv_o)
+        layer.gate, layer.up, layer.down = m(128, 128, True), m(128, 128, True), m(128, 128, True)
+        layer.attn_norm = layer.mlp_norm = 0x20000
+        layers = (T.tf_decoder_layer * 1)(layer)
+        d = T.tf_decoder_desc()
+        d.n_layers, d.d_model, d.d_ff, d.q_dim, d.kv_dim, d.vocab, d.eps = 1, 128, 128, 64, 32, 64, 1e-6
+        d.layers = layers
+        d.final_norm = 0x20000
+        d.readout = m(64, 128, True)
+        return L.tf_decode_step_workspace_bytes(ctypes.byref(d), 8)
+
+    assert step(True) > 0
+    assert step(False) == 0 and "mixes weight codes" in T.last_error()

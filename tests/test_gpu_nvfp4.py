@@ -227,3 +227,76 @@ def test_every_schedule_matches(T, mode, M, K, N, dual):
     else:
         y_ref, ad = oracle.qlinear(oracle.bf16_to_f64(x), w)
         assert_close(host_f64(y), y_ref, tol_linear(ad), f"mode {mode}")
+
+
+# ------------------------------------------------------------------ decoder step and verify block
+
+def test_embed_rows_nvfp4_bit_exact(T):
+    # the token embedding from an NVFP4 tied readout: bf16 of the exact dequantised value
+    rng = np.random.default_rng(380)
+    N, K = 1000, 512
+    w = synth.nvfp4_weights(rng, N, K)
+    ids = np.array([0, 999, 17, 500, 999, 3], dtype=np.int32)
+    ws = T.workspace(256)
+    x = T.tf_embed_rows(pack4(T, w), torch.from_numpy(ids).cuda(), ws=ws)
+    expect = synth.f32_to_bf16_bits(oracle.dequant(w)[ids].astype(np.float32))
+    np.testing.assert_array_equal(x.cpu().view(torch.int16).numpy().view(np.uint16), expect)
+    assert T.tf_workspace_status(ws) == T.TF_OK
+
+
+@pytest.mark.parametrize("M", [1, 8])
+def test_decoder_step_nvfp4_matches_oracle_stage_by_stage(T, M):
+    # every stage of the step against the oracle applied to that stage's own inputs as
+    # the GPU produced them (NVFP4 weights reach 6 * 448 * scale at the edge blocks, so
+    # an earlier stage's rounding would otherwise dominate a later stage's bound)
+    from test_gpu_verify import _decoder
+    cfg = synth.decoder(seed=390 + M, n_layers=2, d_model=256, d_ff=384, n_q_heads=4, n_kv_heads=2, head_dim=64,
+                        vocab=1000, M=M, code="nvfp4")
+    dec = _decoder(T, cfg)
+    d = cfg["dims"]
+    QKV, D, F, q = d["q_dim"] + 2 * d["kv_dim"], d["d_model"], d["d_ff"], d["q_dim"]
+    dbg = torch.zeros(T.tf_decode_step_debug_elems(dec, M), dtype=torch.bfloat16, device="cuda")
+    logits = host_f64(T.tf_decode_step_run(dec, dev_bf16(cfg["x"]), debug=dbg))
+    dbg_h = host_f64(dbg)
+    per = M * (QKV + D + F + D)
+    h = oracle.bf16_to_f64(cfg["x"])
+    rel = 2.0 ** -8
+    for l, L in enumerate(cfg["layers"]):
+        blk = dbg_h[l * per:(l + 1) * per]
+        qkv = blk[:M * QKV].reshape(M, QKV)
+        h1 = blk[M * QKV:M * (QKV + D)].reshape(M, D)
+        a = blk[M * (QKV + D):M * (QKV + D + F)].reshape(M, F)
+        h2 = blk[M * (QKV + D + F):].reshape(M, D)
+        ref, ad = oracle.qlinear(oracle.rmsnorm(h, oracle.bf16_to_f64(L["attn_norm"]), cfg["eps"]), L["qkv"])
+        assert_close(qkv, ref, tol_linear(ad) + rel * np.abs(ref), f"layer {l} qkv")
+        o, ad = oracle.qlinear(qkv[:, :q], L["o"])
+        assert_close(h1, h + o, tol_linear(ad) + rel * np.abs(h + o), f"layer {l} h1")
+        gu = oracle.gateup(h1, L["gate"], L["up"], oracle.bf16_to_f64(L["mlp_norm"]), cfg["eps"])
+        assert_close(a, gu["h"], tol_swiglu(gu["g"], gu["u"], gu["g_abs"], gu["u_abs"]), f"layer {l} swiglu")
+        dn, ad = oracle.qlinear(a, L["down"])
+        assert_close(h2, h1 + dn, tol_linear(ad) + rel * np.abs(h1 + dn), f"layer {l} h2")
+        h = h2
+    ref, ad = oracle.qlinear(oracle.rmsnorm(h, oracle.bf16_to_f64(cfg["final_norm"]), cfg["eps"]), cfg["readout"])
+    assert_close(logits, ref, tol_linear(ad) + rel * np.abs(ref), "logits")
+
+
+def test_generation_with_drafts_nvfp4_equals_plain_decoding(T):
+    from test_gpu_verify import _check_generation, _decoder
+    cfg = synth.decoder(seed=395, n_layers=2, d_model=256, d_ff=384, n_q_heads=4, n_kv_heads=2, head_dim=64,
+                        vocab=1000, M=1, code="nvfp4")
+    _check_generation(T, _decoder(T, cfg), 48, seed=3)
+
+
+def test_chained_step_refuses_nvfp4(T):
+    # the single-kernel step reads affine codes only: asked for, it is refused by name
+    cfg = synth.decoder(seed=396, n_layers=1, d_model=256, d_ff=384, n_q_heads=4, n_kv_heads=2, head_dim=64,
+                        vocab=1000, M=1, code="nvfp4")
+    from test_gpu_verify import _decoder
+    dec = _decoder(T, cfg)
+    T.tune_set(T.TF_TUNE_CHAIN, 2)
+    try:
+        with pytest.raises(T.TfqError) as e:
+            T.tf_decode_step_run(dec, dev_bf16(cfg["x"]))
+        assert e.value.status == T.TF_E_UNSUPPORTED_SHAPE
+    finally:
+        T.tune_set(T.TF_TUNE_CHAIN, -1)

@@ -443,3 +443,16 @@ def test_nvfp4_global_scale_scales_the_projection():
     y1, _ = oracle.qlinear(x, w)
     y2, _ = oracle.qlinear(x, dict(w, gscale=np.float32(w["gscale"]) * np.float32(8.0)))
     np.testing.assert_array_equal(y2, 8.0 * y1)  # a power of two changes no rounding
+
+
+def test_decode_step_readout_row_subset_nvfp4():
+    # the readout restricted to a set of vocabulary rows equals those rows of the full one
+    cfg = synth.decoder(seed=79, n_layers=1, d_model=128, d_ff=192, n_q_heads=2, n_kv_heads=1, head_dim=64,
+                        vocab=300, M=2, code="nvfp4")
+    layers = [{k: (oracle.bf16_to_f64(v) if k.endswith("norm") else v) for k, v in L.items()} for L in cfg["layers"]]
+    x = oracle.bf16_to_f64(cfg["x"])
+    fn = oracle.bf16_to_f64(cfg["final_norm"])
+    full = oracle.decode_step(x, layers, fn, cfg["readout"], cfg["dims"]["q_dim"])
+    rows = np.array([299, 0, 17, 150])
+    sub = oracle.decode_step(x, layers, fn, cfg["readout"], cfg["dims"]["q_dim"], readout_rows=rows)
+    np.testing.assert_array_equal(sub["logits"], full["logits"][:, rows])
