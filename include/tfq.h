@@ -347,6 +347,8 @@ int tf_argmax_rows(const uint16_t* v, int64_t ld, int64_t M, int64_t N, int32_t*
 /*
  * x[m][k] = bf16(s q + b) of row ids[m] of a packed matrix (batch 1), k < K:
  * the dequantised row, rounded to nearest even (exact whenever |b| / |s| < 2^15).
+ * NVFP4: bf16(global_scale * (e4m3 scale * e2m1 code)), the fp32 product of the
+ * exact code-scale product and the matrix scale, rounded to nearest even.
  * ids device int32 [M], x device bf16 [M][K]. ws: 256 zeroed, 256-aligned bytes; an
  * id outside [0, N) records TF_E_INVALID_ARG there (tf_workspace_status) and gives
  * a zero row. Used as the token embedding of a tied readout.
