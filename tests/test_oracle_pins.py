@@ -309,6 +309,139 @@ def test_decode_step_ignores_k_and_v_rows():
     assert not np.array_equal(a["stages"][0]["qkv"][:, q_dim:], b["stages"][0]["qkv"][:, q_dim:])
 
 
+# ---------------------------------------------------------------- compositions: bias-only closed forms
+#
+# With every scale 0 a projection's output is bias * sum(input), the same in every
+# column, and with eps = 0 the RMSNorm of a constant row c is sign(c) * gamma exactly.
+# Constant rows therefore stay constant through a whole layer, and each composition
+# step has a closed form in which swapping two operands (gate and up, the two norms,
+# h and h1, a routing weight and its expert) changes the value.
+
+def _silu(v):
+    return v / (1.0 + math.exp(-v))
+
+
+def _bias_only(rng, N, K, beta, bits=4, batch=None):
+    """Weights with random codes, zero scales and the constant bias beta (exact in bf16)."""
+    w = synth.quant_weights(rng, N, K, bits, batch=batch)
+    w["scales"][:] = 0
+    w["biases"][:] = bf16(beta)
+    return w
+
+
+def test_gateup_order_and_norm_closed_form():
+    # x = 2 (constant), gamma = 0.5, eps = 0: xn = 0.5 everywhere, sum(xn) = K / 2.
+    # gate bias 1/32, up bias -1/16 (K = 128): g = 2, u = -4, h = silu(2) * -4.
+    rng = np.random.default_rng(41)
+    K, N = 128, 24
+    gate = _bias_only(rng, N, K, 1 / 32)
+    up = _bias_only(rng, N, K, -1 / 16)
+    x = np.full((2, K), 2.0)
+    out = oracle.gateup(x, gate, up, gamma=np.full(K, 0.5), eps=0.0)
+    assert np.array_equal(out["xn"], np.full((2, K), 0.5))
+    assert np.array_equal(out["g"], np.full((2, N), 2.0))
+    assert np.array_equal(out["u"], np.full((2, N), -4.0))
+    np.testing.assert_allclose(out["h"], np.full((2, N), -4.0 * _silu(2.0)), rtol=1e-15, atol=0)
+    # the swapped order, silu(u) * g, is a different number
+    assert abs(_silu(-4.0) * 2.0 - (-4.0 * _silu(2.0))) > 1.0
+
+
+def _bias_only_decoder(betas, gammas, n_layers=1, D=128, F=192, q_heads=2, kv_heads=1, hd=64, V=40):
+    rng = np.random.default_rng(43)
+    Q, KV = q_heads * hd, kv_heads * hd
+    layers = []
+    for _ in range(n_layers):
+        layers.append({"attn_norm": np.full(D, gammas["attn"]), "mlp_norm": np.full(D, gammas["mlp"]),
+                       "qkv": _bias_only(rng, Q + 2 * KV, D, betas["qkv"]),
+                       "o": _bias_only(rng, D, Q, betas["o"]),
+                       "gate": _bias_only(rng, F, D, betas["gate"]),
+                       "up": _bias_only(rng, F, D, betas["up"]),
+                       "down": _bias_only(rng, D, F, betas["down"])})
+    readout = _bias_only(rng, V, D, betas["readout"])
+    return layers, np.full(D, gammas["final"]), readout, Q
+
+
+def test_decode_step_mlp_branch_closed_form():
+    # D = 128, Q = 128, F = 192, input row h = 1, eps = 0.
+    #   attention norm (gamma 0.5): xn = 0.5, sum = 64; qkv = 64/64 = 1 (every column)
+    #   o = -1/16 * Q * 1 = -8;  h1 = 1 - 8 = -7
+    #   MLP norm (gamma 0.25) of the negative row -7: -0.25, sum S = -32
+    #   g = S/32 = -1, u = -S/16 = 2, a = silu(-1) * 2 (every column)
+    #   d = F/64 * a = 3 a;  h2 = h1 + d = -7 + 6 silu(-1)
+    #   readout (final gamma 2, bias 1/256): rmsnorm(h2) = -2, sum = -256 -> logits = -1
+    # Taking the attention norm for the MLP (S = -64), h instead of h1 as the MLP input
+    # (S = +32), h instead of h1 in the residual (h2 = 1 + d) or gate and up swapped
+    # each gives another h2.
+    betas = {"qkv": 1 / 64, "o": -1 / 16, "gate": 1 / 32, "up": -1 / 16, "down": 1 / 64, "readout": 1 / 256}
+    gammas = {"attn": 0.5, "mlp": 0.25, "final": 2.0}
+    layers, fn, readout, Q = _bias_only_decoder(betas, gammas)
+    x = np.ones((2, 128))
+    out = oracle.decode_step(x, layers, fn, readout, Q, eps=0.0)
+    st = out["stages"][0]
+    assert np.array_equal(st["qkv"], np.ones((2, Q + 128)))
+    assert np.array_equal(st["h1"], np.full((2, 128), -7.0))
+    a = 2.0 * _silu(-1.0)
+    np.testing.assert_allclose(st["gu"]["h"], np.full((2, 192), a), rtol=1e-15, atol=0)
+    h2 = -7.0 + 3.0 * a
+    np.testing.assert_allclose(st["h2"], np.full((2, 128), h2), rtol=1e-15, atol=0)
+    np.testing.assert_allclose(out["logits"], np.full((2, 40), -1.0), rtol=1e-14, atol=0)
+    wrong = {"attention norm in the MLP": -7.0 + 3.0 * 4.0 * _silu(-2.0),  # S = -64: g = -2, u = 4
+             "h as MLP input": -7.0 + 3.0 * (-2.0) * _silu(1.0),           # S = +32: g = 1, u = -2
+             "h in the residual": 1.0 + 3.0 * a,
+             "gate and up swapped": -7.0 + 3.0 * (-1.0) * _silu(2.0)}
+    for name, v in wrong.items():
+        assert abs(v - h2) > 0.1, name
+
+
+def test_decode_step_two_layers_chain_the_residual():
+    # Layer 1 starts from layer 0's h2 < 0: its attention norm gives -0.5, qkv = -1,
+    # o = +8, h1' = h2 + 8 > -7; the MLP norm of h1' is -0.25 only while h1' < 0,
+    # which holds (h2 + 8 = 1 + 6 silu(-1) < 0), so a is unchanged and h2' = h1' + 3 a.
+    betas = {"qkv": 1 / 64, "o": -1 / 16, "gate": 1 / 32, "up": -1 / 16, "down": 1 / 64, "readout": 1 / 256}
+    gammas = {"attn": 0.5, "mlp": 0.25, "final": 2.0}
+    layers, fn, readout, Q = _bias_only_decoder(betas, gammas, n_layers=2)
+    out = oracle.decode_step(np.ones((1, 128)), layers, fn, readout, Q, eps=0.0)
+    a = 2.0 * _silu(-1.0)
+    h2 = -7.0 + 3.0 * a
+    h1b = h2 + 8.0
+    assert h1b < 0
+    np.testing.assert_allclose(out["stages"][1]["h1"], np.full((1, 128), h1b), rtol=1e-13, atol=0)
+    np.testing.assert_allclose(out["h"], np.full((1, 128), h1b + 3.0 * a), rtol=1e-13, atol=0)
+
+
+def test_moe_pairs_each_weight_with_its_expert():
+    # H = 128, I = 64, x = 1. Bias-only experts: o(e) = b_d * I * silu(b_g H) * b_u H.
+    #   expert 0: b_g = 1/64, b_u = 1/128, b_d = 1/32  -> o = 2 silu(2)
+    #   expert 1: b_g = -1/128, b_u = 1/32, b_d = 1/64 -> o = 4 silu(-1)
+    #   experts 2, 3 (never chosen): o = 4 silu(1), 4 silu(3)
+    # Row 0 prefers expert 1 (logit 1 against 1 - ln 2), row 1 expert 0; weights 2/3, 1/3.
+    H, I, E = 128, 64, 4
+    rng = np.random.default_rng(47)
+    bg = [1 / 64, -1 / 128, 1 / 128, 3 / 128]
+    bu = [1 / 128, 1 / 32, 1 / 64, 1 / 64]
+    bd = [1 / 32, 1 / 64, 1 / 32, 1 / 32]
+    mats = {}
+    for name, (n, k, beta) in {"gate": (I, H, bg), "up": (I, H, bu), "down": (H, I, bd)}.items():
+        w = synth.quant_weights(rng, n, k, 4, batch=E)
+        w["scales"][:] = 0
+        for e in range(E):
+            w["biases"][e] = bf16(beta[e])
+        mats[name] = w
+    o = [bd[e] * I * _silu(bg[e] * H) * bu[e] * H for e in range(E)]
+    np.testing.assert_allclose(o, [2 * _silu(2.0), 4 * _silu(-1.0), 4 * _silu(1.0), 4 * _silu(3.0)],
+                               rtol=1e-15)
+    logits = np.full((2, E), -4.0, dtype=np.float32)
+    logits[0, 1], logits[0, 0] = 1.0, 1.0 - math.log(2.0)
+    logits[1, 0], logits[1, 1] = 1.0, 1.0 - math.log(2.0)
+    out = oracle.moe(np.ones((2, H)), logits, mats["gate"], mats["up"], mats["down"], 2)
+    assert out["idx"].tolist() == [[1, 0], [0, 1]]
+    np.testing.assert_allclose(out["w"], [[2 / 3, 1 / 3]] * 2, rtol=1e-7)
+    for m, (e0, e1) in enumerate([(1, 0), (0, 1)]):
+        w0, w1 = out["w"][m]
+        np.testing.assert_allclose(out["y"][m], np.full(H, w0 * o[e0] + w1 * o[e1]), rtol=1e-14, atol=0)
+        assert abs((w0 * o[e1] + w1 * o[e0]) - (w0 * o[e0] + w1 * o[e1])) > 0.1
+
+
 # ------------------------------------------------------------------ input Hadamard transform
 
 def _signs_to_pm1(signs, K):
