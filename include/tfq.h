@@ -65,6 +65,8 @@ extern "C" {
 #define TF_E_BAD_PACK 4           /* descriptor / packed header mismatch, stale pack */
 #define TF_E_CUDA 5               /* a CUDA runtime call failed; see tf_last_error */
 #define TF_E_TIMEOUT 6            /* a bounded device-side wait gave up */
+#define TF_E_INTERNAL 7           /* a launch-plan invariant failed on the device (a library bug;
+                                     recorded in the status word like TF_E_TIMEOUT) */
 
 #define TF_DTYPE_BF16 0
 #define TF_DTYPE_F32 1
@@ -232,13 +234,26 @@ int tf_qlinear_run_rht(const tf_qweight* w, const uint16_t* x, int64_t ldx, int6
  *          zero and each call leaves it at zero, so it needs no clearing; but two
  *          calls that may run at the same time on one device (different streams,
  *          or host threads) race on it and must not overlap. A device-side wait
- *          that gives up records TF_E_TIMEOUT in the array, where this call cannot
- *          report it, and may leave the split-K slots dirty; use tf_qlinear_run
- *          with a workspace where such failures must be observed.
+ *          that gives up records TF_E_TIMEOUT in the array and may leave its
+ *          split-K counters and slots dirty, so that later calls would be wrong:
+ *          tf_qlinear_noalloc_status reports such a failure and clears the array.
+ *   Device reset: the array's address is cached per device for the life of the
+ *          process; after cudaDeviceReset (or any teardown of the primary context)
+ *          the cached address is stale, so this call must not be used afterwards.
  */
 int tf_qlinear_run_noalloc(const tf_qweight* w, const uint16_t* x, int64_t ldx, int64_t M,
                            const uint16_t* rms_gamma, float rms_eps, const uint16_t* residual,
                            void* y, int y_dtype, unsigned flags, void* stream);
+
+/*
+ * The status word of tf_qlinear_run_noalloc's fixed array on the current device:
+ * TF_OK, or the status a device-side failure recorded there (TF_E_TIMEOUT,
+ * TF_E_INTERNAL). After a failure the whole array (status word, arrival counters,
+ * partial slots) is set back to zero, so the next call starts clean. Synchronises
+ * `stream` (the array lives on the current device); allocates nothing. Must not
+ * overlap a tf_qlinear_run_noalloc call on the same device.
+ */
+int tf_qlinear_noalloc_status(void* stream);
 
 /*
  * Gate and up together with a SwiGLU epilogue (Husky page, "Four
@@ -400,14 +415,19 @@ int tf_workspace_status(void* ws, void* stream);
  * Run one kernel whose bounded wait on a shared-memory barrier is never
  * satisfied, with a limit of `limit_ns` nanoseconds, so that the timeout path
  * can be exercised without hanging the GPU. Records TF_E_TIMEOUT in `ws` (read
- * it with tf_workspace_status). `ws` needs 256 bytes.
+ * it with tf_workspace_status). `ws` needs 256 bytes; ws = NULL targets the
+ * status word of tf_qlinear_run_noalloc's fixed array on the current device
+ * (read it with tf_qlinear_noalloc_status).
  */
 int tf_selftest_wait_timeout(void* ws, uint64_t limit_ns, void* stream);
 
 /*
  * Tuning override for the launch planner: key is one of TF_TUNE_*; value < 0
- * restores the planner's own choice. Process-wide; not thread-safe against
- * concurrent run calls.
+ * restores the planner's own choice. The setting belongs to the calling host
+ * thread: it changes the plans of that thread's later calls only, never another
+ * thread's. A workspace sized by a *_workspace_bytes query under one setting may
+ * be too small for a call made under another (the call then returns
+ * TF_E_WORKSPACE_TOO_SMALL): query and run under the same setting.
  */
 #define TF_TUNE_ROWBLOCKS 0   /* 16-row blocks processed side by side per round (1, 2, 4, 8, 16) */
 #define TF_TUNE_SPLITK 1      /* K splits (must divide K / 64) */

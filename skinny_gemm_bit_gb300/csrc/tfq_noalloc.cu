@@ -14,6 +14,9 @@
 // scratch as it found it (split-K counters and partial slots are re-zeroed by the
 // CTA that consumes them), so it needs no clearing between calls. Its address is
 // looked up once per device, with that device current, on the first call there.
+// A device-side failure (a bounded wait that ran out) leaves its status in the
+// array's first word and may leave counters or partial slots dirty:
+// tf_qlinear_noalloc_status reports it and puts the array back to zero.
 #include <atomic>
 #include <mutex>
 
@@ -63,6 +66,15 @@ int scratch_address(void** out)
 
 }  // namespace
 
+namespace tfq {
+// The current device's fixed array (for the diagnostics in tfq_api.cu).
+int noalloc_scratch(void** out, size_t* bytes)
+{
+    *bytes = kNoAllocScratchBytes;
+    return scratch_address(out);
+}
+}  // namespace tfq
+
 extern "C" int tf_qlinear_run_noalloc(const tf_qweight* w, const uint16_t* x, int64_t ldx, int64_t M,
                                       const uint16_t* rms_gamma, float rms_eps, const uint16_t* residual, void* y,
                                       int y_dtype, unsigned flags, void* stream)
@@ -86,6 +98,31 @@ extern "C" int tf_qlinear_run_noalloc(const tf_qweight* w, const uint16_t* x, in
     void* scratch = nullptr;
     if ((rc = scratch_address(&scratch)))
         return rc;
-    return tf_qlinear_run(w, x, ldx, M, rms_gamma, rms_eps, residual, y, y_dtype, scratch, kNoAllocScratchBytes,
-                          flags, stream);
+    return tfq::qlinear_run_named(w, x, ldx, M, rms_gamma, rms_eps, residual, y, y_dtype, scratch,
+                                  kNoAllocScratchBytes, flags, stream, "tf_qlinear_run_noalloc");
+}
+
+extern "C" int tf_qlinear_noalloc_status(void* stream)
+{
+    void* scratch = nullptr;
+    int rc = scratch_address(&scratch);
+    if (rc)
+        return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int st = 0;
+    cudaError_t e = cudaMemcpyAsync(&st, scratch, sizeof st, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess)
+        e = cudaStreamSynchronize(s);
+    if (e == cudaSuccess && st != 0) {
+        // the failed call may have left arrival counters and partial slots behind
+        e = cudaMemsetAsync(scratch, 0, kNoAllocScratchBytes, s);
+        if (e == cudaSuccess)
+            e = cudaStreamSynchronize(s);
+    }
+    if (e != cudaSuccess)
+        return tfq::report_error(TF_E_CUDA, "tf_qlinear_noalloc_status: %s", cudaGetErrorString(e));
+    if (st != 0)
+        tfq::report_error(st, "tf_qlinear_noalloc_status: a device-side failure was recorded in the fixed array "
+                              "(now cleared)");
+    return st;
 }

@@ -870,7 +870,7 @@ __global__ void __launch_bounds__((NWT + 1) * 32, NWT == 8 ? 2 : 1) qproj_kernel
                 nseg = 0;
                 if (lane == 0) {
                     flags[0] = 1;
-                    atomicCAS(p.status, 0, TF_E_TIMEOUT);
+                    atomicCAS(p.status, 0, TF_E_INTERNAL);
                 }
             }
             for (int i0 = 0; i0 < nseg; i0 += 32) {
@@ -1303,7 +1303,7 @@ __global__ void __launch_bounds__(kThreads, 1) qproj_warp_kernel(const __grid_co
     const bool two = !norm && run1 != run0;
     if (run1 > run0 + 1) {  // never expected: every thread sees it and the CTA leaves untouched
         if (threadIdx.x == 0)
-            atomicCAS(p.status, 0, TF_E_TIMEOUT);
+            atomicCAS(p.status, 0, TF_E_INTERNAL);
         return;
     }
 
@@ -1521,7 +1521,7 @@ __global__ void __launch_bounds__(kThreads, 1) qproj_warp_kernel(const __grid_co
                 } else {  // the host sizes the list; never expected
                     if (lane == 0) {
                         flags[0] = 1;
-                        atomicCAS(p.status, 0, TF_E_TIMEOUT);
+                        atomicCAS(p.status, 0, TF_E_INTERNAL);
                     }
                     alive = false;
                     break;

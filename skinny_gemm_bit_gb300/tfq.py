@@ -23,6 +23,7 @@ TF_E_WORKSPACE_TOO_SMALL = 3
 TF_E_BAD_PACK = 4
 TF_E_CUDA = 5
 TF_E_TIMEOUT = 6
+TF_E_INTERNAL = 7
 TF_DTYPE_BF16 = 0
 TF_DTYPE_F32 = 1
 TF_RUN_PDL = 1
@@ -87,6 +88,7 @@ _SIGS = {
                                           ctypes.c_int, P, ctypes.c_size_t, ctypes.c_uint, P]),
     "tf_qlinear_run_noalloc": (ctypes.c_int, [ctypes.POINTER(tf_qweight), P, I64, I64, P, ctypes.c_float, P, P,
                                               ctypes.c_int, ctypes.c_uint, P]),
+    "tf_qlinear_noalloc_status": (ctypes.c_int, [P]),
     "tf_qmlp_gateup_workspace_bytes": (SZ, [ctypes.POINTER(tf_qweight), ctypes.POINTER(tf_qweight), I64]),
     "tf_qmlp_gateup_run": (ctypes.c_int, [ctypes.POINTER(tf_qweight), ctypes.POINTER(tf_qweight), P, I64, I64,
                                           P, ctypes.c_float, P, P, SZ, ctypes.c_uint, P]),
@@ -290,8 +292,14 @@ def tf_workspace_status(ws: torch.Tensor, stream=None) -> int:
     return lib().tf_workspace_status(_ptr(ws), _stream(stream))
 
 
-def tf_selftest_wait_timeout(ws: torch.Tensor, limit_ns: int, stream=None):
+def tf_selftest_wait_timeout(ws, limit_ns: int, stream=None):
+    """ws=None targets the status word of tf_qlinear_run_noalloc's fixed array."""
     _check(lib().tf_selftest_wait_timeout(_ptr(ws), limit_ns, _stream(stream)))
+
+
+def tf_qlinear_noalloc_status(stream=None) -> int:
+    """Status recorded in tf_qlinear_run_noalloc's fixed array (cleared, with the array, after a failure)."""
+    return lib().tf_qlinear_noalloc_status(_stream(stream))
 
 
 # ---------------------------------------------------------------------------- projections

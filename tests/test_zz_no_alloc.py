@@ -66,6 +66,8 @@ def test_noalloc_matches_workspace_call_twice_in_a_row(T, M, K, N, bits, norm):
         # the projection tolerance (in practice byte for byte), and with the oracle
         assert_close(y, ref_ws, tol, f"noalloc call {i} vs tf_qlinear_run, M={M} K={K} N={N}")
         assert_close(y, y_ref, tol, f"noalloc call {i} vs oracle, M={M} K={K} N={N}")
+    # no device-side failure was recorded in the fixed array by these calls
+    assert T.tf_qlinear_noalloc_status() == T.TF_OK
 
 
 def test_noalloc_refuses_a_shape_beyond_the_fixed_scratch(T):
@@ -101,3 +103,34 @@ def test_noalloc_nvfp4_matches_workspace_call(T, M, K, N):
     y = T.tf_qlinear_run_noalloc(qw, x)
     torch.cuda.synchronize()
     assert torch.equal(y.view(torch.int16), y_ws.view(torch.int16))
+
+
+def test_noalloc_status_reports_a_timeout_and_clears_the_array(T):
+    # a bounded wait that nothing satisfies, aimed at the fixed array's status word (a
+    # 1 ms limit: the kernel gives up and returns, the GPU stays usable), then the
+    # status query reports it once, puts the array back to zero, and the next
+    # split-K projection through the array matches the oracle
+    T.tf_selftest_wait_timeout(None, 1_000_000)
+    assert T.tf_qlinear_noalloc_status() == T.TF_E_TIMEOUT
+    assert "cleared" in T.lib().tf_last_error().decode()
+    assert T.tf_qlinear_noalloc_status() == T.TF_OK
+    cfg = synth.single_projection(seed=7300, M=8, K=12800, N=2560, bits=4)
+    w = pack(T, cfg["w"])
+    y = T.tf_qlinear_run_noalloc(w, dev_bf16(cfg["x"]))
+    torch.cuda.synchronize()
+    y_ref, ad = oracle.qlinear(oracle.bf16_to_f64(cfg["x"]), cfg["w"])
+    assert_close(host_f64(y), y_ref, tol_linear(ad), "noalloc call after a cleared timeout")
+    assert T.tf_qlinear_noalloc_status() == T.TF_OK
+
+
+def test_noalloc_errors_name_the_noalloc_entry_point(T):
+    # an argument error found by the shared projection path is reported under this
+    # entry point's name, not tf_qlinear_run's
+    cfg = synth.single_projection(seed=7400, M=1, K=1024, N=64, bits=4)
+    w = pack(T, cfg["w"])
+    x = torch.zeros((1, 1024), dtype=torch.bfloat16, device="cuda")
+    y = torch.empty((1, 64), dtype=torch.bfloat16, device="cuda")
+    rc = T.lib().tf_qlinear_run_noalloc(ctypes.byref(w.desc), ctypes.c_void_p(x.data_ptr()), 1024, 1, None, 1e-6,
+                                        None, ctypes.c_void_p(y.data_ptr()), 7, 0, None)  # 7: no such y dtype
+    assert rc == T.TF_E_INVALID_ARG
+    assert T.lib().tf_last_error().decode().startswith("tf_qlinear_run_noalloc:")
