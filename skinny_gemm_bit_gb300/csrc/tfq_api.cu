@@ -13,7 +13,9 @@ namespace tfq {
 
 namespace {
 thread_local char g_last_error[512] = "";
-int g_tune[7] = {-1, -1, -1, -1, -1, -1, -1};
+// planner overrides of tf_tune_set: per host thread, so that one caller's tuning
+// never changes another caller's schedule or workspace needs
+thread_local int g_tune[7] = {-1, -1, -1, -1, -1, -1, -1};
 int g_sms_cache[64] = {0};
 
 constexpr size_t kStatusBytes = 256;
@@ -487,6 +489,7 @@ const char* tf_status_str(int status)
     case TF_E_BAD_PACK: return "TF_E_BAD_PACK";
     case TF_E_CUDA: return "TF_E_CUDA";
     case TF_E_TIMEOUT: return "TF_E_TIMEOUT";
+    case TF_E_INTERNAL: return "TF_E_INTERNAL";
     default: return "TF_E_UNKNOWN";
     }
 }
@@ -716,13 +719,14 @@ static int qlinear_impl(const tf_qweight* w, const tf_qweight* w_up, const uint1
 
 static int qlinear_entry(const tf_qweight* w, const uint16_t* x, int64_t ldx, int64_t M, const uint8_t* rht,
                          const uint16_t* rms_gamma, float rms_eps, const uint16_t* residual, void* y, int y_dtype,
-                         void* ws, size_t ws_bytes, unsigned flags, void* stream);
+                         void* ws, size_t ws_bytes, unsigned flags, void* stream, const char* name);
 
 int tf_qlinear_run(const tf_qweight* w, const uint16_t* x, int64_t ldx, int64_t M, const uint16_t* rms_gamma,
                    float rms_eps, const uint16_t* residual, void* y, int y_dtype, void* ws, size_t ws_bytes,
                    unsigned flags, void* stream)
 {
-    return qlinear_entry(w, x, ldx, M, nullptr, rms_gamma, rms_eps, residual, y, y_dtype, ws, ws_bytes, flags, stream);
+    return qlinear_entry(w, x, ldx, M, nullptr, rms_gamma, rms_eps, residual, y, y_dtype, ws, ws_bytes, flags, stream,
+                         "tf_qlinear_run");
 }
 
 int tf_qlinear_run_rht(const tf_qweight* w, const uint16_t* x, int64_t ldx, int64_t M, const uint8_t* rht_signs,
@@ -732,34 +736,48 @@ int tf_qlinear_run_rht(const tf_qweight* w, const uint16_t* x, int64_t ldx, int6
     if (rht_signs == nullptr)
         return fail(TF_E_INVALID_ARG, "tf_qlinear_run_rht: rht_signs is NULL");
     return qlinear_entry(w, x, ldx, M, rht_signs, rms_gamma, rms_eps, residual, y, y_dtype, ws, ws_bytes, flags,
-                         stream);
+                         stream, "tf_qlinear_run_rht");
 }
 
 static int qlinear_entry(const tf_qweight* w, const uint16_t* x, int64_t ldx, int64_t M, const uint8_t* rht,
                          const uint16_t* rms_gamma, float rms_eps, const uint16_t* residual, void* y, int y_dtype,
-                         void* ws, size_t ws_bytes, unsigned flags, void* stream)
+                         void* ws, size_t ws_bytes, unsigned flags, void* stream, const char* name)
 {
-    int rc = check_desc(w, "tf_qlinear_run");
+    int rc = check_desc(w, name);
     if (rc)
         return rc;
     if (w->batch != 1)
-        return fail(TF_E_UNSUPPORTED_SHAPE, "tf_qlinear_run: batch must be 1 (use tf_qmoe_run for experts)");
+        return fail(TF_E_UNSUPPORTED_SHAPE, "%s: batch must be 1 (use tf_qmoe_run for experts)", name);
     if (M < 1 || M > kMaxM)
-        return fail(TF_E_UNSUPPORTED_SHAPE, "tf_qlinear_run: M must be in [1, 8] (got %lld)", (long long)M);
-    if ((rc = check_act(x, ldx, w->K, "tf_qlinear_run: x")))
+        return fail(TF_E_UNSUPPORTED_SHAPE, "%s: M must be in [1, 8] (got %lld)", name, (long long)M);
+    char what[96];
+    snprintf(what, sizeof what, "%s: x", name);
+    if ((rc = check_act(x, ldx, w->K, what)))
         return rc;
     if (rms_gamma != nullptr && (!aligned(rms_gamma, 16) || !(rms_eps >= 0.f)))
-        return fail(TF_E_INVALID_ARG, "tf_qlinear_run: rms_gamma must be 16-byte aligned and rms_eps >= 0");
+        return fail(TF_E_INVALID_ARG, "%s: rms_gamma must be 16-byte aligned and rms_eps >= 0", name);
     if (y == nullptr || (y_dtype != TF_DTYPE_BF16 && y_dtype != TF_DTYPE_F32))
-        return fail(TF_E_INVALID_ARG, "tf_qlinear_run: y NULL or bad y_dtype");
+        return fail(TF_E_INVALID_ARG, "%s: y NULL or bad y_dtype", name);
     if (ws == nullptr || !aligned(ws, 256))
-        return fail(TF_E_INVALID_ARG, "%s: workspace NULL or not 256-byte aligned", "tf_qlinear_run");
+        return fail(TF_E_INVALID_ARG, "%s: workspace NULL or not 256-byte aligned", name);
     if (ws_bytes < kStatusBytes)
-        return fail(TF_E_WORKSPACE_TOO_SMALL, "%s: workspace too small", "tf_qlinear_run");
+        return fail(TF_E_WORKSPACE_TOO_SMALL, "%s: workspace too small", name);
     return qlinear_impl(w, nullptr, x, ldx, M, rms_gamma, rms_eps, residual, y, w->N, y_dtype, ws,
                         static_cast<uint8_t*>(ws) + kStatusBytes, ws_bytes - kStatusBytes, (flags & TF_RUN_PDL) != 0,
-                        static_cast<cudaStream_t>(stream), rht ? "tf_qlinear_run_rht" : "tf_qlinear_run", rht);
+                        static_cast<cudaStream_t>(stream), name, rht);
 }
+
+extern "C++" {
+namespace tfq {
+int qlinear_run_named(const tf_qweight* w, const uint16_t* x, int64_t ldx, int64_t M, const uint16_t* rms_gamma,
+                      float rms_eps, const uint16_t* residual, void* y, int y_dtype, void* ws, size_t ws_bytes,
+                      unsigned flags, void* stream, const char* name)
+{
+    return qlinear_entry(w, x, ldx, M, nullptr, rms_gamma, rms_eps, residual, y, y_dtype, ws, ws_bytes, flags, stream,
+                         name);
+}
+}  // namespace tfq
+}  // extern "C++"
 
 size_t tf_qmlp_gateup_workspace_bytes(const tf_qweight* gate, const tf_qweight* up, int64_t M)
 {
@@ -932,7 +950,7 @@ int tf_qmoe_run(const tf_qweight* gate, const tf_qweight* up, const tf_qweight* 
 namespace {
 struct StepLayout {
     Plan p_qkv, p_o, p_gu, p_dn, p_ro;
-    size_t bar, act, red, total;
+    size_t bar, ssq, act, red, total;
     size_t qkv_e, h_e, a_e;  // elements per activation buffer
 };
 
@@ -990,8 +1008,9 @@ StepLayout step_layout(const tf_decoder_desc* d, int64_t M)
     L.h_e = (size_t)kMaxM * D;
     L.a_e = (size_t)kMaxM * F;
     (void)M;
-    L.bar = kStatusBytes;  // stage arrival counters of the single-kernel step: 4 per layer + 2
-    L.act = align_up(L.bar + (size_t)(4 * d->n_layers + 2) * sizeof(unsigned), 256);
+    L.bar = kStatusBytes;  // stage arrival counters of the single-kernel step: 4 per layer + 1
+    L.ssq = align_up(L.bar + (size_t)(4 * d->n_layers + 1) * sizeof(unsigned), 256);  // [2 L][8] u64
+    L.act = align_up(L.ssq + (size_t)2 * d->n_layers * kMaxM * sizeof(unsigned long long), 256);
     // qkv | h1 | a | h ping | h pong
     const size_t act_bytes = (L.qkv_e + L.h_e + L.a_e + 2 * L.h_e) * sizeof(uint16_t) + 5 * 256;
     L.red = align_up(L.act + act_bytes, 256);
@@ -1063,7 +1082,7 @@ int tf_decode_step_run(const tf_decoder_desc* d, const uint16_t* x, int64_t M, u
     // projections with programmatic dependent launch, which is therefore the default
     int bits = d->readout.bits;
     bool chain = g_tune[TF_TUNE_CHAIN] == 2 && d->readout.code == TF_CODE_AFFINE && d->n_layers <= kChainMaxLayers &&
-                 D <= 1024 &&
+                 D >= kGroup &&
                  std::max<int64_t>(D, std::max<int64_t>(Q, F)) <= (int64_t)kChainMaxGroups * kGroup &&
                  d->vocab <= INT32_MAX;
     for (int l = 0; chain && l < d->n_layers; ++l) {
@@ -1074,28 +1093,24 @@ int tf_decode_step_run(const tf_decoder_desc* d, const uint16_t* x, int64_t M, u
     ChainParams cp{};
     size_t chain_smem_bytes = 0;
     if (chain) {
-        chain_smem_bytes = chain_smem(bits, (int)std::max<int64_t>(D, std::max<int64_t>(Q, F)), &cp.nst, &cp.x_rs,
-                                      &cp.xsum_off, &cp.red_off, &cp.xraw_off, &cp.ring_off);
+        chain_smem_bytes = chain_smem(bits, (int)std::max<int64_t>(D, std::max<int64_t>(Q, F)), (int)D, &cp.nst,
+                                      &cp.x_rs, &cp.xsum_off, &cp.red_off, &cp.gamma_off, &cp.xraw_off, &cp.ring_off);
         chain = cp.nst >= 2 && chain_fits(bits, chain_smem_bytes);
     }
     if (!chain && g_tune[TF_TUNE_CHAIN] == 2)
         return fail(TF_E_UNSUPPORTED_SHAPE, "tf_decode_step_run: the single-kernel step cannot run for these shapes "
                                             "on this device (and it was required)");
-    if (chain) {
+    if (chain && d->n_layers > 0) {
         cp.L = d->n_layers;
         cp.M = (int)M;
         cp.D = (int)D;
         cp.F = (int)F;
         cp.Q = (int)Q;
         cp.KV = (int)KV;
-        cp.V = (int)d->vocab;
         cp.eps = d->eps;
         cp.C = device_sms();
         cp.limit_ns = kDefaultWaitLimitNs;
         cp.x = x;
-        cp.logits = logits;
-        cp.final_norm = d->final_norm;
-        cp.readout = tiles_of(&d->readout);
         if (debug != nullptr) {
             cp.buf[0] = debug;
             cp.buf[1] = debug + M * QKV;
@@ -1111,6 +1126,7 @@ int tf_decode_step_run(const tf_decoder_desc* d, const uint16_t* x, int64_t M, u
             cp.astride[3] = hp_ws[1] - hp_ws[0];
         }
         cp.bar = reinterpret_cast<unsigned*>(wsb + L.bar);
+        cp.ssq = reinterpret_cast<unsigned long long*>(wsb + L.ssq);
         cp.status = static_cast<int*>(ws);
         for (int l = 0; l < d->n_layers; ++l) {
             const tf_decoder_layer& Ly = d->layers[l];
@@ -1120,7 +1136,12 @@ int tf_decode_step_run(const tf_decoder_desc* d, const uint16_t* x, int64_t M, u
         const cudaError_t e = launch_chain(bits, cp, chain_smem_bytes, s);
         if (e != cudaSuccess)
             return cuda_fail(e, "tf_decode_step_run: single-kernel step");
-        return TF_OK;
+        // the final RMSNorm + readout: its own kernel, streaming its weights while the
+        // layers finish (programmatic dependent launch)
+        const int Ll = d->n_layers - 1;
+        const uint16_t* h_last = debug != nullptr ? debug + (size_t)Ll * per_layer + M * (QKV + D + F) : hp_ws[Ll & 1];
+        return qlinear_impl(&d->readout, nullptr, h_last, D, M, d->final_norm, d->eps, nullptr, logits, d->vocab,
+                            TF_DTYPE_BF16, ws, red, red_bytes, true, s, "tf_decode_step_run: readout");
     }
 
     // ---- one kernel per projection
@@ -1185,8 +1206,14 @@ int tf_workspace_status(void* ws, void* stream)
 
 int tf_selftest_wait_timeout(void* ws, uint64_t limit_ns, void* stream)
 {
-    if (ws == nullptr || !aligned(ws, 4))
-        return fail(TF_E_INVALID_ARG, "tf_selftest_wait_timeout: NULL or misaligned workspace");
+    if (ws == nullptr) {  // the status word of tf_qlinear_run_noalloc's fixed array
+        size_t bytes = 0;
+        const int rc = noalloc_scratch(&ws, &bytes);
+        if (rc)
+            return rc;
+    }
+    if (!aligned(ws, 4))
+        return fail(TF_E_INVALID_ARG, "tf_selftest_wait_timeout: misaligned workspace");
     if (limit_ns > 5000000000ull)
         return fail(TF_E_INVALID_ARG, "tf_selftest_wait_timeout: limit above 5 s");
     cudaError_t e = launch_timeout_probe(static_cast<int*>(ws), limit_ns, static_cast<cudaStream_t>(stream));

@@ -120,20 +120,17 @@ struct ChainLayerW {
 
 struct ChainParams {
     int L, M, D, F, Q, KV;
-    int V;
     float eps;
     int C;                                         // CTAs (all co-resident)
-    int nst, x_rs, xsum_off, red_off, xraw_off, ring_off;  // shared-memory layout
+    int nst, x_rs, xsum_off, red_off, gamma_off, xraw_off, ring_off;  // shared-memory layout
     uint64_t limit_ns;
     const uint16_t* x;                             // residual stream entering layer 0, [M][D]
-    uint16_t* logits;                              // [M][V]
-    const uint16_t* final_norm;
-    const uint8_t* readout;
     // activation buffers by role (0 qkv, 1 h1, 2 a, 3 h): layer l uses
     // buf[r] + l * lstride[r] + (l & 1) * astride[r] (elements)
     uint16_t* buf[4];
     int64_t lstride[4], astride[4];
-    unsigned* bar;                                 // [4 L + 2] stage arrival counters (zero, left zero)
+    unsigned* bar;                                 // [4 L + 1] stage arrival counters (zero, left zero)
+    unsigned long long* ssq;                       // [2 L][8] per-row sums of squares, fixed point (zero, left zero)
     int* status;
     ChainLayerW layer[kChainMaxLayers];
 };
@@ -141,7 +138,9 @@ struct ChainParams {
 // tfq_chain.cu
 cudaError_t launch_chain(int bits, const ChainParams& p, size_t smem, cudaStream_t stream);
 bool chain_fits(int bits, size_t smem);  // cooperative launch possible, one CTA per SM fits
-size_t chain_smem(int bits, int kmax, int* nst, int* x_rs, int* xsum_off, int* red_off, int* xraw_off, int* ring_off);
+// kmax: the largest K of a stage (staged rows); dmax: d_model (the staged RMSNorm weight)
+size_t chain_smem(int bits, int kmax, int dmax, int* nst, int* x_rs, int* xsum_off, int* red_off, int* gamma_off,
+                  int* xraw_off, int* ring_off);
 
 // host helpers (tfq_api.cu)
 void set_error(const char* fmt, ...);
@@ -153,6 +152,12 @@ Plan plan_qproj(int n_rb, int groups, int mats, int bits, int slots, int k_full,
 // Error reporting and descriptor validation shared by the entry points (tfq_api.cu).
 int report_error(int status, const char* fmt, ...);
 int validate_desc(const tf_qweight* w, const char* name);
+// The current device's fixed scratch array of tf_qlinear_run_noalloc (tfq_noalloc.cu).
+int noalloc_scratch(void** out, size_t* bytes);
+// tf_qlinear_run with the caller's entry-point name in its error messages
+int qlinear_run_named(const tf_qweight* w, const uint16_t* x, int64_t ldx, int64_t M, const uint16_t* rms_gamma,
+                      float rms_eps, const uint16_t* residual, void* y, int y_dtype, void* ws, size_t ws_bytes,
+                      unsigned flags, void* stream, const char* name);
 
 // launchers (tfq_qproj_b*_*.cu, one instantiation unit per bit width and matrix count)
 cudaError_t launch_qproj_b4_single(bool moe, const Plan& plan, const QProjParams& p, cudaStream_t stream, bool pdl);
