@@ -1,16 +1,20 @@
 """Benchmark of the quantised decode projection on GB300.
 
-Default workload (one JSON line): the fused RMSNorm + gate/up SwiGLU projection,
-4-bit group-64 weights, K=1024, N=2x3072; one step is one M=1 call followed by
-one M=8 call, each on its own copy of the weights from a rotation of copies
-whose total is more than four times the L2 cache, so every call streams its
-weights from HBM. Steps are captured once into a CUDA graph and replayed.
+Default workload (one JSON line): the per-token weight stream of a 28-layer dense
+decoder (d_model 1024, d_ff 3072, 16 q / 8 kv heads of 128, tied readout
+151,936 x 1024; 4-bit group-64 weights, 335 MB per step): one step is one M=1
+decoder step followed by one M=8 decoder step. Each step streams more than twice
+L2 from HBM, and L2 is flushed before every timed replay. Steps are captured
+once into a CUDA graph and replayed; the timed graph is replayed five times and
+the median is reported.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl tfq|reference]
-                  [--workload gateup|proj|wide|wide_rht|readout|step|moe4|moe8|verify|
+                  [--workload step|gateup|proj|wide|wide_rht|readout|moe4|moe8|verify|
                               wide_nvfp4|readout_nvfp4]
 
-The other workloads: proj (one K=1024, N=3072 projection, M=1), wide (K=12800,
+The other workloads: gateup (the fused RMSNorm + gate/up SwiGLU projection, K=1024,
+N=2x3072, one M=1 and one M=8 call; weights rotate over copies whose total is more
+than four times L2), proj (one K=1024, N=3072 projection, M=1), wide (K=12800,
 N=2560, one M=1 and one M=8 call), wide_rht (the same with the input Hadamard
 transform folded into the activation staging), readout (the decoder's RMSNorm + tied readout,
 K=1024, N=151936, one M=1 and one M=8 call), step (the whole per-token weight
@@ -21,13 +25,15 @@ end, against plain one-token decoding), wide_nvfp4 / readout_nvfp4 (the wide and
 readout shapes with NVFP4 weights: E2M1 codes, an E4M3 scale per 16 columns).
 
 value      effective weight GB/s: algorithmic weight bytes (codes + scales +
-           biases) of all calls / device time of the timed region.
+           biases) of all calls / device time of the timed region (median of five
+           timed replays, each after an L2 flush).
 e2e        the same metric with the per-step activations copied in from pinned
            host memory and the outputs copied back inside the timed region.
 roofline   bytes per call / mean call time of the timed region against the
            measured HBM copy bandwidth; a call is one launch of the named kernel
            (four launches for the MoE layer).
-cpu_baseline  the fp64 oracle on a bounded sample, on this host's cores.
+cpu_baseline  the fp64 oracle on a bounded sample, on all of this host's cores (threads
+           splitting the sample's rows), with the single-thread figure beside it.
 
 Under torchrun (N > 1) every rank runs an independent replica of the workload
 (replicas: the projection has no exchange step); the timed region is bracketed by
@@ -51,6 +57,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "effective weight GB/s & % of HBM peak per quantized projection at M=1 and M=8"
+REPLAYS = 5
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 
@@ -235,24 +242,28 @@ class Workload:
             out[M] = ms * 1e3 / reps
         return out
 
-    def oracle_sample(self, seconds: float):
+    def oracle_sample(self, seconds: float, part=(0, 1)):
         """The fp64 oracle on a row subset of one matrix of the workload, M as in a step,
-        for about `seconds`; returns (weight bytes covered, seconds, description)."""
+        for about `seconds`; returns (weight bytes covered, seconds, description).
+        part = (i, n): only the i-th of n equal slices of those rows (one host thread's share)."""
         import oracle
         w, rows, what = self.sample_matrix()
+        r0, r1 = part[0] * rows // part[1], (part[0] + 1) * rows // part[1]
+        n = r1 - r0
         if w.get("code") == "nvfp4":
-            sub = dict(w, codes=w["codes"][:rows], scales=w["scales"][:rows], N=rows)
-            per = rows * w["K"] * (4 / 8 + 1 / 16)
+            sub = dict(w, codes=w["codes"][r0:r1], scales=w["scales"][r0:r1], N=n)
+            per = n * w["K"] * (4 / 8 + 1 / 16)
         else:
-            sub = {"wq": w["wq"][:rows], "scales": w["scales"][:rows], "biases": w["biases"][:rows],
-                   "N": rows, "K": w["K"], "bits": w["bits"]}
-            per = rows * w["K"] * (w["bits"] / 8 + 4 / 64)
+            sub = {"wq": w["wq"][r0:r1], "scales": w["scales"][r0:r1], "biases": w["biases"][r0:r1],
+                   "N": n, "K": w["K"], "bits": w["bits"]}
+            per = n * w["K"] * (w["bits"] / 8 + 4 / 64)
         x = oracle.bf16_to_f64(self.sample_x)
         signs = getattr(self, "host_signs", None)  # input Hadamard transform, when the workload has one
         done, t0, reps = 0, time.perf_counter(), 0
         while True:
             for M in self.step_ms:
-                oracle.qlinear(x[:M] if signs is None else oracle.rht(x[:M], signs), sub)
+                if n > 0:
+                    oracle.qlinear(x[:M] if signs is None else oracle.rht(x[:M], signs), sub)
                 done += per
             reps += 1
             if time.perf_counter() - t0 >= seconds:
@@ -261,7 +272,7 @@ class Workload:
         ms = " and ".join(f"M={M}" for M in self.step_ms)
         what_oracle = "projection" if signs is None else "input Hadamard transform + projection"
         return done, el, (f"{reps} x ({ms} calls of the {what_oracle} oracle on the first {rows} rows of {what}, "
-                          f"K={w['K']}), single thread")
+                          f"K={w['K']})")
 
 
 def _dev_bf16(torch, u16):
@@ -330,12 +341,15 @@ class GateUp(Workload):
         g, u = self.copies[i]
         self.T.tf_qmlp_gateup_run(g, u, x, self.gamma, self.eps, out=out, ws=self.ws, flags=flags)
 
-    def oracle_sample(self, seconds: float):
-        """The fused RMSNorm + gate/up oracle on the first 256 rows of each matrix."""
+    def oracle_sample(self, seconds: float, part=(0, 1)):
+        """The fused RMSNorm + gate/up oracle on the first 256 rows of each matrix (the
+        i-th of n slices of them for part = (i, n))."""
         import oracle
         cfg = self.cfg
-        rows = 256
-        sub = lambda w: {"wq": w["wq"][:rows], "scales": w["scales"][:rows], "biases": w["biases"][:rows],  # noqa
+        total = 256
+        r0, r1 = part[0] * total // part[1], (part[0] + 1) * total // part[1]
+        rows = r1 - r0
+        sub = lambda w: {"wq": w["wq"][r0:r1], "scales": w["scales"][r0:r1], "biases": w["biases"][r0:r1],  # noqa
                          "N": rows, "K": w["K"], "bits": w["bits"]}
         g, u = sub(cfg["gate"]), sub(cfg["up"])
         x = oracle.bf16_to_f64(cfg["x"])
@@ -343,14 +357,15 @@ class GateUp(Workload):
         done, t0, reps = 0, time.perf_counter(), 0
         while True:
             for M in (1, 8):
-                oracle.gateup(x[:M], g, u, gam, cfg["eps"])
+                if rows > 0:
+                    oracle.gateup(x[:M], g, u, gam, cfg["eps"])
                 done += 2 * rows * self.K * (4 / 8 + 4 / 64)
             reps += 1
             if time.perf_counter() - t0 >= seconds:
                 break
         el = time.perf_counter() - t0
         return done, el, (f"{reps} x (M=1 and M=8 calls of the fused RMSNorm + gate/up oracle on the first "
-                          f"{rows} of {self.N} rows of each matrix, K={self.K}), single thread")
+                          f"{total} of {self.N} rows of each matrix, K={self.K})")
 
 
 class Proj(Workload):
@@ -585,29 +600,41 @@ def run_tfq(args):
         g_timed.replay()
         torch.cuda.synchronize()
     torch.cuda.synchronize()
-    barrier(pg)
-    torch.cuda.synchronize()
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    ev0.record()
-    g_timed.replay()
-    ev1.record()
-    torch.cuda.synchronize()
-    barrier(pg)
-    ms = ev0.elapsed_time(ev1)
+    # five timed replays, each after an L2 flush (a buffer of twice L2 written, outside
+    # the timed region): no call of a replay finds its weights in L2
+    flush = torch.empty(2 * l2, dtype=torch.uint8, device="cuda")
+    replay_ms = []
+    for _ in range(REPLAYS):
+        flush.fill_(1)
+        torch.cuda.synchronize()
+        barrier(pg)
+        torch.cuda.synchronize()
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev0.record()
+        g_timed.replay()
+        ev1.record()
+        torch.cuda.synchronize()
+        barrier(pg)
+        replay_ms.append(max_over_ranks(ev0.elapsed_time(ev1), pg, f"cuda:{local}"))
     clocks = sampler.stop()
-    ms_max = max_over_ranks(ms, pg, f"cuda:{local}")
+    ms_max = statistics.median(replay_ms)
 
     # end to end: host buffers in, host buffers out, inside the timed region
     g_e2e.replay()
     torch.cuda.synchronize()
-    barrier(pg)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    g_e2e.replay()
-    e1.record()
-    torch.cuda.synchronize()
-    barrier(pg)
-    ms_e2e = max_over_ranks(e0.elapsed_time(e1), pg, f"cuda:{local}")
+    e2e_ms = []
+    for _ in range(REPLAYS):
+        flush.fill_(1)
+        torch.cuda.synchronize()
+        barrier(pg)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        g_e2e.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        barrier(pg)
+        e2e_ms.append(max_over_ranks(e0.elapsed_time(e1), pg, f"cuda:{local}"))
+    ms_e2e = statistics.median(e2e_ms)
 
     per_m = wl.per_m(flags)
     per_m_nopdl = wl.per_m(0)
@@ -631,8 +658,15 @@ def run_tfq(args):
         "dtype": "bf16", "data": f"synthetic (seeded random {_weights_word(wl)} weights and N(0,1) activations)",
         "config": {"workload": wl.desc, "name": wl.name, "K": wl.K, "N": wl.N, "M": ms_list, "bits": wl.bits,
                    "group": 64,
-                   "l2": (f"weights rotate over {wl.n_copies} copies, more than four times L2, every call reads HBM"
-                          if wl.n_copies > 1 else "every call streams more than twice L2 from HBM"),
+                   "l2": (f"L2 flushed (a buffer of twice L2 written) before each timed replay; the calls of a "
+                          f"replay rotate over {wl.n_copies} weight copies ({wl.n_copies * wl.per_call / l2:.1f}x L2), "
+                          f"so every call streams its weights from HBM"
+                          if wl.n_copies > 1 else
+                          f"L2 flushed before each timed replay; one copy of the weights, "
+                          f"{wl.per_call / 1e6:.1f} MB per call ({wl.per_call / l2:.1f}x L2), streamed from HBM by "
+                          f"every call"),
+                   "timing": f"median of {REPLAYS} timed replays of the {K}-step graph: "
+                             + ", ".join(f"{v:.4f}" for v in replay_ms) + " ms",
                    "graph": "CUDA graph" + (", programmatic dependent launch" if flags else ""),
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "pct_of_hbm_measured": round(100 * value / world / peak, 2),
@@ -740,9 +774,46 @@ def run_verify(args):
         pg.destroy_process_group()
 
 
+def cpu_model() -> str:
+    """The host CPU's model name (from /proc/cpuinfo; lscpu's when that has none)."""
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu model")):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return "unknown"
+
+
 def cpu_baseline(wl, seconds):
-    done, el, desc = wl.oracle_sample(seconds)
-    return {"value": round(done / el / 1e9, 6), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": desc}
+    """The fp64 oracle on a bounded sample of the workload: on every host core at once
+    (threads, each on its own slice of the sample's rows; the oracle's C loops release
+    the interpreter lock) and on one thread."""
+    cores = os.cpu_count() or 1
+    done1, el1, desc1 = wl.oracle_sample(seconds / 2)
+    results = [None] * cores
+    def work(i):
+        results[i] = wl.oracle_sample(seconds / 2, part=(i, cores))
+    threads = [threading.Thread(target=work, args=(i,)) for i in range(cores)]
+    t0 = time.perf_counter()
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    el = time.perf_counter() - t0
+    done = sum(r[0] for r in results)
+    return {"value": round(done / el / 1e9, 6), "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "cpu": cpu_model(),
+            "sample": f"{cores} threads, each on 1/{cores} of the rows of: {results[0][2]}",
+            "single_thread": {"value": round(done1 / el1 / 1e9, 6), "unit": "GB/s", "sample": desc1}}
 
 
 class _HostOnly:
@@ -791,10 +862,10 @@ class _HostOnly:
             self.impl.sample_matrix = lambda w=w, rows=rows, what=what: (w, rows, what)
             self.ms = sorted(set(self.impl.step_ms))
 
-    def oracle_sample(self, seconds):
+    def oracle_sample(self, seconds, part=(0, 1)):
         if self.name == "gateup":
-            return GateUp.oracle_sample(self.impl, seconds)
-        return Workload.oracle_sample(self.impl, seconds)
+            return GateUp.oracle_sample(self.impl, seconds, part)
+        return Workload.oracle_sample(self.impl, seconds, part)
 
 
 def run_reference(args):
@@ -806,12 +877,24 @@ def run_reference(args):
     import oracle
     oracle.build()
     host = _HostOnly(args.workload)
+    cores = os.cpu_count() or 1
     desc = None
     steps_s = []
     for i in range(args.warmup + args.steps):
-        done, el, desc = host.oracle_sample(args.ref_step_seconds)
+        results = [None] * cores
+
+        def work(j):
+            results[j] = host.oracle_sample(args.ref_step_seconds, part=(j, cores))
+        threads = [threading.Thread(target=work, args=(j,)) for j in range(cores)]
+        t0 = time.perf_counter()
+        for t in threads:
+            t.start()
+        for t in threads:
+            t.join()
+        el = time.perf_counter() - t0
+        desc = f"{cores} threads, each on 1/{cores} of the rows of: {results[0][2]}"
         if i >= args.warmup:
-            steps_s.append((done, el))
+            steps_s.append((sum(r[0] for r in results), el))
     total_b = sum(d for d, _ in steps_s)
     total_s = sum(e for _, e in steps_s)
     value = total_b / total_s / 1e9
@@ -822,8 +905,8 @@ def run_reference(args):
         "data": f"synthetic (seeded random {_weights_word(host)} weights and N(0,1) activations)",
         "config": {"workload": host.desc, "name": host.name, "K": host.K, "N": host.N, "M": host.ms,
                    "bits": host.bits, "group": 64},
-        "cpu_baseline": {"value": round(value, 6), "unit": "GB/s", "kind": "oracle", "cores": 1,
-                         "sample": f"each step: {desc}"},
+        "cpu_baseline": {"value": round(value, 6), "unit": "GB/s", "kind": "oracle", "cores": cores,
+                         "cpu": cpu_model(), "sample": f"each step: {desc}"},
         "e2e": {"value": round(value, 6), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -837,11 +920,12 @@ def main():
     ap.add_argument("--impl", default="tfq", choices=["tfq", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--ref-step-seconds", type=float, default=0.2)
-    ap.add_argument("--workload", default="gateup", choices=WORKLOADS,
-                    help="gateup (default): fused RMSNorm + gate/up, K=1024, N=2x3072, M=1 and 8; proj: "
+    ap.add_argument("--workload", default="step", choices=WORKLOADS,
+                    help="step (default): 28-layer decoder weight stream, M=1 and 8; gateup: fused RMSNorm + "
+                         "gate/up, K=1024, N=2x3072, M=1 and 8; proj: "
                          "K=1024, N=3072, M=1; wide: K=12800, N=2560, M=1 and 8; wide_rht: the same with the "
                          "input Hadamard transform; readout: RMSNorm + tied "
-                         "readout, K=1024, N=151936, M=1 and 8; step: 28-layer decoder weight stream, M=1 and 8; "
+                         "readout, K=1024, N=151936, M=1 and 8; "
                          "moe4 / moe8: MoE layer, M=8; verify: greedy generation with prompt-lookup drafts and "
                          "an up-to-8-row verify block on the 28-layer decoder; wide_nvfp4 / readout_nvfp4: the "
                          "wide and readout shapes with NVFP4 weights")
