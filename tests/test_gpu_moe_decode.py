@@ -66,6 +66,35 @@ def test_moe_repeat_is_byte_identical(T):
     assert T.tf_workspace_status(ws) == T.TF_OK
 
 
+def test_moe_expert_down_projection_exact(T):
+    # The expert projections of the MoE layer (gathered rows, per-slot problems) with
+    # every product and sum exact: x = 1, bias-only gate and up (scale 0) with
+    # g = 2048 / 16 = 128 and u = 2048 / 1024 = 2, so h = silu(128) * 2 = 256 exactly (the
+    # exponential underflows in fp32 and fp64 alike) and the bf16 h is exact; random 4-bit
+    # down codes with scale 1 and integer biases give integer sums far below 2^24; top-1
+    # routing weighs each row's expert by exactly 1. The output is then the oracle's
+    # integer rounded once to bf16, bit for bit.
+    rng = np.random.default_rng(47)
+    M, E, H, I = 8, 16, 2048, 768
+    cfg = synth.moe_layer(seed=46, M=M, E=E, top_k=1, hidden=H, inter=I)
+    cfg["x"] = synth.f32_to_bf16_bits(np.ones((M, H), np.float32))
+    for name, beta in (("gate", 1 / 16), ("up", 1 / 1024)):
+        cfg[name]["scales"][:] = 0
+        cfg[name]["biases"][:] = synth.f32_to_bf16_bits(np.float32(beta))
+    dn = cfg["down"]
+    dn["scales"][:] = 0x3F80
+    dn["biases"] = synth.f32_to_bf16_bits(rng.integers(-12, -3, size=dn["scales"].shape).astype(np.float32))
+    y, idx, w = _run_moe(T, cfg)
+    ref = oracle.moe(oracle.bf16_to_f64(cfg["x"]), cfg["logits"], cfg["gate"], cfg["up"], cfg["down"], 1)
+    assert np.array_equal(idx.cpu().numpy(), ref["idx"])
+    assert np.all(w.cpu().numpy() == 1.0)
+    assert all(s["h"].min() == 256.0 and s["h"].max() == 256.0 for row in ref["slots"] for s in row)
+    assert np.abs(ref["y"]).max() < 2 ** 24 and np.all(ref["y"] == np.round(ref["y"]))
+    expect = synth.f32_to_bf16_bits(ref["y"].astype(np.float32))
+    got = y.cpu().view(torch.int16).numpy().view(np.uint16)
+    np.testing.assert_array_equal(got, expect)
+
+
 # ------------------------------------------------------------------ decoder step
 
 def _pack_decoder(T, cfg):
@@ -162,14 +191,16 @@ def test_decoder_step_leaves_workspace_clean_and_repeats_exactly(T):
     assert T.tf_workspace_status(ws) == T.TF_OK
 
 
+@pytest.mark.parametrize("chain", [-1, 2])
 @pytest.mark.parametrize("M", [1, 8])
-def test_decoder_full_size(T, M):
+def test_decoder_full_size(T, M, chain):
     # 28 layers, model_dim 1024, hidden 3072, 16 q / 8 kv heads of 128, tied readout 151,936 x 1024,
-    # through the single-kernel step (required)
+    # through the default chain of per-projection kernels (chain -1: what the benchmark times)
+    # and through the single-kernel step (chain 2, required)
     cfg = synth.decoder(M=M)
     rows = np.sort(np.random.default_rng(9).choice(151936, size=512, replace=False))
     rows = np.concatenate([rows, [0, 151935]])
-    T.tune_set(T.TF_TUNE_CHAIN, 2)
+    T.tune_set(T.TF_TUNE_CHAIN, chain)
     try:
         _check_decoder(T, cfg, M, readout_rows=np.unique(rows))
     finally:

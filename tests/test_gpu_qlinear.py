@@ -108,6 +108,58 @@ def test_fp32_exact_sum_gate(T, bits):
     assert any(_bf16_accumulating_dot(xi[0], wd[n]) != y_ref[0, n] for n in range(8))
 
 
+def _exact_case(rng, M, K, N, bits, xmax):
+    xi = rng.integers(-xmax, xmax + 1, size=(M, K)).astype(np.float32)
+    w = synth.quant_weights(rng, N, K, bits)
+    w["scales"][:] = 0x3F80
+    off = -8 if bits == 4 else -128
+    w["biases"] = synth.f32_to_bf16_bits(rng.integers(off - 4, off + 5, size=w["scales"].shape).astype(np.float32))
+    return xi, w
+
+
+# Every schedule the planner has (1: lock-step teams, 2: warp workers, 3: light teams,
+# 4: light teams with bulk-copied rows, 5: streaming CTAs) on one unsplit and one
+# split-K shape. |x| <= 128 (4-bit) / 64 (8-bit) keeps every partial sum of the warp
+# workers' fp16 form (1024 + q and 1024 + 16 q code units) below 2^24, so the fp32
+# sums are exact in every schedule and must equal the oracle.
+@pytest.mark.parametrize("mode", [1, 2, 3, 4, 5])
+@pytest.mark.parametrize("bits", [4, 8])
+@pytest.mark.parametrize("M,K,N", [(8, 1024, 96), (8, 12800, 256), (3, 4096, 1000)])
+def test_fp32_exact_sum_gate_every_schedule(T, mode, bits, M, K, N):
+    rng = np.random.default_rng(mode * 100 + bits * 10 + M + K)
+    xi, w = _exact_case(rng, M, K, N, bits, 128 if bits == 4 else 64)
+    y_ref, _ = oracle.qlinear(xi.astype(np.float64), w)
+    assert np.abs(y_ref).max() < 2 ** 24
+    T.tune_set(T.TF_TUNE_MODE, mode)
+    try:
+        y = T.tf_qlinear_run(pack(T, w), dev_bf16(synth.f32_to_bf16_bits(xi)), out_dtype=torch.float32)
+    finally:
+        T.tune_set(T.TF_TUNE_MODE, -1)
+    assert np.array_equal(host_f64(y), y_ref), f"mode {mode}"
+
+
+# NVFP4: integer x, every block scale byte 0x38 (E4M3 1.0) and a global scale of 1, so
+# every weight is an E2M1 value (a multiple of 0.5 up to 6) and every partial sum a
+# multiple of 0.5 far below 2^23: exact in fp32 on every schedule the code runs on.
+@pytest.mark.parametrize("mode", [1, 2, 3, 4])
+@pytest.mark.parametrize("M,K,N", [(8, 1024, 96), (8, 12800, 256)])
+def test_nvfp4_exact_sum_gate(T, mode, M, K, N):
+    rng = np.random.default_rng(900 + mode + K)
+    xi = rng.integers(-256, 257, size=(M, K)).astype(np.float32)
+    w = synth.nvfp4_weights(rng, N, K)
+    w["scales"][:] = 0x38
+    w["gscale"] = np.float32(1.0)
+    y_ref, _ = oracle.qlinear(xi.astype(np.float64), w)
+    assert np.all(y_ref * 2 == np.round(y_ref * 2)) and np.abs(y_ref).max() < 2 ** 22
+    T.tune_set(T.TF_TUNE_MODE, mode)
+    try:
+        qw = T.tf_qlinear_pack_nvfp4(w["codes"], w["scales"], float(w["gscale"]))
+        y = T.tf_qlinear_run(qw, dev_bf16(synth.f32_to_bf16_bits(xi)), out_dtype=torch.float32)
+    finally:
+        T.tune_set(T.TF_TUNE_MODE, -1)
+    assert np.array_equal(host_f64(y), y_ref), f"mode {mode}"
+
+
 # ------------------------------------------------------------------ random parity
 
 SHAPES = [  # (M, K, N, bits)
