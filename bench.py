@@ -9,8 +9,8 @@ once into a CUDA graph and replayed; the timed graph is replayed five times and
 the median is reported.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl tfq|reference]
-                  [--workload step|gateup|proj|wide|wide_rht|readout|moe4|moe8|verify|
-                              wide_nvfp4|readout_nvfp4]
+                  [--workload step|gateup|proj|wide|wide_rht|readout|moe4|moe8|moe_nvfp4|
+                              verify|wide_nvfp4|readout_nvfp4]
 
 The other workloads: gateup (the fused RMSNorm + gate/up SwiGLU projection, K=1024,
 N=2x3072, one M=1 and one M=8 call; weights rotate over copies whose total is more
@@ -18,8 +18,8 @@ than four times L2), proj (one K=1024, N=3072 projection, M=1), wide (K=12800,
 N=2560, one M=1 and one M=8 call), wide_rht (the same with the input Hadamard
 transform folded into the activation staging), readout (the decoder's RMSNorm + tied readout,
 K=1024, N=151936, one M=1 and one M=8 call), step (the whole per-token weight
-stream of a 28-layer dense decoder, one M=1 and one M=8 step), moe4 / moe8 (the
-MoE layer, M=8, one call), verify (greedy generation of 64 tokens on that decoder
+stream of a 28-layer dense decoder, one M=1 and one M=8 step), moe4 / moe8 / moe_nvfp4
+(the MoE layer, M=8, one call; 4-bit, 8-bit or NVFP4 experts), verify (greedy generation of 64 tokens on that decoder
 with prompt-lookup drafts verified up to 8 rows a step; host-driven, timed end to
 end, against plain one-token decoding), wide_nvfp4 / readout_nvfp4 (the wide and
 readout shapes with NVFP4 weights: E2M1 codes, an E4M3 scale per 16 columns).
@@ -292,7 +292,7 @@ def _clone_qweight(T, qw):
 
 def _pack(T, w):
     if w.get("code") == "nvfp4":
-        return T.tf_qlinear_pack_nvfp4(w["codes"], w["scales"], float(w["gscale"]))
+        return T.tf_qlinear_pack_nvfp4(w["codes"], w["scales"], w["gscale"])
     return T.tf_qlinear_pack(w["wq"], w["scales"], w["biases"], w["bits"])
 
 
@@ -476,14 +476,16 @@ class MoE(Workload):
     step_ms = (8,)
     launches_per_call = 4
 
-    def __init__(self, T, torch, l2_bytes, bits: int):
+    def __init__(self, T, torch, l2_bytes, bits: int, code: str = "mlx"):
         super().__init__(T, torch)
         from skinny_gemm_bit_gb300 import synth
-        cfg = synth.moe_layer(bits=bits)
+        nvfp4 = code == "nvfp4"
+        cfg = synth.moe_layer(bits=bits, code=code)
         self.cfg = cfg
-        self.name = f"moe{bits}"
-        self.kernel_key = f"moe_b{bits}"
-        self.kernel = f"MoE layer ({bits}-bit): route, gate/up, down, combine"
+        self.name = "moe_nvfp4" if nvfp4 else f"moe{bits}"
+        self.kernel_key = "moe_nvfp4" if nvfp4 else f"moe_b{bits}"
+        what = "NVFP4" if nvfp4 else f"{bits}-bit"
+        self.kernel = f"MoE layer ({what}): route, gate/up, down, combine"
         g, u, dn = _pack(T, cfg["gate"]), _pack(T, cfg["up"]), _pack(T, cfg["down"])
         self.logits = torch.from_numpy(cfg["logits"]).cuda()
         self.K, self.N, self.bits = 2048, 768, bits
@@ -500,8 +502,10 @@ class MoE(Workload):
         distinct = len(np.unique(idx.cpu().numpy()))
         self.per_call = distinct * (g.weight_bytes() + u.weight_bytes() + dn.weight_bytes()) // 128
         self.sample_x = cfg["x"]
-        self.desc = (f"MoE expert projection, M=8, 128 experts, top-8, hidden 2048, intermediate 768, {bits}-bit "
-                     f"group-64 gate/up/down ({distinct} distinct experts read); one call per step")
+        codes = ("NVFP4 (E2M1, an E4M3 scale per 16, an fp32 scale per expert)" if nvfp4
+                 else f"{bits}-bit group-64")
+        self.desc = (f"MoE expert projection, M=8, 128 experts, top-8, hidden 2048, intermediate 768, {codes} "
+                     f"gate/up/down ({distinct} distinct experts read); one call per step")
 
     def call(self, i, M, flags, x, out):
         g, u, dn = self.copies[i]
@@ -509,14 +513,12 @@ class MoE(Workload):
                            flags=flags)
 
     def sample_matrix(self):
-        w = self.cfg["gate"]
-        e0 = {"wq": w["wq"][0], "scales": w["scales"][0], "biases": w["biases"][0], "N": w["N"], "K": w["K"],
-              "bits": w["bits"]}
-        return e0, 128, "expert 0's gate matrix"
+        import oracle
+        return oracle.expert(self.cfg["gate"], 0), 128, "expert 0's gate matrix"
 
 
-WORKLOADS = ("gateup", "proj", "wide", "wide_rht", "readout", "step", "moe4", "moe8", "verify", "wide_nvfp4",
-             "readout_nvfp4")
+WORKLOADS = ("step", "gateup", "proj", "wide", "wide_rht", "readout", "moe4", "moe8", "moe_nvfp4", "verify",
+             "wide_nvfp4", "readout_nvfp4")
 PROJ_KINDS = ("proj", "wide", "wide_rht", "readout", "wide_nvfp4", "readout_nvfp4")
 
 
@@ -529,6 +531,8 @@ def make_workload(name, T, torch, l2_bytes):
         return Step(T, torch, l2_bytes)
     if name in ("moe4", "moe8"):
         return MoE(T, torch, l2_bytes, bits=int(name[3]))
+    if name == "moe_nvfp4":
+        return MoE(T, torch, l2_bytes, bits=4, code="nvfp4")
     raise ValueError(name)
 
 
@@ -849,15 +853,16 @@ class _HostOnly:
                 self.K, self.N, self.bits = 1024, 151936, 4
                 self.desc = "per-token weight stream of a 28-layer dense decoder (sampled: layer 0 QKV rows)"
             else:
-                bits = int(name[3])
-                cfg = synth.moe_layer(bits=bits)
-                g = cfg["gate"]
-                w = {"wq": g["wq"][0], "scales": g["scales"][0], "biases": g["biases"][0], "N": g["N"], "K": g["K"],
-                     "bits": g["bits"]}
+                import oracle
+                nvfp4 = name == "moe_nvfp4"
+                bits = 4 if nvfp4 else int(name[3])
+                cfg = synth.moe_layer(code="nvfp4") if nvfp4 else synth.moe_layer(bits=bits)
+                w = oracle.expert(cfg["gate"], 0)
                 x8, rows, what = cfg["x"], 128, "expert 0's gate matrix"
                 self.impl.step_ms = (8,)
                 self.K, self.N, self.bits = 2048, 768, bits
-                self.desc = f"MoE expert projection, M=8, 128 experts, top-8, {bits}-bit (sampled: expert 0 gate rows)"
+                codes = "NVFP4" if nvfp4 else f"{bits}-bit"
+                self.desc = f"MoE expert projection, M=8, 128 experts, top-8, {codes} (sampled: expert 0 gate rows)"
             self.impl.sample_x = x8
             self.impl.sample_matrix = lambda w=w, rows=rows, what=what: (w, rows, what)
             self.ms = sorted(set(self.impl.step_ms))
@@ -926,7 +931,7 @@ def main():
                          "K=1024, N=3072, M=1; wide: K=12800, N=2560, M=1 and 8; wide_rht: the same with the "
                          "input Hadamard transform; readout: RMSNorm + tied "
                          "readout, K=1024, N=151936, M=1 and 8; "
-                         "moe4 / moe8: MoE layer, M=8; verify: greedy generation with prompt-lookup drafts and "
+                         "moe4 / moe8 / moe_nvfp4: MoE layer, M=8 (4-bit, 8-bit, NVFP4 experts); verify: greedy generation with prompt-lookup drafts and "
                          "an up-to-8-row verify block on the 28-layer decoder; wide_nvfp4 / readout_nvfp4: the "
                          "wide and readout shapes with NVFP4 weights")
     args = ap.parse_args()

@@ -22,9 +22,10 @@
  * checkpoints; the pages give no layout, the format read here is NVIDIA's
  * published NVFP4, weights only: activations stay bf16). tf_qlinear_run,
  * tf_qlinear_run_rht, tf_qlinear_run_noalloc, tf_qmlp_gateup_run,
- * tf_decode_step_run (every matrix of the decoder in the one code; not the
+ * tf_qmoe_run (experts packed by tf_qlinear_pack_nvfp4_experts, one fp32 scale per
+ * expert), tf_decode_step_run (every matrix of the decoder in the one code; not the
  * single-kernel step of TF_TUNE_CHAIN = 2), tf_embed_rows and tf_generate_greedy
- * accept it; tf_qmoe_run returns TF_E_UNSUPPORTED_SHAPE.
+ * accept it.
  *
  * Conventions shared by every call:
  *   - Pointers named x, y, h, logits, residual, gamma, ws, packed and the
@@ -116,8 +117,9 @@ int tf_version(void);
 
 /*
  * Bytes of the packed buffer for `batch` matrices of N x K at `bits` with
- * `group` (bits 4 with group 16: the NVFP4 code). Returns 0 for an unsupported
- * combination (not 4/64, 8/64 or 4/16, K not a multiple of 64, N < 1, batch < 1).
+ * `group` (bits 4 with group 16: the NVFP4 code, whose buffer ends with a table of
+ * one fp32 scale per matrix). Returns 0 for an unsupported combination (not 4/64,
+ * 8/64 or 4/16, K not a multiple of 64, N < 1, batch < 1).
  */
 size_t tf_qlinear_packed_bytes(int64_t batch, int64_t N, int64_t K, int bits, int group);
 
@@ -156,11 +158,26 @@ int tf_qlinear_pack_nvfp4(const uint8_t* codes, const uint8_t* block_scales, flo
                           void* stream);
 
 /*
+ * tf_qlinear_pack_nvfp4 for a stack of E expert matrices of one MoE layer (the
+ * TensorFold page's NVFP4 checkpoints hold one scale per matrix):
+ *   codes          uint8 [E][N][K/2], block_scales uint8 [E][N][K/16] (as above)
+ *   global_scales  device fp32 [E]: the scale of each expert's matrix (read during the call)
+ *   packed         output, `packed_bytes` >= tf_qlinear_packed_bytes(E, N, K, 4, 16)
+ *   desc           output (batch E); desc->global_scale is 1 and unused: each matrix's
+ *                  scale is the packed buffer's table entry
+ * For tf_qmoe_run (gate, up: [E][I][H]; down: [E][H][I]). Asynchronous on `stream`.
+ */
+int tf_qlinear_pack_nvfp4_experts(const uint8_t* codes, const uint8_t* block_scales, const float* global_scales,
+                                  int64_t E, int64_t N, int64_t K, void* packed, size_t packed_bytes,
+                                  tf_qweight* desc, void* stream);
+
+/*
  * Inverse of tf_qlinear_pack: write the MLX-layout arrays back out of a packed
  * buffer (same shapes as the packer's inputs). Used to prove the packing is a
  * lossless permutation. For NVFP4 weights: the codes go to `wq` (the bytes of
- * uint8 [N][K/2]), the block scales to `scales` (the bytes of uint8 [N][K/16]),
- * and `biases` is not written (may be NULL).
+ * uint8 [batch][N][K/2]), the block scales to `scales` (the bytes of uint8
+ * [batch][N][K/16]), and `biases`, when not NULL, receives the per-matrix fp32
+ * scales (the bytes of fp32 [batch]).
  */
 int tf_qlinear_unpack_debug(const tf_qweight* w, uint32_t* wq, uint16_t* scales, uint16_t* biases,
                             void* stream);
@@ -280,6 +297,9 @@ int tf_qmlp_gateup_run(const tf_qweight* gate, const tf_qweight* up, const uint1
  * chose it; the weighted sum runs in slot order j (deterministic).
  *   gate, up       packed, batch = E experts of [I][H]
  *   down           packed, batch = E experts of [H][I]
+ *                  (all three in one weight code: MLX affine 4/8-bit from tf_qlinear_pack,
+ *                  or NVFP4 from tf_qlinear_pack_nvfp4_experts, each expert's matrix
+ *                  scaled by its own fp32 scale)
  *   router_logits  fp32 [M][E]
  *   x              bf16 [M][H] (row stride H)
  *   y              bf16 [M][H]

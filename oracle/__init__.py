@@ -239,7 +239,11 @@ def topk_softmax(logits, top_k: int):
 # ----------------------------------------------------------------------------
 
 def expert(w: dict, e: int) -> dict:
-    """The e-th matrix of a stacked [E, ...] weight dict."""
+    """The e-th matrix of a stacked [E, ...] weight dict (NVFP4 stacks: codes, block
+    scales and one global scale per expert)."""
+    if is_nvfp4(w):
+        return {"code": "nvfp4", "codes": w["codes"][e], "scales": w["scales"][e],
+                "gscale": np.float32(np.asarray(w["gscale"]).reshape(-1)[e]), "N": w["N"], "K": w["K"]}
     return {"wq": w["wq"][e], "scales": w["scales"][e], "biases": w["biases"][e],
             "N": w["N"], "K": w["K"], "bits": w["bits"]}
 

@@ -51,7 +51,7 @@ int check_desc(const tf_qweight* w, const char* name)
     const bool nvfp4 = w->code == TF_CODE_NVFP4;
     if (w->code != TF_CODE_AFFINE && !nvfp4)
         return fail(TF_E_BAD_PACK, "%s: unknown weight code %d", name, w->code);
-    if (nvfp4 ? (w->bits != 4 || w->group != 16 || w->batch != 1 || !std::isfinite(w->global_scale))
+    if (nvfp4 ? (w->bits != 4 || w->group != 16 || !std::isfinite(w->global_scale))
               : ((w->bits != 4 && w->bits != 8) || w->group != kGroup))
         return fail(TF_E_BAD_PACK, "%s: bits=%d group=%d do not match the weight code", name, w->bits, w->group);
     if (w->K <= 0 || w->K % kGroup != 0 || w->N <= 0 || w->batch <= 0)
@@ -82,16 +82,17 @@ const uint8_t* tiles_of(const tf_qweight* w)
     return static_cast<const uint8_t*>(w->data) + TF_PACK_HEADER_BYTES;
 }
 
+// The per-matrix fp32 scale table of an NVFP4 pack (after its matrices); null for affine codes.
+const float* nvfp4_scales_of(const tf_qweight* w)
+{
+    if (w->code != TF_CODE_NVFP4)
+        return nullptr;
+    return reinterpret_cast<const float*>(tiles_of(w) + w->batch * w->matrix_bytes);
+}
+
 size_t plan_scratch(const Plan& p) { return p.ws_counters + p.ws_partials; }
 
 // For the calls whose kernels read MLX affine codes only (the MoE layer).
-int check_affine(const tf_qweight* w, const char* name)
-{
-    int rc = check_desc(w, name);
-    if (rc == TF_OK && w->code != TF_CODE_AFFINE)
-        rc = fail(TF_E_UNSUPPORTED_SHAPE, "%s: the MoE layer takes MLX affine codes only (not NVFP4)", name);
-    return rc;
-}
 
 void fill_common(QProjParams& p, const Plan& pl, void* ws, uint8_t* scratch)
 {
@@ -514,7 +515,9 @@ size_t tf_qlinear_packed_bytes(int64_t batch, int64_t N, int64_t K, int bits, in
     if (!ok_code || K <= 0 || K % kGroup != 0 || N < 1 || batch < 1)
         return 0;
     const int64_t n_pad = (N + 15) / 16 * 16;
-    return (size_t)TF_PACK_HEADER_BYTES + (size_t)batch * (n_pad / 16) * (K / kGroup) * tile_bytes_for(bits);
+    const bool nvfp4 = group == 16;
+    return (size_t)TF_PACK_HEADER_BYTES + (size_t)batch * (n_pad / 16) * (K / kGroup) * tile_bytes_for(bits) +
+           (nvfp4 ? nvfp4_scale_table_bytes(batch) : 0);
 }
 
 int tf_qlinear_pack(const uint32_t* wq, const uint16_t* scales, const uint16_t* biases, int64_t batch, int64_t N,
@@ -557,23 +560,23 @@ int tf_qlinear_pack(const uint32_t* wq, const uint16_t* scales, const uint16_t* 
     return TF_OK;
 }
 
-int tf_qlinear_pack_nvfp4(const uint8_t* codes, const uint8_t* block_scales, float global_scale, int64_t N, int64_t K,
-                          void* packed, size_t packed_bytes, tf_qweight* desc, void* stream)
+static int pack_nvfp4_impl(const uint8_t* codes, const uint8_t* block_scales, float global_scale,
+                           const float* global_scales, int64_t batch, int64_t N, int64_t K, void* packed,
+                           size_t packed_bytes, tf_qweight* desc, void* stream, const char* name)
 {
     if (K <= 0 || K % kGroup != 0)
-        return fail(TF_E_UNSUPPORTED_SHAPE, "tf_qlinear_pack_nvfp4: K must be a positive multiple of 64");
-    if (N < 1)
-        return fail(TF_E_INVALID_ARG, "tf_qlinear_pack_nvfp4: N must be >= 1");
+        return fail(TF_E_UNSUPPORTED_SHAPE, "%s: K must be a positive multiple of 64", name);
+    if (N < 1 || batch < 1)
+        return fail(TF_E_INVALID_ARG, "%s: N and the number of matrices must be >= 1", name);
     if (!std::isfinite(global_scale))
-        return fail(TF_E_INVALID_ARG, "tf_qlinear_pack_nvfp4: global_scale must be finite");
+        return fail(TF_E_INVALID_ARG, "%s: global_scale must be finite", name);
     if (codes == nullptr || block_scales == nullptr || packed == nullptr || desc == nullptr)
-        return fail(TF_E_INVALID_ARG, "tf_qlinear_pack_nvfp4: NULL pointer");
+        return fail(TF_E_INVALID_ARG, "%s: NULL pointer", name);
     if (!aligned(packed, 16))
-        return fail(TF_E_INVALID_ARG, "tf_qlinear_pack_nvfp4: packed must be 16-byte aligned");
-    const size_t need = tf_qlinear_packed_bytes(1, N, K, 4, 16);
+        return fail(TF_E_INVALID_ARG, "%s: packed must be 16-byte aligned", name);
+    const size_t need = tf_qlinear_packed_bytes(batch, N, K, 4, 16);
     if (packed_bytes < need)
-        return fail(TF_E_WORKSPACE_TOO_SMALL, "tf_qlinear_pack_nvfp4: packed buffer has %zu bytes, needs %zu",
-                    packed_bytes, need);
+        return fail(TF_E_WORKSPACE_TOO_SMALL, "%s: packed buffer has %zu bytes, needs %zu", name, packed_bytes, need);
     PackHeader h{};
     h.magic = TF_QWEIGHT_MAGIC;
     h.version = TF_PACK_VERSION;
@@ -581,16 +584,16 @@ int tf_qlinear_pack_nvfp4(const uint8_t* codes, const uint8_t* block_scales, flo
     h.group = 16;
     h.code = TF_CODE_NVFP4;
     h.global_scale = global_scale;
-    h.batch = 1;
+    h.batch = batch;
     h.N = N;
     h.K = K;
     h.n_pad = (N + 15) / 16 * 16;
     h.tile_bytes = tile_bytes_for(kNvfp4);
     h.matrix_bytes = h.n_pad / 16 * (K / kGroup) * h.tile_bytes;
-    cudaError_t e = launch_pack_nvfp4(codes, block_scales, N, K, static_cast<uint8_t*>(packed), h,
-                                      static_cast<cudaStream_t>(stream));
+    cudaError_t e = launch_pack_nvfp4(codes, block_scales, global_scales, batch, N, K, static_cast<uint8_t*>(packed),
+                                      h, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess)
-        return cuda_fail(e, "tf_qlinear_pack_nvfp4");
+        return cuda_fail(e, name);
     desc->magic = h.magic;
     desc->version = h.version;
     desc->bits = h.bits;
@@ -607,6 +610,25 @@ int tf_qlinear_pack_nvfp4(const uint8_t* codes, const uint8_t* block_scales, flo
     return TF_OK;
 }
 
+int tf_qlinear_pack_nvfp4(const uint8_t* codes, const uint8_t* block_scales, float global_scale, int64_t N, int64_t K,
+                          void* packed, size_t packed_bytes, tf_qweight* desc, void* stream)
+{
+    return pack_nvfp4_impl(codes, block_scales, global_scale, nullptr, 1, N, K, packed, packed_bytes, desc, stream,
+                           "tf_qlinear_pack_nvfp4");
+}
+
+int tf_qlinear_pack_nvfp4_experts(const uint8_t* codes, const uint8_t* block_scales, const float* global_scales,
+                                  int64_t E, int64_t N, int64_t K, void* packed, size_t packed_bytes, tf_qweight* desc,
+                                  void* stream)
+{
+    if (global_scales == nullptr || !aligned(global_scales, 4))
+        return fail(TF_E_INVALID_ARG, "tf_qlinear_pack_nvfp4_experts: global_scales NULL or misaligned");
+    // the descriptor's own global_scale is not used for a batch: each matrix's comes from the
+    // scale table in the packed buffer
+    return pack_nvfp4_impl(codes, block_scales, 1.f, global_scales, E, N, K, packed, packed_bytes, desc, stream,
+                           "tf_qlinear_pack_nvfp4_experts");
+}
+
 int tf_qlinear_unpack_debug(const tf_qweight* w, uint32_t* wq, uint16_t* scales, uint16_t* biases, void* stream)
 {
     int rc = check_desc(w, "tf_qlinear_unpack_debug");
@@ -615,9 +637,15 @@ int tf_qlinear_unpack_debug(const tf_qweight* w, uint32_t* wq, uint16_t* scales,
     if (w->code == TF_CODE_NVFP4) {
         if (wq == nullptr || scales == nullptr)
             return fail(TF_E_INVALID_ARG, "tf_qlinear_unpack_debug: NULL output");
-        cudaError_t e = launch_unpack_nvfp4(static_cast<const uint8_t*>(w->data), w->N, w->K,
-                                            reinterpret_cast<uint8_t*>(wq), reinterpret_cast<uint8_t*>(scales),
-                                            static_cast<cudaStream_t>(stream));
+        cudaStream_t st = static_cast<cudaStream_t>(stream);
+        cudaError_t e = cudaSuccess;
+        for (int64_t b = 0; b < w->batch && e == cudaSuccess; ++b)
+            e = launch_unpack_nvfp4(static_cast<const uint8_t*>(w->data) + b * w->matrix_bytes, w->N, w->K,
+                                    reinterpret_cast<uint8_t*>(wq) + b * w->N * (w->K / 2),
+                                    reinterpret_cast<uint8_t*>(scales) + b * w->N * (w->K / 16), st);
+        if (e == cudaSuccess && biases != nullptr)  // the per-matrix fp32 scales, when asked for
+            e = cudaMemcpyAsync(biases, nvfp4_scales_of(w), (size_t)w->batch * sizeof(float),
+                                cudaMemcpyDeviceToDevice, st);
         return e == cudaSuccess ? TF_OK : cuda_fail(e, "tf_qlinear_unpack_debug");
     }
     if (wq == nullptr || scales == nullptr || biases == nullptr)
@@ -829,8 +857,8 @@ MoeLayout moe_layout(const tf_qweight* gate, const tf_qweight* down, int64_t M, 
     MoeLayout L{};
     const int E = (int)gate->batch;
     L.slots = (int)(M * top_k < E ? M * top_k : E);
-    L.pgu = plan_qproj((int)(gate->n_pad / 16), (int)(gate->K / kGroup), 2, gate->bits, L.slots, 0, kMaxM);
-    L.pdn = plan_qproj((int)(down->n_pad / 16), (int)(down->K / kGroup), 1, down->bits, L.slots, 0, kMaxM);
+    L.pgu = plan_qproj((int)(gate->n_pad / 16), (int)(gate->K / kGroup), 2, kernel_bits(gate), L.slots, 0, kMaxM);
+    L.pdn = plan_qproj((int)(down->n_pad / 16), (int)(down->K / kGroup), 1, kernel_bits(down), L.slots, 0, kMaxM);
     L.meta = kStatusBytes;
     L.h = align_up(L.meta + sizeof(MoeMeta), 256);
     L.o = align_up(L.h + (size_t)L.slots * kMaxM * gate->N * sizeof(uint16_t), 256);
@@ -843,9 +871,11 @@ MoeLayout moe_layout(const tf_qweight* gate, const tf_qweight* down, int64_t M, 
 int check_moe(const tf_qweight* gate, const tf_qweight* up, const tf_qweight* down, int64_t M, int top_k,
               const char* name)
 {
-    int rc = check_affine(gate, "gate");
-    if (rc || (rc = check_affine(up, "up")) || (rc = check_affine(down, "down")))
+    int rc = check_desc(gate, "gate");
+    if (rc || (rc = check_desc(up, "up")) || (rc = check_desc(down, "down")))
         return rc;
+    if (up->code != gate->code || down->code != gate->code)
+        return fail(TF_E_UNSUPPORTED_SHAPE, "%s: gate, up and down must share one weight code", name);
     if (up->batch != gate->batch || down->batch != gate->batch || up->N != gate->N || up->K != gate->K ||
         down->K != gate->N || down->N != gate->K || up->bits != gate->bits || down->bits != gate->bits)
         return fail(TF_E_UNSUPPORTED_SHAPE, "%s: expert shapes must be gate/up [E][I][H], down [E][H][I]", name);
@@ -913,7 +943,9 @@ int tf_qmoe_run(const tf_qweight* gate, const tf_qweight* up, const tf_qweight* 
     p.meta = meta;
     p.gather = 1;
     fill_common(p, L.pgu, ws, wsb + L.gu);
-    e = launch_qproj(gate->bits, true, true, L.pgu, p, s, true);
+    p.wscales0 = nvfp4_scales_of(gate);
+    p.wscales1 = nvfp4_scales_of(up);
+    e = launch_qproj(kernel_bits(gate), true, true, L.pgu, p, s, true);
     if (e != cudaSuccess)
         return cuda_fail(e, "tf_qmoe_run: gate/up");
 
@@ -935,7 +967,8 @@ int tf_qmoe_run(const tf_qweight* gate, const tf_qweight* up, const tf_qweight* 
     q.meta = meta;
     q.gather = 0;
     fill_common(q, L.pdn, ws, wsb + L.dn);
-    e = launch_qproj(down->bits, false, true, L.pdn, q, s, true);
+    q.wscales0 = nvfp4_scales_of(down);
+    e = launch_qproj(kernel_bits(down), false, true, L.pdn, q, s, true);
     if (e != cudaSuccess)
         return cuda_fail(e, "tf_qmoe_run: down");
 

@@ -94,6 +94,9 @@ struct QProjParams {
     int x_direct;   // activations loaded straight into registers (unsplit calls), not by bulk copy
     const uint8_t* rht;  // input Hadamard transform signs (K bits, LSB first, set = -1) or nullptr
     float wscale0, wscale1;  // NVFP4: global scale of matrix 0 / 1 (unused by affine codes)
+    // NVFP4 MoE: the fp32 scale of every expert of matrix 0 / 1, indexed by expert
+    const float* wscales0;
+    const float* wscales1;
 };
 
 struct Plan {
@@ -166,12 +169,13 @@ cudaError_t launch_qproj_b8_single(bool moe, const Plan& plan, const QProjParams
 cudaError_t launch_qproj_b8_dual(bool moe, const Plan& plan, const QProjParams& p, cudaStream_t stream, bool pdl);
 
 cudaError_t launch_qproj_nvfp4(bool dual, const Plan& plan, const QProjParams& p, cudaStream_t stream, bool pdl);
+cudaError_t launch_qproj_nvfp4_moe(bool dual, const Plan& plan, const QProjParams& p, cudaStream_t stream, bool pdl);
 
 inline cudaError_t launch_qproj(int bits, bool dual, bool moe, const Plan& plan, const QProjParams& p,
                                 cudaStream_t stream, bool pdl)
 {
     if (bits == kNvfp4)
-        return moe ? cudaErrorInvalidValue : launch_qproj_nvfp4(dual, plan, p, stream, pdl);
+        return moe ? launch_qproj_nvfp4_moe(dual, plan, p, stream, pdl) : launch_qproj_nvfp4(dual, plan, p, stream, pdl);
     if (bits == 4)
         return dual ? launch_qproj_b4_dual(moe, plan, p, stream, pdl) : launch_qproj_b4_single(moe, plan, p, stream, pdl);
     return dual ? launch_qproj_b8_dual(moe, plan, p, stream, pdl) : launch_qproj_b8_single(moe, plan, p, stream, pdl);
@@ -182,8 +186,10 @@ cudaError_t launch_pack(const uint32_t* wq, const uint16_t* s, const uint16_t* b
                         int64_t K, int bits, uint8_t* packed, cudaStream_t stream);
 cudaError_t launch_unpack(const uint8_t* packed, int64_t batch, int64_t N, int64_t K, int bits, uint32_t* wq,
                           uint16_t* s, uint16_t* b, cudaStream_t stream);
-cudaError_t launch_pack_nvfp4(const uint8_t* codes, const uint8_t* scales, int64_t N, int64_t K, uint8_t* packed,
-                              const PackHeader& hdr, cudaStream_t stream);
+// batch matrices [batch][N][K/2] codes, [batch][N][K/16] scales; their fp32 scales from the
+// device array gscales [batch], or hdr.global_scale when gscales is null (batch 1)
+cudaError_t launch_pack_nvfp4(const uint8_t* codes, const uint8_t* scales, const float* gscales, int64_t batch,
+                              int64_t N, int64_t K, uint8_t* packed, const PackHeader& hdr, cudaStream_t stream);
 cudaError_t launch_unpack_nvfp4(const uint8_t* packed, int64_t N, int64_t K, uint8_t* codes, uint8_t* scales,
                                 cudaStream_t stream);
 
@@ -198,5 +204,7 @@ cudaError_t launch_embed_rows(const uint8_t* packed, int64_t N, int64_t K, int b
                               int64_t M, uint16_t* x, int64_t ldx, int* status, cudaStream_t stream);
 // The kernels' BITS value of a descriptor's weight code.
 inline int desc_kernel_bits(const tf_qweight* w) { return w->code == TF_CODE_NVFP4 ? kNvfp4 : w->bits; }
+// Bytes of the per-matrix fp32 scale table after the matrices of an NVFP4 pack.
+inline size_t nvfp4_scale_table_bytes(int64_t batch) { return ((size_t)batch * 4 + 15) / 16 * 16; }
 
 }  // namespace tfq

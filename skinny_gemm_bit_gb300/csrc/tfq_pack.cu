@@ -211,14 +211,14 @@ __global__ void embed_rows_kernel(const uint8_t* __restrict__ packed, int64_t N,
 }
 
 __global__ void pack_nvfp4_kernel(const uint8_t* __restrict__ codes, const uint8_t* __restrict__ scales, int64_t N,
-                                  int64_t K, uint8_t* __restrict__ packed, PackHeader hdr)
+                                  int64_t K, uint8_t* __restrict__ packed, PackHeader hdr, bool write_header)
 {
     const int64_t G = K / kGroup;
     const int64_t n_rb = (N + kRowsPerBlock - 1) / kRowsPerBlock;
     constexpr int tile_words = tile_bytes_for(kNvfp4) / 4, q_words = tile_q_bytes_for(kNvfp4) / 4;
     const int64_t total = n_rb * G * tile_words;
     uint32_t* out = reinterpret_cast<uint32_t*>(packed + TF_PACK_HEADER_BYTES);
-    if (blockIdx.x == 0 && threadIdx.x == 0)
+    if (write_header && blockIdx.x == 0 && threadIdx.x == 0)
         *reinterpret_cast<PackHeader*>(packed) = hdr;
     for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
          idx += (int64_t)gridDim.x * blockDim.x) {
@@ -316,11 +316,28 @@ cudaError_t launch_unpack(const uint8_t* packed, int64_t batch, int64_t N, int64
     return cudaGetLastError();
 }
 
-cudaError_t launch_pack_nvfp4(const uint8_t* codes, const uint8_t* scales, int64_t N, int64_t K, uint8_t* packed,
-                              const PackHeader& hdr, cudaStream_t stream)
+// The per-matrix fp32 scales of a packed NVFP4 buffer, after its matrices: from a device
+// array (src != nullptr) or, for one matrix, the value given.
+__global__ void nvfp4_scale_table_kernel(float* __restrict__ table, const float* __restrict__ src, float value,
+                                         int64_t batch)
+{
+    for (int64_t e = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; e < batch; e += (int64_t)gridDim.x * blockDim.x)
+        table[e] = src != nullptr ? src[e] : value;
+}
+
+cudaError_t launch_pack_nvfp4(const uint8_t* codes, const uint8_t* scales, const float* gscales, int64_t batch,
+                              int64_t N, int64_t K, uint8_t* packed, const PackHeader& hdr, cudaStream_t stream)
 {
     const int64_t total = (hdr.n_pad / kRowsPerBlock) * (K / kGroup) * (tile_bytes_for(kNvfp4) / 4);
-    pack_nvfp4_kernel<<<grid_for(total, 256), 256, 0, stream>>>(codes, scales, N, K, packed, hdr);
+    for (int64_t e = 0; e < batch; ++e) {
+        pack_nvfp4_kernel<<<grid_for(total, 256), 256, 0, stream>>>(codes + e * N * (K / 2), scales + e * N * (K / 16),
+                                                                    N, K, packed + e * hdr.matrix_bytes, hdr, e == 0);
+        const cudaError_t err = cudaGetLastError();
+        if (err != cudaSuccess)
+            return err;
+    }
+    float* table = reinterpret_cast<float*>(packed + TF_PACK_HEADER_BYTES + batch * hdr.matrix_bytes);
+    nvfp4_scale_table_kernel<<<grid_for(batch, 128), 128, 0, stream>>>(table, gscales, hdr.global_scale, batch);
     return cudaGetLastError();
 }
 

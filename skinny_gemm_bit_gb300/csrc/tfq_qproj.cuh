@@ -1087,12 +1087,19 @@ __global__ void __launch_bounds__((NWT + 1) * 32, NWT == 8 ? 2 : 1) qproj_kernel
             }
         }
 
-        if constexpr (BITS == kNvfp4) {  // the matrices' global scales
+        if constexpr (BITS == kNvfp4) {  // the matrices' global scales (an MoE problem's: its expert's)
+            float sc0 = p.wscale0, sc1 = p.wscale1;
+            if constexpr (MOE) {
+                const int e = slot_ec[first.x].x;
+                sc0 = __ldg(p.wscales0 + e);
+                if constexpr (DUAL)
+                    sc1 = __ldg(p.wscales1 + e);
+            }
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                acc0[i] *= p.wscale0;
+                acc0[i] *= sc0;
                 if constexpr (DUAL)
-                    acc1[i] *= p.wscale1;
+                    acc1[i] *= sc1;
             }
         }
 
@@ -1494,12 +1501,19 @@ __global__ void __launch_bounds__(kThreads, 1) qproj_warp_kernel(const __grid_co
                         acc1[i] = 0.f;
                     }
                 }
-                if constexpr (BITS == kNvfp4) {  // the matrices' global scales
+                if constexpr (BITS == kNvfp4) {  // the matrices' global scales (an MoE problem's: its expert's)
+                    float sc0 = p.wscale0, sc1 = p.wscale1;
+                    if constexpr (MOE) {
+                        const int e = slot_ec[pp].x;
+                        sc0 = __ldg(p.wscales0 + e);
+                        if constexpr (DUAL)
+                            sc1 = __ldg(p.wscales1 + e);
+                    }
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
-                        acc0[i] *= p.wscale0;
+                        acc0[i] *= sc0;
                         if constexpr (DUAL)
-                            acc1[i] *= p.wscale1;
+                            acc1[i] *= sc1;
                     }
                 }
                 if (S == 1 && len == p.groups) {

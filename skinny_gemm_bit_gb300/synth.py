@@ -98,19 +98,25 @@ def quant_weights(rng, N: int, K: int, bits: int = 4, batch: int | None = None) 
     return {"wq": wq, "scales": scales, "biases": biases, "N": N, "K": K, "bits": bits}
 
 
-def nvfp4_weights(rng, N: int, K: int) -> dict:
-    """Random NVFP4 weights: codes uint8 [N, K/2] (even column in the low nibble),
-    E4M3 block scales uint8 [N, K/16], fp32 global scale."""
+def nvfp4_weights(rng, N: int, K: int, batch: int | None = None) -> dict:
+    """Random NVFP4 weights: codes uint8 [(B,) N, K/2] (even column in the low nibble),
+    E4M3 block scales uint8 [(B,) N, K/16], fp32 global scale (a stack of B experts: one
+    per expert, 0.004 times a power of two from 1/2 to 2, so each expert's differs)."""
     if K % GROUP:
         raise ValueError("K must be a multiple of 64")
-    codes = rng.integers(0, 256, size=(N, K // 2), dtype=np.uint8)
-    e = rng.integers(4, 12, size=(N, K // 16), dtype=np.uint8)
-    m = rng.integers(0, 8, size=(N, K // 16), dtype=np.uint8)
+    lead = () if batch is None else (batch,)
+    codes = rng.integers(0, 256, size=lead + (N, K // 2), dtype=np.uint8)
+    e = rng.integers(4, 12, size=lead + (N, K // 16), dtype=np.uint8)
+    m = rng.integers(0, 8, size=lead + (N, K // 16), dtype=np.uint8)
     scales = (e << 3) | m
-    edge = rng.integers(0, 64, size=(N, K // 16)) == 0
-    pick = np.array([0x00, 0x01, 0x07, 0x7E], dtype=np.uint8)[rng.integers(0, 4, size=(N, K // 16))]
+    edge = rng.integers(0, 64, size=lead + (N, K // 16)) == 0
+    pick = np.array([0x00, 0x01, 0x07, 0x7E], dtype=np.uint8)[rng.integers(0, 4, size=lead + (N, K // 16))]
     scales = np.where(edge, pick, scales).astype(np.uint8)
-    return {"code": "nvfp4", "codes": codes, "scales": scales, "gscale": np.float32(0.004), "N": N, "K": K}
+    if batch is None:
+        gscale = np.float32(0.004)
+    else:
+        gscale = (np.float32(0.004) * np.exp2(rng.integers(-1, 2, size=batch)).astype(np.float32)).astype(np.float32)
+    return {"code": "nvfp4", "codes": codes, "scales": scales, "gscale": gscale, "N": N, "K": K}
 
 
 def concat_rows(*ws) -> dict:
@@ -187,12 +193,17 @@ def decoder(seed: int = 3, n_layers: int = 28, d_model: int = 1024, d_ff: int = 
 
 
 def moe_layer(seed: int = 4, M: int = 8, E: int = 128, top_k: int = 8, hidden: int = 2048,
-              inter: int = 768, bits: int = 4) -> dict:
-    """MoE layer: router logits, per-expert gate/up [E, inter, hidden], down [E, hidden, inter]."""
+              inter: int = 768, bits: int = 4, code: str = "mlx") -> dict:
+    """MoE layer: router logits, per-expert gate/up [E, inter, hidden], down [E, hidden, inter]
+    (MLX affine codes of `bits`, or NVFP4 experts with code="nvfp4")."""
     rng = np.random.default_rng(seed)
     x = activations(rng, M, hidden)
     logits = router_logits(rng, M, E)
-    gate = quant_weights(rng, inter, hidden, bits, batch=E)
-    up = quant_weights(rng, inter, hidden, bits, batch=E)
-    down = quant_weights(rng, hidden, inter, bits, batch=E)
+
+    def weights(N, K):
+        return nvfp4_weights(rng, N, K, batch=E) if code == "nvfp4" else quant_weights(rng, N, K, bits, batch=E)
+
+    gate = weights(inter, hidden)
+    up = weights(inter, hidden)
+    down = weights(hidden, inter)
     return {"x": x, "logits": logits, "gate": gate, "up": up, "down": down, "top_k": top_k}

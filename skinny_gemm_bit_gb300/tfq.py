@@ -79,6 +79,7 @@ _SIGS = {
     "tf_qlinear_pack": (ctypes.c_int, [P, P, P, I64, I64, I64, ctypes.c_int, ctypes.c_int, P, SZ,
                                        ctypes.POINTER(tf_qweight), P]),
     "tf_qlinear_pack_nvfp4": (ctypes.c_int, [P, P, ctypes.c_float, I64, I64, P, SZ, ctypes.POINTER(tf_qweight), P]),
+    "tf_qlinear_pack_nvfp4_experts": (ctypes.c_int, [P, P, P, I64, I64, I64, P, SZ, ctypes.POINTER(tf_qweight), P]),
     "tf_qlinear_unpack_debug": (ctypes.c_int, [ctypes.POINTER(tf_qweight), P, P, P, P]),
     "tf_qweight_check": (ctypes.c_int, [ctypes.POINTER(tf_qweight), P]),
     "tf_qlinear_workspace_bytes": (SZ, [ctypes.POINTER(tf_qweight), I64]),
@@ -228,34 +229,46 @@ def tf_qlinear_pack(wq, scales, biases, bits: int, device="cuda", stream=None) -
     return QWeight(buf, desc)
 
 
-def tf_qlinear_pack_nvfp4(codes, block_scales, global_scale: float, device="cuda", stream=None) -> QWeight:
+def tf_qlinear_pack_nvfp4(codes, block_scales, global_scale, device="cuda", stream=None) -> QWeight:
     """Pack NVFP4 weights (codes uint8 [N, K/2], E4M3 block scales uint8 [N, K/16], fp32
-    global scale) into a QWeight."""
+    global scale) into a QWeight; a stack of experts (codes [E, N, K/2], block scales
+    [E, N, K/16], global scales fp32 [E]) goes through tf_qlinear_pack_nvfp4_experts."""
     codes = _as_dev(codes, torch.uint8, device)
     block_scales = _as_dev(block_scales, torch.uint8, device)
-    N, K = codes.shape[0], codes.shape[1] * 2
-    if codes.dtype != torch.uint8 or block_scales.dtype != torch.uint8 or tuple(block_scales.shape) != (N, K // 16):
-        raise TfqError(TF_E_INVALID_ARG, "codes must be uint8 [N, K/2] and block_scales uint8 [N, K/16]")
-    nbytes = packed_bytes(1, N, K, 4, 16)
+    experts = codes.dim() == 3
+    E = codes.shape[0] if experts else 1
+    N, K = codes.shape[-2], codes.shape[-1] * 2
+    lead = (E,) if experts else ()
+    if codes.dtype != torch.uint8 or block_scales.dtype != torch.uint8 or tuple(block_scales.shape) != lead + (N, K // 16):
+        raise TfqError(TF_E_INVALID_ARG, "codes must be uint8 [(E,) N, K/2] and block_scales uint8 [(E,) N, K/16]")
+    nbytes = packed_bytes(E, N, K, 4, 16)
     if nbytes == 0:
         raise TfqError(TF_E_UNSUPPORTED_SHAPE, f"unsupported NVFP4 packing N={N} K={K}")
     buf = torch.empty(nbytes, dtype=torch.uint8, device=device)
     desc = tf_qweight()
-    _check(lib().tf_qlinear_pack_nvfp4(_ptr(codes), _ptr(block_scales), float(global_scale), N, K, _ptr(buf), nbytes,
-                                       ctypes.byref(desc), _stream(stream)))
+    if experts:
+        gs = torch.as_tensor(np.asarray(global_scale, dtype=np.float32).reshape(E)).to(device)
+        _check(lib().tf_qlinear_pack_nvfp4_experts(_ptr(codes), _ptr(block_scales), _ptr(gs), E, N, K, _ptr(buf),
+                                                   nbytes, ctypes.byref(desc), _stream(stream)))
+    else:
+        _check(lib().tf_qlinear_pack_nvfp4(_ptr(codes), _ptr(block_scales), float(global_scale), N, K, _ptr(buf),
+                                           nbytes, ctypes.byref(desc), _stream(stream)))
     torch.cuda.current_stream().synchronize() if stream is None else stream.synchronize()
     return QWeight(buf, desc)
 
 
 def tf_qlinear_unpack_debug(w: QWeight, stream=None):
     """(wq int32, scales int16, biases int16) in MLX layout, read back out of the packed buffer;
-    for NVFP4 weights (codes uint8 [N, K/2], block scales uint8 [N, K/16], None)."""
+    for NVFP4 weights (codes uint8 [(E,) N, K/2], block scales uint8 [(E,) N, K/16], the
+    per-matrix fp32 scales [E])."""
     dev = w.buf.device
     if w.code == TF_CODE_NVFP4:
-        codes = torch.empty((w.N, w.K // 2), dtype=torch.uint8, device=dev)
-        sc = torch.empty((w.N, w.K // 16), dtype=torch.uint8, device=dev)
-        _check(lib().tf_qlinear_unpack_debug(ctypes.byref(w.desc), _ptr(codes), _ptr(sc), None, _stream(stream)))
-        return codes, sc, None
+        lead = (w.batch,) if w.batch > 1 else ()
+        codes = torch.empty(lead + (w.N, w.K // 2), dtype=torch.uint8, device=dev)
+        sc = torch.empty(lead + (w.N, w.K // 16), dtype=torch.uint8, device=dev)
+        gs = torch.empty(w.batch, dtype=torch.float32, device=dev)
+        _check(lib().tf_qlinear_unpack_debug(ctypes.byref(w.desc), _ptr(codes), _ptr(sc), _ptr(gs), _stream(stream)))
+        return codes, sc, gs
     lead = (w.batch,) if w.batch > 1 else ()
     wq = torch.empty(lead + (w.N, w.K * w.bits // 32), dtype=torch.int32, device=dev)
     s = torch.empty(lead + (w.N, w.K // 64), dtype=torch.int16, device=dev)

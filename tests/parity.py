@@ -63,7 +63,7 @@ def assert_close(y, ref, tol, what=""):
 
 def pack(T, w: dict):
     if w.get("code") == "nvfp4":
-        return T.tf_qlinear_pack_nvfp4(w["codes"], w["scales"], float(w["gscale"]))
+        return T.tf_qlinear_pack_nvfp4(w["codes"], w["scales"], w["gscale"])
     return T.tf_qlinear_pack(w["wq"], w["scales"], w["biases"], w["bits"])
 
 

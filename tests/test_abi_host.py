@@ -44,7 +44,7 @@ def test_binding_covers_every_declared_symbol(T):
 def test_status_strings(T):
     for code, name in [(0, "TF_OK"), (1, "TF_E_INVALID_ARG"), (2, "TF_E_UNSUPPORTED_SHAPE"),
                        (3, "TF_E_WORKSPACE_TOO_SMALL"), (4, "TF_E_BAD_PACK"), (5, "TF_E_CUDA"),
-                       (6, "TF_E_TIMEOUT")]:
+                       (6, "TF_E_TIMEOUT"), (7, "TF_E_INTERNAL")]:
         assert T.status_str(code) == name
     assert T.status_str(99) == "TF_E_UNKNOWN"
     assert T.lib().tf_version() >= 10000
@@ -58,8 +58,11 @@ def test_packed_bytes(T):
     for bad in [(1, 64, 64, 3, 64), (1, 64, 64, 4, 32), (1, 64, 100, 4, 64), (1, 0, 64, 4, 64), (0, 64, 64, 4, 64),
                 (1, 64, 64, 8, 16), (1, 64, 96, 4, 16)]:
         assert L.tf_qlinear_packed_bytes(*bad) == 0
-    # NVFP4 (bits 4, group 16): 512 bytes of codes + 64 of block scales a 16 x 64 tile
-    assert L.tf_qlinear_packed_bytes(1, 2560, 12800, 4, 16) == 256 + 160 * 200 * 576
+    # NVFP4 (bits 4, group 16): 512 bytes of codes + 64 of block scales a 16 x 64 tile, then
+    # one fp32 scale per matrix (the table padded to 16 bytes)
+    assert L.tf_qlinear_packed_bytes(1, 2560, 12800, 4, 16) == 256 + 160 * 200 * 576 + 16
+    assert L.tf_qlinear_packed_bytes(128, 768, 2048, 4, 16) == 256 + 128 * 48 * 32 * 576 + 512
+    assert L.tf_qlinear_packed_bytes(5, 64, 64, 4, 16) == 256 + 5 * 4 * 576 + 32
 
 
 FAKE = ctypes.c_void_p(0x10000)  # aligned, never dereferenced: validation fails first
@@ -157,7 +160,7 @@ def test_nvfp4_descriptors_are_validated(T):
     L = T.lib()
     good = _nvfp4_desc(T)
     assert L.tf_qlinear_workspace_bytes(ctypes.byref(good), 8) >= 256
-    for field, value in [("group", 64), ("bits", 8), ("batch", 2), ("global_scale", float("nan")),
+    for field, value in [("group", 64), ("bits", 8), ("global_scale", float("nan")),
                          ("global_scale", float("inf")), ("code", 7)]:
         d = _nvfp4_desc(T)
         setattr(d, field, value)
@@ -183,12 +186,22 @@ def test_nvfp4_pack_refuses_bad_arguments(T):
     assert d.magic == 0
 
 
-def test_nvfp4_weights_are_refused_where_only_affine_codes_run(T):
+def test_weight_codes_are_not_mixed(T):
     L = T.lib()
     d = _nvfp4_desc(T)
-    # the MoE layer (three NVFP4 expert stacks)
-    assert L.tf_qmoe_workspace_bytes(ctypes.byref(d), ctypes.byref(d), ctypes.byref(d), 1, 1) == 0
-    assert "NVFP4" in T.last_error()
+    # a stack of NVFP4 experts is a valid descriptor; a single projection of it is refused
+    e2 = _nvfp4_desc(T)
+    e2.batch = 2
+    assert L.tf_qlinear_workspace_bytes(ctypes.byref(e2), 8) >= 256
+    assert L.tf_qlinear_run(ctypes.byref(e2), FAKE, 128, 1, None, 1e-6, None, FAKE, T.TF_DTYPE_BF16, FAKE, 1 << 20, 0,
+                            None) == T.TF_E_UNSUPPORTED_SHAPE
+    # the MoE layer takes NVFP4 experts (gate/up [E][I][H], down [E][H][I]) ...
+    g, dn = _nvfp4_desc(T, N=64, K=128), _nvfp4_desc(T, N=128, K=64)
+    assert L.tf_qmoe_workspace_bytes(ctypes.byref(g), ctypes.byref(g), ctypes.byref(dn), 1, 1) > 0
+    # ... but not a mix of codes
+    a_dn = _desc(T, N=128, K=64)
+    assert L.tf_qmoe_workspace_bytes(ctypes.byref(g), ctypes.byref(g), ctypes.byref(a_dn), 1, 1) == 0
+    assert "one weight code" in T.last_error()
     # gate and up must carry the same code
     a = _desc(T)
     ws = L.tf_qmlp_gateup_run(ctypes.byref(a), ctypes.byref(d), FAKE, 128, 1, None, 1e-6, FAKE, FAKE, 1 << 20, 0,

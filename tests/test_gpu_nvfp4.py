@@ -302,3 +302,33 @@ def test_chained_step_refuses_nvfp4(T):
         assert e.value.status == T.TF_E_UNSUPPORTED_SHAPE
     finally:
         T.tune_set(T.TF_TUNE_CHAIN, -1)
+
+
+# ------------------------------------------------------------------ MoE experts
+
+def test_pack_experts_roundtrip(T):
+    # a stack of 5 expert matrices with their own fp32 scales: codes, block scales and the
+    # scale table come back bit for bit
+    w = synth.nvfp4_weights(np.random.default_rng(501), 40, 128, batch=5)
+    qw = T.tf_qlinear_pack_nvfp4(w["codes"], w["scales"], w["gscale"])
+    T.tf_qweight_check(qw)
+    assert qw.batch == 5 and qw.code == T.TF_CODE_NVFP4
+    codes, scales, gs = T.tf_qlinear_unpack_debug(qw)
+    assert np.array_equal(codes.cpu().numpy(), w["codes"]) and np.array_equal(scales.cpu().numpy(), w["scales"])
+    assert np.array_equal(gs.cpu().numpy(), w["gscale"])
+    assert len(set(w["gscale"].tolist())) > 1  # the experts' scales differ, so pairing them matters
+
+
+def _check_moe_nvfp4(T, cfg):
+    from test_gpu_moe_decode import _check_moe
+    _check_moe(T, cfg)
+
+
+def test_moe_nvfp4_full_size(T):
+    # M=8 rows, 128 NVFP4 experts, top-8, hidden 2048, expert intermediate 768
+    _check_moe_nvfp4(T, synth.moe_layer(code="nvfp4"))
+
+
+@pytest.mark.parametrize("M,E,top_k", [(1, 128, 8), (3, 16, 4), (8, 8, 8), (2, 5, 1)])
+def test_moe_nvfp4_small(T, M, E, top_k):
+    _check_moe_nvfp4(T, synth.moe_layer(seed=60 + M + E, M=M, E=E, top_k=top_k, hidden=256, inter=128, code="nvfp4"))
