@@ -326,6 +326,32 @@ Plan plan_qproj(int n_rb, int groups, int mats, int bits, int slots, int k_full,
     bool light = light_ok && g_tune[TF_TUNE_MODE] <= 0;
     if (g_tune[TF_TUNE_MODE] == 3 || g_tune[TF_TUNE_MODE] == 4)
         light = light_ok;
+    // ---- the stage kernel: one CTA per whole row block (all of K), the activations loaded
+    // straight into registers (with an RMSNorm: K <= 1024), no weight ring, no partial sums;
+    // small enough for two CTAs an SM (the next kernel's CTAs start beside the running ones)
+    if (light && slots == 1 && k_full <= 1024 && g_tune[TF_TUNE_MODE] <= 0) {
+        const size_t fixed = 256 + kMaxSlots * 8 + kMaxSlots * kMaxM * 4;  // barrier, flags, slots
+        Plan sp = pl;
+        sp.mode = 3;
+        sp.C = n_rb;
+        sp.aligned = 1;
+        sp.kmax = 1;
+        sp.nst = 1;
+        sp.cg = groups;
+        sp.nw = 8;
+        sp.KW = 8;
+        sp.R = 1;
+        sp.red_off = (int)align_up(fixed + (size_t)groups * kMaxM * 4, 128);
+        sp.xraw_off = (int)align_up(sp.red_off + (size_t)2 * 8 * 32 * 16, 128);
+        sp.x_rs = groups * kGroup * 2 + 16;
+        sp.stage_off = (int)align_up(sp.xraw_off + (size_t)rows * sp.x_rs, 128);
+        sp.smem = sp.stage_off + (size_t)mats * groups * tile;
+        sp.ws_counters = 0;
+        sp.ws_partials = 0;
+        sp.x_direct = 1;
+        if (sp.smem <= 110 * 1024)
+            return sp;
+    }
     if (light) {
         pl.nw = 8;
         pl.C = (int)std::max<int64_t>(items, 1);

@@ -100,7 +100,8 @@ struct QProjParams {
 };
 
 struct Plan {
-    int mode;  // 0: teams in lock-step (latency-bound calls), 1: warp workers, 2: streaming (one large matrix)
+    int mode;  // 0: teams in lock-step (latency-bound calls), 1: warp workers, 2: streaming (one large matrix),
+               // 3: one CTA per whole row block (the stage kernel)
     int KW, R, S, Gs, cg, nst, C, aligned, kmax, segmax, slots;
     int red_off, seg_off, round_off, last_off, xraw_off, x_rs, stage_off;
     int nw, pw, xsum1_off, xraw1_off, gamma_off;

@@ -1605,6 +1605,8 @@ __global__ void __launch_bounds__(kThreads, 1) qproj_warp_kernel(const __grid_co
     }
 }
 
+#include "tfq_stage.cuh"
+
 template <int BITS, bool DUAL, bool MOE>
 cudaError_t launch_qproj_warp(const Plan& plan, const QProjParams& p, cudaStream_t stream, bool pdl)
 {
@@ -1656,6 +1658,10 @@ cudaError_t launch_qproj_kw(const Plan& plan, const QProjParams& p, cudaStream_t
 template <int BITS, bool DUAL, bool MOE>
 cudaError_t launch_qproj_t(const Plan& plan, const QProjParams& p, cudaStream_t stream, bool pdl)
 {
+    if constexpr (!MOE) {
+        if (plan.mode == 3)
+            return launch_qstage<BITS, DUAL>(plan, p, stream, pdl);
+    }
     if (plan.mode == 1)
         return launch_qproj_warp<BITS, DUAL, MOE>(plan, p, stream, pdl);
     if (plan.nw == 8) {  // light teams: one item per CTA, several CTAs per SM

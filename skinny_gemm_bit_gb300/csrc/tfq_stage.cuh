@@ -1,0 +1,194 @@
+// The projection of one 16-row block by one CTA, for calls whose every row block fits a
+// CTA whole (one K split, at most a few hundred row blocks): the common case of a decoder
+// step, where each projection is one dependent stage and its time is latency, not bytes.
+//
+//   thread 0        issues the row block's weight copy (one bulk copy per matrix: a row
+//                   block's groups are contiguous in the packed layout) before the kernel
+//                   waits for the previous one (programmatic dependent launch): weights
+//                   never depend on the previous kernel, so they stream during its tail
+//   all NW warps    stage the activation rows straight from L2 into registers (normalised
+//                   when an RMSNorm is folded in; rotated when an input Hadamard transform
+//                   is), form the per-group sums, then warp w
+//                   multiplies groups w, w + NW, ... of the row block (two tiles per
+//                   iteration into independent accumulators), the warps' sums are added
+//                   in warp order through shared memory, and warp 0 applies the epilogue
+//                   (SwiGLU, residual: loaded right after the wait, so its L2 round trip
+//                   overlaps the staging and the tiles) and stores.
+//
+// The same tile math, activation staging and epilogue as the general schedules, without
+// their machinery (segment lists, rounds, a weight ring, split-K partial sums): one
+// bounded wait on one barrier, three CTA barriers. Shared memory: the row block's tiles,
+// the staged rows and the warps' sums.
+//
+// Included by tfq_qproj.cuh, inside namespace tfq, after the helpers it uses.
+#pragma once
+
+constexpr int kStageWarps = 8;
+constexpr int kBarStage = 1;  // named barrier of the compute warps
+
+template <int BITS, bool DUAL>
+__global__ void __launch_bounds__(kStageWarps * 32, 2) qstage_kernel(const __grid_constant__ QProjParams p)
+{
+    constexpr int MATS = DUAL ? 2 : 1;
+    constexpr int TILE = tile_bytes_for(BITS);
+    constexpr int NW = kStageWarps;
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint64_t* wbar = reinterpret_cast<uint64_t*>(smem + QSmem::kFullOff);
+    float* xsum = reinterpret_cast<float*>(smem + QSmem::kXsumOff);
+    float4* red4 = reinterpret_cast<float4*>(smem + p.red_off);  // [MATS][NW][32]
+    uint8_t* xraw = smem + p.xraw_off;
+    uint8_t* wt = smem + p.stage_off;  // [MATS][groups] tiles
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int gi = lane >> 2, tq = lane & 3;
+    const int rb = blockIdx.x;
+    const int G = p.groups;
+
+    if (threadIdx.x == 0) {
+        mbar_init(wbar, 1);
+        fence_mbar_init();
+        const uint64_t pol = policy_evict_first();
+        const uint32_t bytes = (uint32_t)(G * TILE);
+        mbar_arrive_expect_tx(wbar, bytes * MATS);
+        bulk_g2s(wt, p.w0 + (int64_t)rb * G * TILE, bytes, wbar, pol);
+        if constexpr (DUAL)
+            bulk_g2s(wt + (size_t)G * TILE, p.w1 + (int64_t)rb * G * TILE, bytes, wbar, pol);
+    }
+    pdl_launch_dependents();
+    pdl_wait();
+
+    // warp 0's residual values (it stores the outputs), raw bits: the L2 round trip runs
+    // while the rows are staged and the tiles multiplied
+    uint32_t res[4] = {0u, 0u, 0u, 0u};
+    if (warp == 0 && p.residual != nullptr) {
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+            const int n = rb * kRowsPerBlock + gi + 8 * (v >> 1);
+            const int m = 2 * tq + (v & 1);
+            if (n < p.N && m < p.M)
+                res[v] = (uint32_t)__ldcg(p.residual + (int64_t)m * p.ldr + n);
+        }
+    }
+
+    // ---- the activation rows (and their group sums), straight from L2; ends with a barrier
+    // that also publishes the barrier initialisation above
+    x_direct_raw<4>(p.x, p.ldx, p.K, p.gamma, p.eps, p.x_rs, xraw, p.M, xsum, nullptr, warp, lane, NW, kBarStage);
+    if (p.rht != nullptr)  // the input Hadamard transform, a pass over the staged rows
+        x_rht(xraw, p.x_rs, xsum, p.M, 0, G, p.rht, warp, lane, NW, kBarStage);
+
+    // ---- the row block's tiles
+    const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(wbar, 0u, p.limit_ns));
+    float acc0[4] = {0.f, 0.f, 0.f, 0.f}, acc1[4] = {0.f, 0.f, 0.f, 0.f};
+    float bcc0[4] = {0.f, 0.f, 0.f, 0.f}, bcc1[4] = {0.f, 0.f, 0.f, 0.f};  // second chain
+    if (ok) {
+        const uint8_t* t0 = wt;
+        const uint8_t* t1 = wt + (size_t)G * TILE;
+        int g = warp;
+        for (; g + NW < G; g += 2 * NW) {
+            uint4 xa, xb, ya, yb;
+            x_frag(xraw, p.x_rs, gi, tq, g, p.M, xa, xb);
+            x_frag(xraw, p.x_rs, gi, tq, g + NW, p.M, ya, yb);
+            const float2 xs = *reinterpret_cast<const float2*>(xsum + g * kMaxM + 2 * tq);
+            const float2 ys = *reinterpret_cast<const float2*>(xsum + (g + NW) * kMaxM + 2 * tq);
+            tile_mac<BITS>(t0 + g * TILE, lane, xa, xb, xs, acc0);
+            tile_mac<BITS>(t0 + (g + NW) * TILE, lane, ya, yb, ys, bcc0);
+            if constexpr (DUAL) {
+                tile_mac<BITS>(t1 + g * TILE, lane, xa, xb, xs, acc1);
+                tile_mac<BITS>(t1 + (g + NW) * TILE, lane, ya, yb, ys, bcc1);
+            }
+        }
+        if (g < G) {
+            uint4 xa, xb;
+            x_frag(xraw, p.x_rs, gi, tq, g, p.M, xa, xb);
+            const float2 xs = *reinterpret_cast<const float2*>(xsum + g * kMaxM + 2 * tq);
+            tile_mac<BITS>(t0 + g * TILE, lane, xa, xb, xs, acc0);
+            if constexpr (DUAL)
+                tile_mac<BITS>(t1 + g * TILE, lane, xa, xb, xs, acc1);
+        }
+    } else if (lane == 0) {
+        atomicCAS(p.status, 0, TF_E_TIMEOUT);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        acc0[i] += bcc0[i];
+        acc1[i] += bcc1[i];
+    }
+    // ---- the warps' sums, in warp order, by warp 0; then the epilogue
+    red4[warp * 32 + lane] = make_float4(acc0[0], acc0[1], acc0[2], acc0[3]);
+    if constexpr (DUAL)
+        red4[(NW + warp) * 32 + lane] = make_float4(acc1[0], acc1[1], acc1[2], acc1[3]);
+    named_bar_sync(kBarStage, NW * 32);
+    if (warp == 0) {
+#pragma unroll
+        for (int q = 1; q < NW; ++q) {
+            const float4 o0 = red4[q * 32 + lane];
+            acc0[0] += o0.x;
+            acc0[1] += o0.y;
+            acc0[2] += o0.z;
+            acc0[3] += o0.w;
+            if constexpr (DUAL) {
+                const float4 o1 = red4[(NW + q) * 32 + lane];
+                acc1[0] += o1.x;
+                acc1[1] += o1.y;
+                acc1[2] += o1.z;
+                acc1[3] += o1.w;
+            }
+        }
+        if constexpr (BITS == kNvfp4) {  // the matrices' global scales
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                acc0[i] *= p.wscale0;
+                if constexpr (DUAL)
+                    acc1[i] *= p.wscale1;
+            }
+        }
+        if (ok) {
+            // rows rb*16 + gi (+ 8) of the block, activation rows 2 tq (+ 1): SwiGLU for
+            // gate/up, residual add, store
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+                const int n = rb * kRowsPerBlock + gi + 8 * (v >> 1);
+                const int m = 2 * tq + (v & 1);
+                if (n >= p.N || m >= p.M)
+                    continue;
+                float val = acc0[v];
+                if constexpr (DUAL)
+                    val = val / (1.f + expf(-val)) * acc1[v];
+                if (p.residual != nullptr)
+                    val += __uint_as_float(res[v] << 16);
+                const int64_t idx = (int64_t)m * p.ldy + n;
+                if (p.y_f32)
+                    static_cast<float*>(p.y)[idx] = val;
+                else
+                    static_cast<__nv_bfloat16*>(p.y)[idx] = __float2bfloat16_rn(val);
+            }
+        }
+    }
+    // a wait that gave up: no copy may still be in flight when the CTA leaves
+    if (!ok && threadIdx.x == 0)
+        mbar_wait_bounded(wbar, 0u, p.limit_ns);
+}
+
+template <int BITS, bool DUAL>
+cudaError_t launch_qstage(const Plan& plan, const QProjParams& p, cudaStream_t stream, bool pdl)
+{
+    auto kern = qstage_kernel<BITS, DUAL>;
+    static bool configured = false;
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+        if (e != cudaSuccess)
+            return e;
+        configured = true;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)plan.C, 1, 1);
+    cfg.blockDim = dim3(kStageWarps * 32, 1, 1);
+    cfg.dynamicSmemBytes = plan.smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, p);
+}
