@@ -338,11 +338,11 @@ Plan plan_qproj(int n_rb, int groups, int mats, int bits, int slots, int k_full,
         sp.kmax = 1;
         sp.nst = 1;
         sp.cg = groups;
-        sp.nw = 8;
-        sp.KW = 8;
+        sp.nw = n_rb <= sms ? 16 : 8;  // 16 warps when one CTA an SM holds every row block
+        sp.KW = sp.nw;
         sp.R = 1;
         sp.red_off = (int)align_up(fixed + (size_t)groups * kMaxM * 4, 128);
-        sp.xraw_off = (int)align_up(sp.red_off + (size_t)2 * 8 * 32 * 16, 128);
+        sp.xraw_off = (int)align_up(sp.red_off + (size_t)2 * sp.nw * 32 * 16, 128);
         sp.x_rs = groups * kGroup * 2 + 16;
         sp.stage_off = (int)align_up(sp.xraw_off + (size_t)rows * sp.x_rs, 128);
         sp.smem = sp.stage_off + (size_t)mats * groups * tile;

@@ -23,15 +23,14 @@
 // Included by tfq_qproj.cuh, inside namespace tfq, after the helpers it uses.
 #pragma once
 
-constexpr int kStageWarps = 8;
 constexpr int kBarStage = 1;  // named barrier of the compute warps
 
-template <int BITS, bool DUAL>
-__global__ void __launch_bounds__(kStageWarps * 32, 2) qstage_kernel(const __grid_constant__ QProjParams p)
+// NW warps: 8 (two CTAs an SM) or 16 (calls with at most one row block an SM)
+template <int BITS, bool DUAL, int NW>
+__global__ void __launch_bounds__(NW * 32, NW == 8 ? 2 : 1) qstage_kernel(const __grid_constant__ QProjParams p)
 {
     constexpr int MATS = DUAL ? 2 : 1;
     constexpr int TILE = tile_bytes_for(BITS);
-    constexpr int NW = kStageWarps;
     extern __shared__ __align__(128) uint8_t smem[];
     uint64_t* wbar = reinterpret_cast<uint64_t*>(smem + QSmem::kFullOff);
     float* xsum = reinterpret_cast<float*>(smem + QSmem::kXsumOff);
@@ -169,10 +168,10 @@ __global__ void __launch_bounds__(kStageWarps * 32, 2) qstage_kernel(const __gri
         mbar_wait_bounded(wbar, 0u, p.limit_ns);
 }
 
-template <int BITS, bool DUAL>
-cudaError_t launch_qstage(const Plan& plan, const QProjParams& p, cudaStream_t stream, bool pdl)
+template <int BITS, bool DUAL, int NW>
+cudaError_t launch_qstage_w(const Plan& plan, const QProjParams& p, cudaStream_t stream, bool pdl)
 {
-    auto kern = qstage_kernel<BITS, DUAL>;
+    auto kern = qstage_kernel<BITS, DUAL, NW>;
     static bool configured = false;
     if (!configured) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
@@ -182,7 +181,7 @@ cudaError_t launch_qstage(const Plan& plan, const QProjParams& p, cudaStream_t s
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)plan.C, 1, 1);
-    cfg.blockDim = dim3(kStageWarps * 32, 1, 1);
+    cfg.blockDim = dim3(NW * 32, 1, 1);
     cfg.dynamicSmemBytes = plan.smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -191,4 +190,11 @@ cudaError_t launch_qstage(const Plan& plan, const QProjParams& p, cudaStream_t s
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
+template <int BITS, bool DUAL>
+cudaError_t launch_qstage(const Plan& plan, const QProjParams& p, cudaStream_t stream, bool pdl)
+{
+    return plan.nw == 16 ? launch_qstage_w<BITS, DUAL, 16>(plan, p, stream, pdl)
+                         : launch_qstage_w<BITS, DUAL, 8>(plan, p, stream, pdl);
 }
