@@ -75,9 +75,9 @@ extern "C" {
 /* run flags */
 #define TF_RUN_PDL 1u  /* the caller asserts that the kernel enqueued just before
                           this call on `stream` does not write this call's
-                          weights: the first kernel may then be launched with
-                          programmatic dependent launch and stream its weights
-                          while that kernel finishes. */
+                          weights or RMSNorm gamma: the first kernel may then be
+                          launched with programmatic dependent launch and read
+                          them while that kernel finishes. */
 
 #define TF_QWEIGHT_MAGIC 0x31515446u /* "TFQ1" */
 #define TF_PACK_VERSION 2u

@@ -128,6 +128,18 @@ __device__ __forceinline__ uint64_t policy_evict_first()
     return p;
 }
 
+// 16 bytes of read-only global memory through the non-coherent path, issued where it
+// stands: the asm is volatile, so the load keeps its place among the other volatile asm
+// (a grid-dependency wait, a barrier) instead of sinking to its first use.
+__device__ __forceinline__ uint4 ld_nc_v4_here(const void* ptr)
+{
+    uint4 r;
+    asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(ptr));
+    return r;
+}
+
 // ---------------------------------------------------------------- PDL
 
 __device__ __forceinline__ void pdl_wait()

@@ -25,6 +25,65 @@
 
 constexpr int kBarStage = 1;  // named barrier of the compute warps
 
+// gamma's chunks j 32 + lane (j < 4) for the RMSNorm staging below. gamma is a weight:
+// it does not depend on the previous kernel, so this runs before the grid-dependency
+// wait and its latency hides behind it.
+__device__ __forceinline__ void stage_gamma_prefetch(const uint16_t* gamma, int K, int lane, uint4 (&gv)[4])
+{
+    const uint4* g4 = reinterpret_cast<const uint4*>(gamma);
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        gv[j] = j * 32 + lane < K / 8 ? ld_nc_v4_here(g4 + j * 32 + lane) : make_uint4(0u, 0u, 0u, 0u);
+}
+
+// The rows x[m][0, K) (m < M, K <= 1024), normalised with the prefetched gamma and
+// rounded to bf16 into buf (row stride x_rs), with the per-group sums into xs[g * 8 + m]
+// (zero for rows >= M): one warp a row, four chunks a lane, the row's sum of squares a
+// warp reduction in an order that does not depend on M (the same arithmetic as the
+// other schedules' staging). Ends with a barrier of the NW warps.
+template <int NW>
+__device__ __forceinline__ void stage_rows_norm(const uint16_t* x, int64_t ldx, int K, const uint4 (&gv)[4], float eps,
+                                                int x_rs, uint8_t* buf, int M, float* xs, int warp, int lane)
+{
+    const int nch = K / 8;
+    for (int i = warp * 32 + lane; i < (K / kGroup) * kMaxM; i += NW * 32)
+        if ((i & 7) >= M)
+            xs[i] = 0.f;
+    for (int m = warp; m < M; m += NW) {
+        const uint4* x4 = reinterpret_cast<const uint4*>(x + (int64_t)m * ldx);
+        uint4 v[4];
+        float sq[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            v[j] = j * 32 + lane < nch ? __ldcg(x4 + j * 32 + lane) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint32_t vv[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float a = bf16lo_f32(vv[q]), b = bf16hi_f32(vv[q]);
+                sq[q] = fmaf(b, b, fmaf(a, a, sq[q]));
+            }
+        }
+        const float inv = rsqrtf(warp_sum((sq[0] + sq[1]) + (sq[2] + sq[3])) / (float)K + eps);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            if (j * 32 >= nch)  // warp-uniform
+                break;
+            const int c = j * 32 + lane;
+            const uint32_t xv[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+            const uint32_t gg[4] = {gv[j].x, gv[j].y, gv[j].z, gv[j].w};
+            uint32_t vv[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                vv[q] = f32x2_to_bf16x2(bf16lo_f32(xv[q]) * inv * bf16lo_f32(gg[q]),
+                                        bf16hi_f32(xv[q]) * inv * bf16hi_f32(gg[q]));
+            x_put_chunk(buf, x_rs, xs, m, c, c < nch, vv);
+        }
+    }
+    named_bar_sync(kBarStage, NW * 32);
+}
+
 // NW warps: 8 (two CTAs an SM) or 16 (calls with at most one row block an SM)
 template <int BITS, bool DUAL, int NW>
 __global__ void __launch_bounds__(NW * 32, NW == 8 ? 2 : 1) qstage_kernel(const __grid_constant__ QProjParams p)
@@ -54,6 +113,10 @@ __global__ void __launch_bounds__(NW * 32, NW == 8 ? 2 : 1) qstage_kernel(const 
             bulk_g2s(wt + (size_t)G * TILE, p.w1 + (int64_t)rb * G * TILE, bytes, wbar, pol);
     }
     pdl_launch_dependents();
+    // gamma (a weight) before the wait
+    uint4 gpre[4];
+    if (p.gamma != nullptr)
+        stage_gamma_prefetch(p.gamma, p.K, lane, gpre);
     pdl_wait();
 
     // warp 0's residual values (it stores the outputs), raw bits: the L2 round trip runs
@@ -71,7 +134,10 @@ __global__ void __launch_bounds__(NW * 32, NW == 8 ? 2 : 1) qstage_kernel(const 
 
     // ---- the activation rows (and their group sums), straight from L2; ends with a barrier
     // that also publishes the barrier initialisation above
-    x_direct_raw<4>(p.x, p.ldx, p.K, p.gamma, p.eps, p.x_rs, xraw, p.M, xsum, nullptr, warp, lane, NW, kBarStage);
+    if (p.gamma != nullptr)
+        stage_rows_norm<NW>(p.x, p.ldx, p.K, gpre, p.eps, p.x_rs, xraw, p.M, xsum, warp, lane);
+    else
+        x_direct_raw<4>(p.x, p.ldx, p.K, nullptr, p.eps, p.x_rs, xraw, p.M, xsum, nullptr, warp, lane, NW, kBarStage);
     if (p.rht != nullptr)  // the input Hadamard transform, a pass over the staged rows
         x_rht(xraw, p.x_rs, xsum, p.M, 0, G, p.rht, warp, lane, NW, kBarStage);
 
