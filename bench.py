@@ -438,7 +438,7 @@ class Step(Workload):
 
     name = "step"
     kernel_key = "step_b4_l28_d1024"
-    kernel = "qproj kernels, 4 per layer + readout, chained with programmatic dependent launch"
+    kernel = "stage kernels (one CTA per 16-row block), 4 per layer, + the readout's warp-worker kernel, chained with programmatic dependent launch"
     launches_per_call = 4 * 28 + 1
 
     def __init__(self, T, torch, l2_bytes):
