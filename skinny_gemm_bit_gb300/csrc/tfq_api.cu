@@ -991,6 +991,7 @@ int tf_qmoe_run(const tf_qweight* gate, const tf_qweight* up, const tf_qweight* 
     q.y_f32 = 1;
     q.y_slot_stride = (int64_t)kMaxM * H;
     q.meta = meta;
+    q.meta_ready = 1;  // written by the routing kernel, which the gate/up launch waited for
     q.gather = 0;
     fill_common(q, L.pdn, ws, wsb + L.dn);
     q.wscales0 = nvfp4_scales_of(down);

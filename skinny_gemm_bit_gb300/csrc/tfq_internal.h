@@ -76,6 +76,8 @@ struct QProjParams {
     int y_f32;
     int64_t y_slot_stride;   // MoE: y offset of a problem (elements)
     const MoeMeta* meta;     // MoE routing table or nullptr
+    int meta_ready;          // MoE: the table was complete before this launch could start (it is
+                             // read before the wait for the previous kernel, which wrote x)
     int P;                   // problems (1 unless MoE, whose count comes from meta)
     int C;                   // CTAs in the persistent grid
     int aligned;             // 1: CTAs take whole row blocks; 0: stream-K shares of the units

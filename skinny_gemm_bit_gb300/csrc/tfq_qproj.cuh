@@ -817,12 +817,18 @@ __global__ void __launch_bounds__((NWT + 1) * 32, NWT == 8 ? 2 : 1) qproj_kernel
         fence_mbar_init();
     }
     __syncthreads();
-    pdl_launch_dependents();
+    if constexpr (!MOE)
+        pdl_launch_dependents();
 
     int P = p.P;
     if constexpr (MOE) {
-        // the routing table comes from the previous kernel
-        pdl_wait();
+        // the routing table comes from the previous kernel, or from an earlier one that had
+        // completed before this launch could start (meta_ready: the gate/up launch waited for
+        // it before it let its dependents start, so the down launch reads it at once and
+        // streams its experts' weights while gate/up finishes)
+        if (!p.meta_ready)
+            pdl_wait();
+        pdl_launch_dependents();
         P = __ldcg(&p.meta->n_active);
         for (int i = threadIdx.x; i < P; i += blockDim.x) {
             slot_ec[i] = make_int2(__ldcg(&p.meta->slot[i].expert), __ldcg(&p.meta->slot[i].count));
@@ -957,7 +963,7 @@ __global__ void __launch_bounds__((NWT + 1) * 32, NWT == 8 ? 2 : 1) qproj_kernel
     const int cw = warp;
     const int r_me = cw / KW, kp = cw % KW;
     const int gi = lane >> 2, tq = lane & 3;
-    if constexpr (!MOE)
+    if (!MOE || p.meta_ready)  // the activations come from the previous kernel
         pdl_wait();
     const bool norm = p.gamma != nullptr;
     bool alive = true;
@@ -1269,11 +1275,16 @@ __global__ void __launch_bounds__(kThreads, 1) qproj_warp_kernel(const __grid_co
         fence_mbar_init();
     }
     __syncthreads();
-    pdl_launch_dependents();
+    if constexpr (!MOE)
+        pdl_launch_dependents();
 
     int P = p.P;
     if constexpr (MOE) {
-        pdl_wait();
+        // as in the team kernel: wait for the routing table unless it was complete before
+        // this launch could start, and let dependents start only once it is known complete
+        if (!p.meta_ready)
+            pdl_wait();
+        pdl_launch_dependents();
         P = __ldcg(&p.meta->n_active);
         for (int i = threadIdx.x; i < P; i += blockDim.x) {
             slot_ec[i] = make_int2(__ldcg(&p.meta->slot[i].expert), __ldcg(&p.meta->slot[i].count));
@@ -1383,7 +1394,7 @@ __global__ void __launch_bounds__(kThreads, 1) qproj_warp_kernel(const __grid_co
     // ------------------------------------------------------------ consumers
     const int cw = warp;
     const int gi = lane >> 2, tq = lane & 3;
-    if constexpr (!MOE)
+    if (!MOE || p.meta_ready)  // the activations come from the previous kernel
         pdl_wait();
 
     // stage the activations of the CTA's runs (once)
