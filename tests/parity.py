@@ -19,6 +19,10 @@ import oracle
 EPS = 1e-2
 ATOL = 1e-3
 BF16_REL = 2.0 ** -8
+# tight bounds for fp32 outputs (derivation and measurements in test_gpu_tight_bounds.py)
+PLAIN_TIGHT = 2.0 ** -14
+NORM_TIGHT = 2.0 ** -9 + 2.0 ** -14
+TINY = 1e-7
 
 
 def dev_bf16(u16) -> torch.Tensor:
