@@ -101,3 +101,65 @@ def test_gateup_tight(T, M):
     dg, du = NORM * ref["g_abs"], NORM * ref["u_abs"]
     tol = 1.1 * dg * (np.abs(ref["u"]) + du) + np.abs(silu(ref["g"])) * du + 2.0 ** -8 * np.abs(ref["h"]) + TINY
     assert_close(host_f64(h), ref["h"], tol, "gate/up")
+
+
+def _pack_decoder(T, cfg):
+    layers = [{"qkv": pack(T, L["qkv"]), "o": pack(T, L["o"]), "gate": pack(T, L["gate"]), "up": pack(T, L["up"]),
+               "down": pack(T, L["down"]), "attn_norm": dev_bf16(L["attn_norm"]), "mlp_norm": dev_bf16(L["mlp_norm"])}
+              for L in cfg["layers"]]
+    d = cfg["dims"]
+    return T.Decoder(layers, dev_bf16(cfg["final_norm"]), pack(T, cfg["readout"]), d["d_model"], d["d_ff"],
+                     d["q_dim"], d["kv_dim"], cfg["eps"])
+
+
+# The decoder step stage by stage: each stage's reference is the oracle applied to the GPU's
+# own input to that stage (the bf16 values the previous stage stored), so every stage is held
+# to its own tight bound, plus 2^-8 |y| for the bf16 store (after the residual add where
+# there is one), instead of a bound that grows through the layers.
+@pytest.mark.parametrize("full", [False, True])
+@pytest.mark.parametrize("M", [1, 8])
+def test_decoder_stages_tight(T, M, full):
+    if full:  # 28 layers, d_model 1024, d_ff 3072, 16 q / 8 kv heads of 128; 4096 rows of the readout
+        cfg = synth.decoder(M=M)
+        rows = np.arange(0, cfg["dims"]["vocab"], cfg["dims"]["vocab"] // 4096)[:4096]
+    else:
+        cfg = synth.decoder(seed=50 + M, n_layers=3, d_model=256, d_ff=384, n_q_heads=4, n_kv_heads=2,
+                            head_dim=64, vocab=1000, M=M)
+        rows = None
+    d = cfg["dims"]
+    D, F, Q = d["d_model"], d["d_ff"], d["q_dim"]
+    QKV = Q + 2 * d["kv_dim"]
+    eps = cfg["eps"]
+    dec = _pack_decoder(T, cfg)
+    dbg = torch.zeros(T.tf_decode_step_debug_elems(dec, M), dtype=torch.bfloat16, device="cuda")
+    logits = host_f64(T.tf_decode_step_run(dec, dev_bf16(cfg["x"]), debug=dbg))
+    dbg_h = host_f64(dbg)
+    per = M * (QKV + D + F + D)
+    R = 2.0 ** -8
+    h = oracle.bf16_to_f64(cfg["x"])
+    for l, L in enumerate(cfg["layers"]):
+        blk = dbg_h[l * per:(l + 1) * per]
+        qkv = blk[:M * QKV].reshape(M, QKV)
+        h1 = blk[M * QKV:M * (QKV + D)].reshape(M, D)
+        a = blk[M * (QKV + D):M * (QKV + D + F)].reshape(M, F)
+        h2 = blk[M * (QKV + D + F):].reshape(M, D)
+        ref, ad = oracle.qlinear(oracle.rmsnorm(h, oracle.bf16_to_f64(L["attn_norm"]), eps), L["qkv"])
+        assert_close(qkv, ref, NORM * ad + R * np.abs(ref) + TINY, f"layer {l} qkv")
+        o, ad = oracle.qlinear(qkv[:, :Q], L["o"])
+        ref = h + o
+        assert_close(h1, ref, PLAIN * ad + R * np.abs(ref) + TINY, f"layer {l} h1")
+        gu = oracle.gateup(h1, L["gate"], L["up"], oracle.bf16_to_f64(L["mlp_norm"]), eps)
+        dg, du = NORM * gu["g_abs"], NORM * gu["u_abs"]
+        tol = 1.1 * dg * (np.abs(gu["u"]) + du) + np.abs(silu(gu["g"])) * du + R * np.abs(gu["h"]) + TINY
+        assert_close(a, gu["h"], tol, f"layer {l} swiglu")
+        dn, ad = oracle.qlinear(a, L["down"])
+        ref = h1 + dn
+        assert_close(h2, ref, PLAIN * ad + R * np.abs(ref) + TINY, f"layer {l} h2")
+        h = h2
+    ro = cfg["readout"]
+    if rows is not None:
+        ro = {"wq": ro["wq"][rows], "scales": ro["scales"][rows], "biases": ro["biases"][rows], "N": len(rows),
+              "K": ro["K"], "bits": ro["bits"]}
+        logits = logits[:, rows]
+    ref, ad = oracle.qlinear(oracle.rmsnorm(h, oracle.bf16_to_f64(cfg["final_norm"]), eps), ro)
+    assert_close(logits, ref, NORM * ad + R * np.abs(ref) + TINY, "logits")
