@@ -47,10 +47,10 @@ def tol_linear(absdot):
     return EPS * absdot + ATOL
 
 
-def tol_swiglu(g, u, g_abs, u_abs):
-    dg, du = EPS * g_abs, EPS * u_abs
+def tol_swiglu(g, u, g_abs, u_abs, eps=EPS, atol=ATOL):
+    dg, du = eps * g_abs, eps * u_abs
     h = silu(g) * u
-    return 1.1 * dg * (np.abs(u) + du) + np.abs(silu(g)) * du + BF16_REL * np.abs(h) + ATOL
+    return 1.1 * dg * (np.abs(u) + du) + np.abs(silu(g)) * du + BF16_REL * np.abs(h) + atol
 
 
 def assert_close(y, ref, tol, what=""):
@@ -71,16 +71,17 @@ def pack(T, w: dict):
     return T.tf_qlinear_pack(w["wq"], w["scales"], w["biases"], w["bits"])
 
 
-def moe_tolerance(ref: dict, down: dict, w_gpu: np.ndarray):
-    """Bound on |y_gpu - y_ref| for the MoE layer (see module docstring)."""
+def moe_tolerance(ref: dict, down: dict, w_gpu: np.ndarray, eps=EPS, atol=ATOL):
+    """Bound on |y_gpu - y_ref| for the MoE layer (see module docstring); eps and atol are
+    the per-projection bound's relative and absolute terms."""
     M, k = ref["idx"].shape
     H = ref["y"].shape[1]
     tol = np.zeros((M, H))
     for m in range(M):
         for j in range(k):
             s = ref["slots"][m][j]
-            tol_h = tol_swiglu(s["g"], s["u"], s["g_abs"], s["u_abs"])
+            tol_h = tol_swiglu(s["g"], s["u"], s["g_abs"], s["u_abs"], eps, atol)
             _, prop = oracle.qlinear(tol_h[None, :], oracle.expert(down, s["e"]))
             dw = abs(float(w_gpu[m, j]) - ref["w"][m, j])
-            tol[m] += dw * np.abs(s["o"]) + ref["w"][m, j] * (EPS * s["o_abs"] + prop[0] + ATOL)
-    return tol + BF16_REL * np.abs(ref["y"]) + ATOL
+            tol[m] += dw * np.abs(s["o"]) + ref["w"][m, j] * (eps * s["o_abs"] + prop[0] + atol)
+    return tol + BF16_REL * np.abs(ref["y"]) + atol

@@ -22,7 +22,8 @@ import pytest
 import torch
 
 import oracle
-from parity import NORM_TIGHT as NORM, PLAIN_TIGHT as PLAIN, TINY, assert_close, dev_bf16, host_f64, pack, silu
+from parity import (NORM_TIGHT as NORM, PLAIN_TIGHT as PLAIN, TINY, assert_close, dev_bf16, dev_f32, host_f64,
+                    moe_tolerance, pack, silu)
 from skinny_gemm_bit_gb300 import synth
 
 pytestmark = pytest.mark.gpu
@@ -163,3 +164,17 @@ def test_decoder_stages_tight(T, M, full):
         logits = logits[:, rows]
     ref, ad = oracle.qlinear(oracle.rmsnorm(h, oracle.bf16_to_f64(cfg["final_norm"]), eps), ro)
     assert_close(logits, ref, NORM * ad + R * np.abs(ref) + TINY, "logits")
+
+
+# The MoE layer at full size (M=8, 128 experts, top-8, hidden 2048, intermediate 768): the
+# task's propagation through gate/up, SwiGLU (bf16 store), down and the weighted sum, with
+# the plain tight bound in place of 1e-2 for every projection (the rows are not normalised).
+@pytest.mark.parametrize("code,bits", [("mlx", 4), ("mlx", 8), ("nvfp4", 4)])
+def test_moe_tight(T, code, bits):
+    cfg = synth.moe_layer(bits=bits, code=code)
+    y, idx, w = T.tf_qmoe_run(pack(T, cfg["gate"]), pack(T, cfg["up"]), pack(T, cfg["down"]), dev_f32(cfg["logits"]),
+                              dev_bf16(cfg["x"]), cfg["top_k"])
+    ref = oracle.moe(oracle.bf16_to_f64(cfg["x"]), cfg["logits"], cfg["gate"], cfg["up"], cfg["down"], cfg["top_k"])
+    assert np.array_equal(idx.cpu().numpy(), ref["idx"])
+    w = w.cpu().numpy().astype(np.float64)
+    assert_close(host_f64(y), ref["y"], moe_tolerance(ref, cfg["down"], w, PLAIN, TINY), f"moe {code} {bits}")
