@@ -311,12 +311,37 @@ def _proj_config(kind):
             "readout_nvfp4": lambda: synth.nvfp4_projection(seed=9, M=8, K=1024, N=151936)}[kind]()
 
 
+# Workload descriptions, shared by both arms so that their lines name the same config
+STEP_DESC = ("per-token weight stream of a 28-layer dense decoder, 4-bit group-64: norm+QKV, O, "
+             "norm+gate/up+SwiGLU, down per layer, norm+tied readout 151936x1024; one M=1 and one M=8 step")
+
+
+def gateup_desc(K, N):
+    return (f"fused RMSNorm + gate/up SwiGLU projection, 4-bit group-64, K={K}, N=2x{N}; "
+            f"one M=1 and one M=8 call per step")
+
+
+def proj_desc(kind, K, N, step_ms):
+    ms = " and ".join(f"M={M}" for M in step_ms)
+    what = {"wide": "wide verify 4-bit group-64", "wide_rht": "input Hadamard transform + wide verify 4-bit group-64",
+            "readout": "RMSNorm + tied readout 4-bit group-64", "proj": "single 4-bit group-64",
+            "wide_nvfp4": "wide verify NVFP4 (E2M1, E4M3 scale per 16)",
+            "readout_nvfp4": "RMSNorm + tied readout NVFP4 (E2M1, E4M3 scale per 16)"}[kind]
+    return f"{what} projection, K={K}, N={N}; one {ms} call per step"
+
+
+def moe_desc(nvfp4, bits, distinct):
+    codes = "NVFP4 (E2M1, an E4M3 scale per 16, an fp32 scale per expert)" if nvfp4 else f"{bits}-bit group-64"
+    return (f"MoE expert projection, M=8, 128 experts, top-8, hidden 2048, intermediate 768, {codes} "
+            f"gate/up/down ({distinct} distinct experts read); one call per step")
+
+
 class GateUp(Workload):
     """Fused RMSNorm + gate/up SwiGLU, K=1024, N=2x3072; one M=1 and one M=8 call per step."""
 
     name = "gateup"
     kernel_key = "qproj_b4_dual_k1024_n3072"
-    kernel = "qproj_kernel<4, dual> (light team schedule)"
+    kernel = "qstage_kernel<4, dual> (stage kernel, one CTA per row block)"
 
     def __init__(self, T, torch, l2_bytes, K=1024, N=3072):
         super().__init__(T, torch)
@@ -334,8 +359,7 @@ class GateUp(Workload):
         self._io(cfg["x"], N)
         self.ws = T.workspace(T.tf_qmlp_gateup_workspace_bytes(g, u, 8))
         self.sample_x = cfg["x"]
-        self.desc = (f"fused RMSNorm + gate/up SwiGLU projection, 4-bit group-64, K={K}, N=2x{N}; "
-                     f"one M=1 and one M=8 call per step")
+        self.desc = gateup_desc(K, N)
 
     def call(self, i, M, flags, x, out):
         g, u = self.copies[i]
@@ -403,7 +427,7 @@ class Proj(Workload):
             self.gamma = _dev_bf16(torch, synth.gamma(np.random.default_rng(5), 1024))
         else:
             self.name, self.step_ms = "proj", (1,)
-            self.kernel_key, self.kernel = "qproj_b4_k1024_n3072", "qproj_kernel<4> (light team schedule)"
+            self.kernel_key, self.kernel = "qproj_b4_k1024_n3072", "qstage_kernel<4> (stage kernel, one CTA per row block)"
         w0 = _pack(T, cfg["w"])
         self.w = cfg["w"]
         self.K, self.N, self.bits = w0.K, w0.N, 4
@@ -415,12 +439,7 @@ class Proj(Workload):
         self._io(x8, self.N)
         self.ws = T.workspace(T.tf_qlinear_workspace_bytes(w0, 8))
         self.sample_x = x8
-        ms = " and ".join(f"M={M}" for M in self.step_ms)
-        what = {"wide": "wide verify 4-bit group-64", "wide_rht": "input Hadamard transform + wide verify 4-bit group-64",
-                "readout": "RMSNorm + tied readout 4-bit group-64", "proj": "single 4-bit group-64",
-                "wide_nvfp4": "wide verify NVFP4 (E2M1, E4M3 scale per 16)",
-                "readout_nvfp4": "RMSNorm + tied readout NVFP4 (E2M1, E4M3 scale per 16)"}[kind]
-        self.desc = f"{what} projection, K={self.K}, N={self.N}; one {ms} call per step"
+        self.desc = proj_desc(kind, self.K, self.N, self.step_ms)
 
     def call(self, i, M, flags, x, out):
         if self.signs is not None:
@@ -460,8 +479,7 @@ class Step(Workload):
         self._io(cfg["x"], d["vocab"])
         self.ws = T.workspace(T.tf_decode_step_workspace_bytes(self.dec, 8))
         self.sample_x = cfg["x"]
-        self.desc = ("per-token weight stream of a 28-layer dense decoder, 4-bit group-64: norm+QKV, O, "
-                     "norm+gate/up+SwiGLU, down per layer, norm+tied readout 151936x1024; one M=1 and one M=8 step")
+        self.desc = STEP_DESC
 
     def call(self, i, M, flags, x, out):
         self.T.tf_decode_step_run(self.dec, x, out=out, ws=self.ws, flags=flags)
@@ -502,10 +520,7 @@ class MoE(Workload):
         distinct = len(np.unique(idx.cpu().numpy()))
         self.per_call = distinct * (g.weight_bytes() + u.weight_bytes() + dn.weight_bytes()) // 128
         self.sample_x = cfg["x"]
-        codes = ("NVFP4 (E2M1, an E4M3 scale per 16, an fp32 scale per expert)" if nvfp4
-                 else f"{bits}-bit group-64")
-        self.desc = (f"MoE expert projection, M=8, 128 experts, top-8, hidden 2048, intermediate 768, {codes} "
-                     f"gate/up/down ({distinct} distinct experts read); one call per step")
+        self.desc = moe_desc(nvfp4, bits, distinct)
 
     def call(self, i, M, flags, x, out):
         g, u, dn = self.copies[i]
@@ -830,8 +845,7 @@ class _HostOnly:
             self.impl = GateUp.__new__(GateUp)
             cfg = synth.fused_gateup(seed=1, M=8)
             self.impl.cfg, self.impl.K, self.impl.N = cfg, 1024, 3072
-            self.desc = ("fused RMSNorm + gate/up SwiGLU projection, 4-bit group-64, K=1024, N=2x3072; "
-                         "one M=1 and one M=8 call per step")
+            self.desc = gateup_desc(1024, 3072)
             self.K, self.N, self.ms, self.bits = 1024, 3072, [1, 8], 4
         else:
             self.impl = Workload.__new__(Workload)
@@ -844,14 +858,13 @@ class _HostOnly:
                 if name == "wide_rht":
                     self.impl.host_signs = synth.rht_signs(np.random.default_rng(2), 12800)
                 self.K, self.N, self.bits = w["K"], w["N"], 4
-                code = "NVFP4" if w.get("code") == "nvfp4" else "4-bit group-64"
-                self.desc = f"{name} {code} projection, K={w['K']}, N={w['N']}"
+                self.desc = proj_desc(name, w["K"], w["N"], self.impl.step_ms)
             elif name in ("step", "verify"):
                 cfg = synth.decoder(M=8, n_layers=1)  # layer 0 of the same seeded model
                 w, x8, rows, what = cfg["layers"][0]["qkv"], cfg["x"], 256, "layer 0's QKV matrix"
                 self.impl.step_ms = (1, 8)
                 self.K, self.N, self.bits = 1024, 151936, 4
-                self.desc = "per-token weight stream of a 28-layer dense decoder (sampled: layer 0 QKV rows)"
+                self.desc = STEP_DESC
             else:
                 import oracle
                 nvfp4 = name == "moe_nvfp4"
@@ -861,8 +874,8 @@ class _HostOnly:
                 x8, rows, what = cfg["x"], 128, "expert 0's gate matrix"
                 self.impl.step_ms = (8,)
                 self.K, self.N, self.bits = 2048, 768, bits
-                codes = "NVFP4" if nvfp4 else f"{bits}-bit"
-                self.desc = f"MoE expert projection, M=8, 128 experts, top-8, {codes} (sampled: expert 0 gate rows)"
+                idx, _ = oracle.topk_softmax(cfg["logits"], cfg["top_k"])
+                self.desc = moe_desc(nvfp4, bits, len(np.unique(idx)))
             self.impl.sample_x = x8
             self.impl.sample_matrix = lambda w=w, rows=rows, what=what: (w, rows, what)
             self.ms = sorted(set(self.impl.step_ms))
