@@ -134,6 +134,17 @@ void set_error(const char* fmt, ...)
     va_end(ap);
 }
 
+// A fingerprint of the calling thread's tuning overrides (they change launch plans).
+uint64_t tune_fingerprint()
+{
+    uint64_t h = 1469598103934665603ull;
+    for (int v : g_tune) {
+        h ^= (uint64_t)(uint32_t)v;
+        h *= 1099511628211ull;
+    }
+    return h;
+}
+
 int device_sms()
 {
     int dev = 0;

@@ -171,6 +171,7 @@ cudaError_t launch_qproj_b4_dual(bool moe, const Plan& plan, const QProjParams& 
 cudaError_t launch_qproj_b8_single(bool moe, const Plan& plan, const QProjParams& p, cudaStream_t stream, bool pdl);
 cudaError_t launch_qproj_b8_dual(bool moe, const Plan& plan, const QProjParams& p, cudaStream_t stream, bool pdl);
 
+uint64_t tune_fingerprint();  // the calling thread's tuning overrides, hashed
 cudaError_t launch_qproj_nvfp4(bool dual, const Plan& plan, const QProjParams& p, cudaStream_t stream, bool pdl);
 cudaError_t launch_qproj_nvfp4_moe(bool dual, const Plan& plan, const QProjParams& p, cudaStream_t stream, bool pdl);
 

@@ -10,7 +10,10 @@
 //   tf_draft_prompt_lookup  the draft of one step (host only)
 //   tf_generate_greedy      the loop: embed the block, one decoder step at M = block
 //                           length, argmax, accept the matching drafts (host-driven,
-//                           synchronises once per step)
+//                           synchronises once per step). The device part of a step
+//                           (embed, ~115 projection launches, argmax) is replayed from a
+//                           CUDA graph kept per thread for the decoder, workspace and
+//                           block length, so a step costs one launch on the host.
 #include <algorithm>
 #include <cstring>
 #include <vector>
@@ -22,6 +25,43 @@ namespace {
 
 constexpr int kArgmaxThreads = 1024;
 constexpr int kMaxDraft = kMaxM - 1;  // the block is the current token plus the drafts
+
+// ---- step graphs: the embed, decoder-step and argmax launches of one block length,
+// captured once and replayed. Keyed by everything the launches bake in: the decoder's
+// descriptors (shapes and pointers), the workspace, the block length, the device and the
+// tuning overrides. A small per-thread cache; the oldest entry is replaced (its
+// executable destroyed). Entries are never freed at thread exit: the CUDA context may
+// already be gone then, and its teardown releases them.
+struct StepGraph {
+    uint64_t key;
+    cudaGraphExec_t exec;
+};
+constexpr int kStepGraphs = 16;
+thread_local StepGraph g_step_graphs[kStepGraphs] = {};
+thread_local int g_step_graph_next = 0;
+thread_local cudaStream_t g_capture_stream[64] = {};
+
+uint64_t fnv_bytes(uint64_t h, const void* p, size_t n)
+{
+    const unsigned char* b = static_cast<const unsigned char*>(p);
+    for (size_t i = 0; i < n; ++i) {
+        h ^= b[i];
+        h *= 1099511628211ull;
+    }
+    return h;
+}
+
+uint64_t step_graph_key(const tf_decoder_desc* d, const void* ws, size_t ws_bytes, int64_t M, int dev)
+{
+    uint64_t h = fnv_bytes(1469598103934665603ull, d, sizeof *d);
+    h = fnv_bytes(h, d->layers, sizeof(tf_decoder_layer) * (size_t)d->n_layers);
+    h = fnv_bytes(h, &ws, sizeof ws);
+    h = fnv_bytes(h, &ws_bytes, sizeof ws_bytes);
+    h = fnv_bytes(h, &M, sizeof M);
+    h = fnv_bytes(h, &dev, sizeof dev);
+    const uint64_t t = tune_fingerprint();
+    return fnv_bytes(h, &t, sizeof t);
+}
 
 // Order-preserving key of a bf16 value (-0 as +0, NaN below every number).
 __device__ __forceinline__ uint32_t bf16_order_key(uint32_t h)
@@ -84,6 +124,53 @@ GenLayout gen_layout(const tf_decoder_desc* d)
     L.step_bytes = tf_decode_step_workspace_bytes(d, kMaxM);
     L.total = L.step_bytes == 0 ? 0 : L.step + L.step_bytes;
     return L;
+}
+
+// The cached graph of one step for (decoder, workspace, M), captured on first use on this
+// thread's capture stream; nullptr when it cannot be had (the capture or the
+// instantiation failed: the caller then launches the step directly, after the error
+// state those calls left has been cleared).
+template <class Enqueue>
+cudaGraphExec_t step_graph(const tf_decoder_desc* d, const void* ws, size_t ws_bytes, int64_t M, Enqueue&& enqueue)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    const uint64_t key = step_graph_key(d, ws, ws_bytes, M, dev);
+    for (const StepGraph& g : g_step_graphs)
+        if (g.exec != nullptr && g.key == key)
+            return g.exec;
+    if (g_capture_stream[dev] == nullptr &&
+        cudaStreamCreateWithFlags(&g_capture_stream[dev], cudaStreamNonBlocking) != cudaSuccess) {
+        g_capture_stream[dev] = nullptr;
+        cudaGetLastError();
+        return nullptr;
+    }
+    cudaStream_t cs = g_capture_stream[dev];
+    if (cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    const int rc = enqueue(cs);
+    cudaGraph_t graph = nullptr;
+    const cudaError_t ce = cudaStreamEndCapture(cs, &graph);
+    cudaGraphExec_t exec = nullptr;
+    if (rc == TF_OK && ce == cudaSuccess && graph != nullptr && cudaGraphInstantiate(&exec, graph, 0) != cudaSuccess)
+        exec = nullptr;
+    if (graph != nullptr)
+        cudaGraphDestroy(graph);
+    cudaGetLastError();
+    if (exec == nullptr)
+        return nullptr;
+    StepGraph& slot = g_step_graphs[g_step_graph_next];
+    g_step_graph_next = (g_step_graph_next + 1) % kStepGraphs;
+    if (slot.exec != nullptr)
+        cudaGraphExecDestroy(slot.exec);
+    slot.key = key;
+    slot.exec = exec;
+    return exec;
 }
 
 }  // namespace
@@ -205,15 +292,26 @@ int tf_generate_greedy(const tf_decoder_desc* d, const int32_t* prompt, int64_t 
             block[i + 1] = draft[i];
         if ((e = cudaMemcpyAsync(ids, block, (size_t)M * sizeof(int32_t), cudaMemcpyHostToDevice, s)) != cudaSuccess)
             return cuda_err(e, "ids to device");
-        if ((e = launch_embed_rows(static_cast<const uint8_t*>(E.data), E.N, E.K, desc_kernel_bits(&E), E.global_scale,
-                                   ids, M, x, E.K, status, s)) != cudaSuccess)
-            return cuda_err(e, "embed");
-        int rc = tf_decode_step_run(d, x, M, logits, wsb + L.step, L.step_bytes, nullptr, 0, stream);
-        if (rc)
+        // the device part of the step: embed, decoder step, argmax
+        auto enqueue = [&](cudaStream_t q) -> int {
+            cudaError_t le = launch_embed_rows(static_cast<const uint8_t*>(E.data), E.N, E.K, desc_kernel_bits(&E),
+                                               E.global_scale, ids, M, x, E.K, status, q);
+            if (le != cudaSuccess)
+                return cuda_err(le, "embed");
+            const int r = tf_decode_step_run(d, x, M, logits, wsb + L.step, L.step_bytes, nullptr, 0, q);
+            if (r)
+                return r;
+            argmax_rows_kernel<<<(unsigned)M, kArgmaxThreads, 0, q>>>(logits, d->vocab, d->vocab, pred);
+            le = cudaGetLastError();
+            return le == cudaSuccess ? TF_OK : cuda_err(le, "argmax");
+        };
+        cudaGraphExec_t exec = step_graph(d, ws, ws_bytes, M, enqueue);
+        if (exec != nullptr) {
+            if ((e = cudaGraphLaunch(exec, s)) != cudaSuccess)
+                return cuda_err(e, "step graph launch");
+        } else if (int rc = enqueue(s)) {
             return rc;
-        argmax_rows_kernel<<<(unsigned)M, kArgmaxThreads, 0, s>>>(logits, d->vocab, d->vocab, pred);
-        if ((e = cudaGetLastError()) != cudaSuccess)
-            return cuda_err(e, "argmax");
+        }
         if ((e = cudaMemcpyAsync(host, pred, (kMaxM + 1) * sizeof(int32_t), cudaMemcpyDeviceToHost, s)) != cudaSuccess)
             return cuda_err(e, "predictions to host");
         if ((e = cudaStreamSynchronize(s)) != cudaSuccess)
