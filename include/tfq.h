@@ -416,6 +416,11 @@ int64_t tf_draft_prompt_lookup(const int32_t* prompt, int64_t prompt_len, const 
  *               NULL): decoder steps run, drafts kept
  *   ws          tf_generate_workspace_bytes(d) bytes, 256-aligned, zeroed once
  * Synchronises `stream` once per step (the predictions decide the next block).
+ * The device part of a step (embed, decoder step, argmax) is captured as a CUDA
+ * graph the first time a (decoder, ws, block length) is seen on the calling thread
+ * and replayed after that; the thread keeps up to 16 such graphs and one capture
+ * stream per device until the CUDA context is destroyed. A step whose graph cannot
+ * be captured or launched is launched directly.
  */
 size_t tf_generate_workspace_bytes(const tf_decoder_desc* d);
 int tf_generate_greedy(const tf_decoder_desc* d, const int32_t* prompt, int64_t prompt_len, int64_t max_new,

@@ -126,6 +126,15 @@ GenLayout gen_layout(const tf_decoder_desc* d)
     return L;
 }
 
+void forget_step_graph(cudaGraphExec_t exec)
+{
+    for (StepGraph& g : g_step_graphs)
+        if (g.exec == exec) {
+            g.exec = nullptr;
+            g.key = 0;
+        }
+}
+
 // The cached graph of one step for (decoder, workspace, M), captured on first use on this
 // thread's capture stream; nullptr when it cannot be had (the capture or the
 // instantiation failed: the caller then launches the step directly, after the error
@@ -151,6 +160,7 @@ cudaGraphExec_t step_graph(const tf_decoder_desc* d, const void* ws, size_t ws_b
     cudaStream_t cs = g_capture_stream[dev];
     if (cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
         cudaGetLastError();
+        g_capture_stream[dev] = nullptr;  // made again next time (the old one may be from a gone context)
         return nullptr;
     }
     const int rc = enqueue(cs);
@@ -306,12 +316,16 @@ int tf_generate_greedy(const tf_decoder_desc* d, const int32_t* prompt, int64_t 
             return le == cudaSuccess ? TF_OK : cuda_err(le, "argmax");
         };
         cudaGraphExec_t exec = step_graph(d, ws, ws_bytes, M, enqueue);
-        if (exec != nullptr) {
-            if ((e = cudaGraphLaunch(exec, s)) != cudaSuccess)
-                return cuda_err(e, "step graph launch");
-        } else if (int rc = enqueue(s)) {
-            return rc;
+        if (exec != nullptr && cudaGraphLaunch(exec, s) != cudaSuccess) {
+            // a cached executable that no longer launches (the context it was made in is
+            // gone): forget it and launch the step directly
+            cudaGetLastError();
+            forget_step_graph(exec);
+            exec = nullptr;
         }
+        if (exec == nullptr)
+            if (int rc = enqueue(s))
+                return rc;
         if ((e = cudaMemcpyAsync(host, pred, (kMaxM + 1) * sizeof(int32_t), cudaMemcpyDeviceToHost, s)) != cudaSuccess)
             return cuda_err(e, "predictions to host");
         if ((e = cudaStreamSynchronize(s)) != cudaSuccess)
