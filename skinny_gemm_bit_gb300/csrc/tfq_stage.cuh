@@ -4,8 +4,9 @@
 //
 //   thread 0        issues the row block's weight copy (one bulk copy per matrix: a row
 //                   block's groups are contiguous in the packed layout) before the kernel
-//                   waits for the previous one (programmatic dependent launch): weights
-//                   never depend on the previous kernel, so they stream during its tail
+//                   waits for the previous one (programmatic dependent launch), and every
+//                   thread loads its chunks of the RMSNorm gamma: weights never depend on
+//                   the previous kernel, so they stream during its tail
 //   all NW warps    stage the activation rows straight from L2 into registers (normalised
 //                   when an RMSNorm is folded in; rotated when an input Hadamard transform
 //                   is), form the per-group sums, then warp w

@@ -112,3 +112,27 @@ def test_greedy_generation_with_drafts_equals_plain_decoding_full_size(T, chain)
         _check_generation(T, _decoder(T, cfg), 24, seed=2)
     finally:
         T.tune_set(T.TF_TUNE_CHAIN, -1)
+
+
+def test_generation_reuses_and_separates_its_step_graphs(T):
+    # a step is replayed from a graph cached per (decoder, workspace, block length): the
+    # same call twice on one workspace (replayed), a second decoder on that workspace
+    # (its own graphs), the first again, and the first on another workspace give the
+    # tokens of a fresh run each time
+    cfg_a = synth.decoder(seed=61, n_layers=2, d_model=256, d_ff=384, n_q_heads=4, n_kv_heads=2, head_dim=64,
+                          vocab=1000, M=1)
+    cfg_b = synth.decoder(seed=62, n_layers=2, d_model=256, d_ff=384, n_q_heads=4, n_kv_heads=2, head_dim=64,
+                          vocab=1000, M=1)
+    dec_a, dec_b = _decoder(T, cfg_a), _decoder(T, cfg_b)
+    ws = T.workspace(T.tf_generate_workspace_bytes(dec_a))
+    prompt = [5, 17, 3, 5, 17]
+    ref_a = T.tf_generate_greedy(dec_a, prompt, 20, max_draft=7, ws=ws)
+    ref_b = T.tf_generate_greedy(dec_b, prompt, 20, max_draft=7, ws=T.workspace(T.tf_generate_workspace_bytes(dec_b)))
+    assert ref_a[0] != ref_b[0]  # two different models
+    assert T.tf_generate_greedy(dec_a, prompt, 20, max_draft=7, ws=ws) == ref_a
+    assert T.tf_generate_greedy(dec_b, prompt, 20, max_draft=7, ws=ws) == ref_b
+    assert T.tf_generate_greedy(dec_a, prompt, 20, max_draft=7, ws=ws) == ref_a
+    ws2 = T.workspace(T.tf_generate_workspace_bytes(dec_a))
+    assert T.tf_generate_greedy(dec_a, prompt, 20, max_draft=7, ws=ws2) == ref_a
+    # plain decoding agrees token by token
+    assert T.tf_generate_greedy(dec_a, prompt, 20, max_draft=0, ws=ws)[0] == ref_a[0]
