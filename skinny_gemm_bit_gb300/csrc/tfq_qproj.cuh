@@ -508,12 +508,42 @@ __device__ __forceinline__ void x_direct_raw(const uint16_t* x, int64_t ldx, int
                     v[m] = (m < Mrows && c < nch)
                                ? __ldcg(reinterpret_cast<const uint4*>(x + (int64_t)m * ldx) + c)
                                : make_uint4(0u, 0u, 0u, 0u);
+                if (Mrows == 1) {  // uniform
+                    const uint32_t vv[4] = {v[0].x, v[0].y, v[0].z, v[0].w};
+                    x_put_chunk(buf, x_rs, xs, 0, c, c < nch, vv);
+                } else {
+                    // each row's partial sums of the chunk, then a butterfly over the 8 lanes
+                    // of the group (4 + 2 + 1 shuffles for all 8 rows, not 3 per row) leaves
+                    // lane l with row (l & 7)'s group sum, added in the same order as the
+                    // per-row reduction of x_put_chunk (so the sums are the same bits)
+                    float a[kMaxM];
 #pragma unroll
-                for (int m = 0; m < kMaxM; ++m) {
-                    if (m >= Mrows)  // uniform
-                        break;
-                    const uint32_t vv[4] = {v[m].x, v[m].y, v[m].z, v[m].w};
-                    x_put_chunk(buf, x_rs, xs, m, c, c < nch, vv);
+                    for (int m = 0; m < kMaxM; ++m) {
+                        const uint32_t vv[4] = {v[m].x, v[m].y, v[m].z, v[m].w};
+                        float part = 0.f;
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            part += bf16lo_f32(vv[q]) + bf16hi_f32(vv[q]);
+                        a[m] = part;
+                        if (m < Mrows && c < nch)
+                            *reinterpret_cast<uint4*>(buf + m * x_rs + c * 16) = v[m];
+                    }
+                    const bool h4 = (lane & 4) != 0, h2 = (lane & 2) != 0, h1 = (lane & 1) != 0;
+                    float b[4], d2[2];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const float r = __shfl_xor_sync(0xffffffffu, h4 ? a[i] : a[i + 4], 4);
+                        b[i] = (h4 ? a[i + 4] : a[i]) + r;
+                    }
+#pragma unroll
+                    for (int i = 0; i < 2; ++i) {
+                        const float r = __shfl_xor_sync(0xffffffffu, h2 ? b[i] : b[i + 2], 2);
+                        d2[i] = (h2 ? b[i + 2] : b[i]) + r;
+                    }
+                    const float r = __shfl_xor_sync(0xffffffffu, h1 ? d2[0] : d2[1], 1);
+                    const float sum = (h1 ? d2[1] : d2[0]) + r;  // group sum of row lane & 7
+                    if (c < nch && (lane & 7) < Mrows)
+                        xs[(c >> 3) * kMaxM + (lane & 7)] = sum;
                 }
             }
         }
