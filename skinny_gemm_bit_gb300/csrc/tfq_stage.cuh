@@ -67,10 +67,9 @@ __device__ __forceinline__ void stage_rows_norm(const uint16_t* x, int64_t ldx, 
             }
         }
         const float inv = rsqrtf(warp_sum((sq[0] + sq[1]) + (sq[2] + sq[3])) / (float)K + eps);
+        float part[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            if (j * 32 >= nch)  // warp-uniform
-                break;
             const int c = j * 32 + lane;
             const uint32_t xv[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
             const uint32_t gg[4] = {gv[j].x, gv[j].y, gv[j].z, gv[j].w};
@@ -79,8 +78,31 @@ __device__ __forceinline__ void stage_rows_norm(const uint16_t* x, int64_t ldx, 
             for (int q = 0; q < 4; ++q)
                 vv[q] = f32x2_to_bf16x2(bf16lo_f32(xv[q]) * inv * bf16lo_f32(gg[q]),
                                         bf16hi_f32(xv[q]) * inv * bf16hi_f32(gg[q]));
-            x_put_chunk(buf, x_rs, xs, m, c, c < nch, vv);
+            float s = 0.f;
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                s += bf16lo_f32(vv[q]) + bf16hi_f32(vv[q]);
+            part[j] = s;
+            if (c < nch)
+                *reinterpret_cast<uint4*>(buf + m * x_rs + c * 16) = make_uint4(vv[0], vv[1], vv[2], vv[3]);
         }
+        // the group sums: lane l holds chunks j 32 + l (j < 4) of four groups; a butterfly
+        // over the 8 lanes of a group (2 + 1 + 1 shuffles for the four, not 3 each) leaves
+        // lanes l and l ^ 1 with the sum for j = 2 bit2(l) + bit1(l), added in the order of
+        // x_put_chunk's reduction (the same bits); the even lane stores it
+        const bool h4 = (lane & 4) != 0, h2 = (lane & 2) != 0;
+        float b[2];
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const float r = __shfl_xor_sync(0xffffffffu, h4 ? part[i] : part[i + 2], 4);
+            b[i] = (h4 ? part[i + 2] : part[i]) + r;
+        }
+        const float r2 = __shfl_xor_sync(0xffffffffu, h2 ? b[0] : b[1], 2);
+        const float cq = (h2 ? b[1] : b[0]) + r2;
+        const float sum = cq + __shfl_xor_sync(0xffffffffu, cq, 1);
+        const int jj = (h4 ? 2 : 0) + (h2 ? 1 : 0), cc = jj * 32 + lane;
+        if ((lane & 1) == 0 && cc < nch)
+            xs[(cc >> 3) * kMaxM + m] = sum;
     }
     named_bar_sync(kBarStage, NW * 32);
 }
