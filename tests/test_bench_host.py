@@ -26,3 +26,13 @@ def test_nvfp4_sample_counts_nvfp4_bytes():
     rows, K = 32, 12800
     per_call = rows * K * (0.5 + 1 / 16)
     assert done % per_call == 0 and "NVFP4" in host.desc
+
+
+def test_reference_arm_names_the_gpu_arms_workloads():
+    # both arms print the same config["workload"], so their lines describe one config
+    assert bench._HostOnly("step").desc == bench.STEP_DESC
+    assert bench._HostOnly("gateup").desc == bench.gateup_desc(1024, 3072)
+    for name, (K, N, ms) in {"proj": (1024, 3072, (1,)), "wide": (12800, 2560, (1, 8)),
+                             "wide_nvfp4": (12800, 2560, (1, 8))}.items():
+        assert bench._HostOnly(name).desc == bench.proj_desc(name, K, N, ms)
+    assert bench._HostOnly("moe4").desc == bench.moe_desc(False, 4, 56)
